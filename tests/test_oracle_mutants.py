@@ -1,0 +1,46 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU, in a
+temporary directory), builds it, and runs the pin suite against the broken build in a
+child process: the suite must fail.  The real oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "attn_oracle.c")
+
+MUTANTS = {
+    "causal_off_by_one": ("if (causal && j > q_pos) return 0;", "if (causal && j >= q_pos) return 0;"),
+    "window_off_by_one": ("j < q_pos - window + 1", "j < q_pos - window"),
+    "gqa_modulo_map": ("return h / (hq / hkv);", "return h % hkv;"),
+    "scale_dropped": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "max_dropped_from_lse": ("return m + log(l);", "return log(l);"),
+    "no_normalisation": ("p[j] = p[j] / l;", "p[j] = p[j];"),
+    "top_left_alignment": ("return i + (skv - sq);", "return i;"),
+    "pv_reads_k": ("oracle_pv(p, v, skv, d, o);", "oracle_pv(p, k, skv, d, o);"),
+    "page_slot_swapped": ("(size_t)(j % page)) * d", "(size_t)(j / page % page)) * d"),
+    "tril_strict": ("(uint8_t)(u <= t)", "(uint8_t)(u < t)"),
+    "decode_qpos_drops_t": ("qp[t] = len - s_active + t;", "qp[t] = len - s_active;"),
+    "exp_sign_flipped": ("exp(s[j] - m)", "exp(m - s[j])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(lib), str(mutant), "-lm"],
+                   check=True)
+    env = dict(os.environ, ATTN_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

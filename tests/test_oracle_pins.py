@@ -1,0 +1,317 @@
+"""Pins of the fp64 oracle to facts outside itself.
+
+Each test ties the oracle to something the pages or the mathematics fix: hand-worked
+golden cases, closed forms, invariants of the softmax, an independent library routine
+(PyTorch's scaled_dot_product_attention in float64, scipy's logsumexp), and brute-force
+cross-mode identities.  Together they are chosen so that a dropped term, a wrong sign,
+a wrong index, a wrong head map or a transposed operand fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import rng
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tiny_cases.json")
+
+
+def bits(x):
+    """float values that are exact in bf16 -> bf16 bit patterns."""
+    b = rng.f32_to_bf16_bits_np(np.asarray(x, dtype=np.float32))
+    assert np.array_equal(rng.bf16_bits_to_f32_np(b), np.asarray(x, dtype=np.float32))
+    return b
+
+
+def rand_bits(seed, shape, name="x"):
+    n = int(np.prod(shape))
+    return rng.normal_bf16_np(rng.stream_seed(seed, name), 0, n).reshape(shape)
+
+
+def f64(b):
+    return rng.bf16_bits_to_f32_np(b).astype(np.float64)
+
+
+def frac_arr(a):
+    return np.vectorize(lambda nd: float(Fraction(nd[0], nd[1])), signature="(n)->()")(np.asarray(a))
+
+
+def load_golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+# ----------------------------------------------------------------------------- golden
+@pytest.mark.parametrize("case", load_golden()["prefill"], ids=lambda c: c["name"])
+def test_golden_prefill(case):
+    q = bits(case["q"])[None]
+    k = bits(case["k"])[None]
+    v = bits(case["v"])[None]
+    o, lse = oracle.prefill(q, k, v, math.log(case["scale_exp"]), case["causal"], case["window"])
+    np.testing.assert_allclose(o[0], frac_arr(case["o"]), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[0], np.log(np.asarray(case["lse_exp"], dtype=np.float64)),
+                               rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("case", load_golden()["decode"], ids=lambda c: c["name"])
+def test_golden_decode_paged(case):
+    page, n = case["page"], case["cache_len"]
+    lk, lv = bits(case["logical_k"]), bits(case["logical_v"])
+    table = np.asarray([case["block_table"]], dtype=np.uint32)
+    npages = len(case["block_table"])
+    kc = np.full((npages, 1, page, case["d"]), rng.BF16_NAN_BITS, dtype=np.uint16)
+    vc = kc.copy()
+    for j in range(n):
+        kc[table[0, j // page], 0, j % page] = lk[j]
+        vc[table[0, j // page], 0, j % page] = lv[j]
+    q = bits(case["q"])[None]
+    o, lse = oracle.decode(q, kc, vc, table, np.array([n], dtype=np.int32),
+                           math.log(case["scale_exp"]))
+    np.testing.assert_allclose(o[0, 0], frac_arr(case["o"]), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[0, 0], np.log(np.asarray(case["lse_exp"], float)), atol=1e-13)
+    m = oracle.decode_mask(np.array([n], np.int32), 1, case["s_active"], case["mask_max_len"])
+    np.testing.assert_array_equal(m[0, 0], np.asarray(case["mask"], dtype=np.uint8))
+
+
+# ----------------------------------------------------------------------------- invariants
+@pytest.mark.parametrize("causal,window,sq,skv", [(0, 0, 40, 56), (1, 0, 48, 48), (1, 7, 40, 56),
+                                                  (1, 0, 60, 20)])
+def test_rows_of_p_sum_to_one_and_masked_p_is_zero(causal, window, sq, skv):
+    d = 16
+    q, k, v = rand_bits(1, (sq, d), "q"), rand_bits(1, (skv, d), "k"), rand_bits(1, (skv, d), "v")
+    qp = np.array([oracle.q_pos(i, sq, skv) for i in range(sq)])
+    o, lse, p = oracle.attention_rows(q, k, v, qp, 0.3, causal, window, want_p=True)
+    for r in range(sq):
+        allowed = np.array([oracle.allowed(j, skv, qp[r], causal, window) for j in range(skv)])
+        if allowed.any():
+            assert abs(p[r].sum() - 1.0) < 1e-12
+            assert (p[r][allowed] > 0).all()
+            np.testing.assert_allclose(o[r], p[r] @ f64(v), atol=1e-12)
+        else:  # fully masked row (queries before the first key): O = 0, LSE = -inf
+            assert lse[r] == -np.inf and (o[r] == 0).all()
+        assert (p[r][~allowed] == 0.0).all()
+
+
+def test_allowed_predicate_counts_by_hand():
+    # sq = skv = 6, causal, window 3: row i sees keys max(0, i-2) .. i -> 1, 2, 3, 3, 3, 3
+    counts = [sum(oracle.allowed(j, 6, i, 1, 3) for j in range(6)) for i in range(6)]
+    assert counts == [1, 2, 3, 3, 3, 3]
+    # causal only: row i sees i + 1 keys
+    assert [sum(oracle.allowed(j, 6, i, 1, 0) for j in range(6)) for i in range(6)] == [1, 2, 3, 4, 5, 6]
+    # queries at the tail: 2 queries after 5 keys sit at positions 3 and 4
+    assert [oracle.q_pos(i, 2, 5) for i in range(2)] == [3, 4]
+    # keys at or past skv are never allowed
+    assert not oracle.allowed(5, 5, 9, 0, 0) and not oracle.allowed(-1, 5, 3, 0, 0)
+
+
+def test_gqa_head_map_by_hand():
+    assert [oracle.kv_head(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    assert [oracle.kv_head(h, 6, 3) for h in range(6)] == [0, 0, 1, 1, 2, 2]
+    assert [oracle.kv_head(h, 4, 4) for h in range(4)] == [0, 1, 2, 3]
+
+
+def test_constant_v_gives_that_constant():
+    sq, skv, d = 24, 40, 8
+    q, k = rand_bits(2, (1, 1, sq, d), "q"), rand_bits(2, (1, 1, skv, d), "k")
+    c = np.array([0.75, -2.0, 3.5, 0.0, 1.0, -0.125, 8.0, 0.5], dtype=np.float32)
+    v = np.broadcast_to(bits(c), (1, 1, skv, d)).copy()
+    for causal, window in [(0, 0), (1, 0), (1, 5)]:
+        o, _ = oracle.prefill(q, k, v, 0.7, causal, window)
+        np.testing.assert_allclose(o[0, 0], np.broadcast_to(c, (sq, d)), rtol=0, atol=1e-12)
+
+
+def test_single_allowed_key_gives_its_v_row_and_score():
+    # window 1 with causal: each row sees only its own position
+    sq = skv = 20
+    d = 8
+    q, k, v = (rand_bits(3, (1, 1, sq, d), n) for n in "qkv")
+    scale = 0.37
+    o, lse = oracle.prefill(q, k, v, scale, 1, 1)
+    np.testing.assert_array_equal(o[0, 0], f64(v[0, 0]))
+    s_diag = scale * np.einsum("ix,ix->i", f64(q[0, 0]), f64(k[0, 0]))
+    np.testing.assert_allclose(lse[0, 0], s_diag, atol=1e-12)
+
+
+def test_first_causal_row_is_v0():
+    q, k, v = (rand_bits(4, (1, 2, 16, 8), n) for n in "qkv")
+    o, _ = oracle.prefill(q, k, v, 0.5, 1, 0)
+    np.testing.assert_array_equal(o[0, :, 0], f64(v[0, :, 0]))
+
+
+@pytest.mark.parametrize("causal,window,sq,skv,counts", [
+    (1, 3, 6, 6, [1, 2, 3, 3, 3, 3]),
+    (1, 3, 4, 6, [3, 3, 3, 3]),
+    (1, 0, 3, 5, [3, 4, 5]),
+    (0, 0, 3, 5, [5, 5, 5]),
+])
+def test_zero_q_gives_mean_of_allowed_v_and_log_count(causal, window, sq, skv, counts):
+    d = 4
+    q = np.zeros((1, 1, sq, d), dtype=np.uint16)
+    k, v = rand_bits(5, (1, 1, skv, d), "k"), rand_bits(5, (1, 1, skv, d), "v")
+    o, lse = oracle.prefill(q, k, v, 1.0, causal, window)
+    vf = f64(v[0, 0])
+    for i, c in enumerate(counts):
+        last = i + skv - sq  # the row's own position: the newest allowed key when causal
+        hi = last if causal else skv - 1
+        np.testing.assert_allclose(o[0, 0, i], vf[hi - c + 1: hi + 1].mean(0), atol=1e-12)
+        assert abs(lse[0, 0, i] - math.log(c)) < 1e-12
+
+
+def test_changing_masked_kv_changes_nothing():
+    sq = skv = 32
+    d = 8
+    q, k, v = (rand_bits(6, (1, 1, sq, d), n) for n in "qkv")
+    o1, l1 = oracle.prefill(q, k, v, 0.4, 1, 9)
+    # rows 20..31 never see keys < 11 (window 9) nor keys after themselves
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 0, :11] = rand_bits(7, (11, d), "k")
+    v2[0, 0, :11] = rng.BF16_NAN_BITS
+    o2, l2 = oracle.prefill(q, k2, v2, 0.4, 1, 9)
+    np.testing.assert_array_equal(o1[0, 0, 20:], o2[0, 0, 20:])
+    np.testing.assert_array_equal(l1[0, 0, 20:], l2[0, 0, 20:])
+    assert not np.array_equal(o1[0, 0, :20], o2[0, 0, :20])
+
+
+def test_noncausal_key_permutation_invariance():
+    sq, skv, d = 12, 50, 8
+    q, k, v = (rand_bits(8, (1, 1, n_, d), n) for n_, n in ((sq, "q"), (skv, "k"), (skv, "v")))
+    perm = np.argsort(rng.u64_np(99, 0, skv), kind="stable")
+    o1, l1 = oracle.prefill(q, k, v, 0.6, 0, 0)
+    o2, l2 = oracle.prefill(q, k[:, :, perm], v[:, :, perm], 0.6, 0, 0)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+    # a causal mask is not permutation invariant: the same permutation must change it
+    o3, _ = oracle.prefill(q, k, v, 0.6, 1, 0)
+    o4, _ = oracle.prefill(q, k[:, :, perm], v[:, :, perm], 0.6, 1, 0)
+    assert not np.allclose(o3, o4)
+
+
+def test_gqa_equals_mha_with_repeated_kv():
+    b, hq, hkv, s, d = 2, 6, 2, 20, 8
+    q = rand_bits(9, (b, hq, s, d), "q")
+    k, v = rand_bits(9, (b, hkv, s, d), "k"), rand_bits(9, (b, hkv, s, d), "v")
+    o1, l1 = oracle.prefill(q, k, v, 0.3, 1, 0)
+    rep = hq // hkv
+    o2, l2 = oracle.prefill(q, np.repeat(k, rep, axis=1), np.repeat(v, rep, axis=1), 0.3, 1, 0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+# ----------------------------------------------------------------------------- library routines
+def test_matches_torch_sdpa_float64():
+    """PyTorch's scaled_dot_product_attention (float64, CPU) is an independent implementation
+    of the same definition: its own causal triangle and its own GQA expansion."""
+    import torch
+    import torch.nn.functional as F
+
+    b, hq, hkv, s, d = 2, 8, 2, 70, 32
+    q = rand_bits(10, (b, hq, s, d), "q")
+    k, v = rand_bits(10, (b, hkv, s, d), "k"), rand_bits(10, (b, hkv, s, d), "v")
+    t = lambda a: torch.from_numpy(f64(a))
+    scale = 1 / math.sqrt(d)
+    for causal in (0, 1):
+        o, _ = oracle.prefill(q, k, v, scale, causal, 0)
+        ref = F.scaled_dot_product_attention(t(q), t(k).repeat_interleave(hq // hkv, 1),
+                                             t(v).repeat_interleave(hq // hkv, 1),
+                                             is_causal=bool(causal), scale=scale)
+        np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_lse_matches_scipy_logsumexp():
+    from scipy.special import logsumexp
+
+    sq, skv, d = 10, 33, 16
+    q, k, v = (rand_bits(11, (1, 1, n_, d), n) for n_, n in ((sq, "q"), (skv, "k"), (skv, "v")))
+    _, lse = oracle.prefill(q, k, v, 0.25, 0, 0)
+    s = 0.25 * f64(q[0, 0]) @ f64(k[0, 0]).T
+    np.testing.assert_allclose(lse[0, 0], logsumexp(s, axis=1), atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- decode
+def _flat_and_paged(seed, b, hkv, d, lens, page, permute):
+    max_len = int(max(lens))
+    flat_k = np.full((b, hkv, max_len, d), rng.BF16_NAN_BITS, dtype=np.uint16)
+    flat_v = flat_k.copy()
+    for i, n in enumerate(lens):
+        flat_k[i, :, :n] = rand_bits(seed + i, (hkv, n, d), "k")
+        flat_v[i, :, :n] = rand_bits(seed + i, (hkv, n, d), "v")
+    npg = [-(-n // page) for n in lens]
+    total = sum(npg)
+    phys = (np.argsort(rng.u64_np(seed, 0, total), kind="stable") if permute
+            else np.arange(total)).astype(np.uint32)
+    maxp = -(-max_len // page)
+    table = np.full((b, maxp), 0xFFFFFFFF, dtype=np.uint32)
+    kc = np.full((total, hkv, page, d), rng.BF16_NAN_BITS, dtype=np.uint16)
+    vc = kc.copy()
+    off = 0
+    for i, n in enumerate(lens):
+        table[i, : npg[i]] = phys[off: off + npg[i]]
+        off += npg[i]
+        for j in range(n):
+            kc[table[i, j // page], :, j % page] = flat_k[i, :, j]
+            vc[table[i, j // page], :, j % page] = flat_v[i, :, j]
+    return flat_k, flat_v, kc, vc, table
+
+
+def test_decode_equals_last_rows_of_causal_prefill():
+    hq, hkv, d, n, sa = 4, 2, 16, 45, 3
+    fk, fv, _, _, _ = _flat_and_paged(20, 1, hkv, d, [n], 8, False)
+    q = rand_bits(21, (1, hq, sa, d), "q")
+    o_dec, l_dec = oracle.decode(q, fk, fv, None, np.array([n], np.int32), 0.2)
+    # prefill with sq = s_active queries at the tail of n keys
+    o_pre, l_pre = oracle.prefill(q, fk[:, :, :n], fv[:, :, :n], 0.2, 1, 0)
+    np.testing.assert_array_equal(o_dec, o_pre)
+    np.testing.assert_array_equal(l_dec, l_pre)
+
+
+def test_decode_paged_permuted_equals_identity_equals_flat():
+    b, hq, hkv, d, page, sa = 3, 4, 2, 8, 4, 2
+    lens = [9, 16, 5]
+    q = rand_bits(30, (b, hq, sa, d), "q")
+    cl = np.array(lens, np.int32)
+    fk, fv, kc, vc, table = _flat_and_paged(31, b, hkv, d, lens, page, True)
+    _, _, kc2, vc2, table2 = _flat_and_paged(31, b, hkv, d, lens, page, False)
+    assert not np.array_equal(table, table2)
+    o1, l1 = oracle.decode(q, kc, vc, table, cl, 0.3)
+    o2, l2 = oracle.decode(q, kc2, vc2, table2, cl, 0.3)
+    o3, l3 = oracle.decode(q, fk, fv, None, cl, 0.3)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(o1, o3)
+    np.testing.assert_array_equal(l1, l3)
+    assert np.isfinite(o1).all()  # NaN padding slots never leak
+
+
+def test_decode_single_cached_key():
+    d = 8
+    fk, fv, _, _, _ = _flat_and_paged(40, 1, 1, d, [1], 4, False)
+    q = rand_bits(41, (1, 2, 1, d), "q")
+    o, lse = oracle.decode(q, fk, fv, None, np.array([1], np.int32), 0.5)
+    np.testing.assert_array_equal(o[0, :, 0], np.broadcast_to(f64(fv[0, 0, 0]), (2, d)))
+    np.testing.assert_allclose(lse[0, :, 0], 0.5 * f64(q[0, :, 0]) @ f64(fk[0, 0, 0]), atol=1e-12)
+
+
+def test_gather_rejects_out_of_range_page():
+    cache = np.zeros((2, 1, 4, 2), np.uint16)
+    with pytest.raises(RuntimeError, match="page index"):
+        oracle.gather_paged(cache, np.array([0, 2], np.uint32), 2, 0, 6)
+
+
+def test_decode_mask_structure():
+    lens = np.array([5, 9, 4], np.int32)
+    sa, max_len = 4, 12
+    m = oracle.decode_mask(lens, 2, sa, max_len)
+    for b, n in enumerate(lens):
+        for t in range(sa):
+            # each query row sees exactly the prefix up to its own position
+            assert m[b, 0, t].sum() == n - sa + t + 1
+            assert (m[b, 0, t, n:] == 0).all()
+        # the new tokens' block is tril(ones) and the prior block is all ones
+        np.testing.assert_array_equal(m[b, 1, :, n - sa: n], np.tril(np.ones((sa, sa), np.uint8)))
+        assert (m[b, 1, :, : n - sa] == 1).all()
+    # one new token: the mask is exactly the length cut (type A)
+    m1 = oracle.decode_mask(lens, 1, 1, max_len)
+    np.testing.assert_array_equal(m1[:, 0, 0], (np.arange(max_len)[None] < lens[:, None]))
