@@ -1,0 +1,227 @@
+"""Python binding of the GB300 attention-forward C ABI (``include/attn.h``).
+
+The functions here carry the same names as the C entry points and only marshal
+arguments: they check tensor dtypes, devices and shapes, allocate outputs the caller
+did not pass, and hand raw device pointers and the current CUDA stream to
+``libattn_gb300.so``.  Every step of the computation runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "AttnError", "ATTN_BF16", "ATTN_F32", "library_path", "load_library",
+    "attn_fwd_prefill", "attn_fwd_decode", "attn_decode_workspace_bytes",
+    "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
+]
+
+ATTN_BF16, ATTN_F32 = 0, 1
+_STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+           4: "ATTN_ERR_PAGE_OOB", 5: "ATTN_ERR_DEVICE_TIMEOUT", 6: "ATTN_ERR_WORKSPACE",
+           7: "ATTN_ERR_CACHE_LEN"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    from . import _build
+
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False):
+    """Load libattn_gb300.so (building it first only if asked).  Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if build_if_missing:
+            from . import _build
+
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(the attention path has no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P]
+        lib.attn_fwd_prefill.restype = I
+        lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        lib.attn_decode_workspace_bytes.restype = S
+        lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, I, I, P,
+                                        S, P]
+        lib.attn_fwd_decode.restype = I
+        lib.attn_gen_mask_decode.argtypes = [P, I, I, I, I, P, P]
+        lib.attn_gen_mask_decode.restype = I
+        lib.attn_get_device_error.argtypes = [P]
+        lib.attn_get_device_error.restype = I
+        lib.attn_status_string.argtypes = [I]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise AttnError(status, where)
+
+
+def _stream_ptr(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _req(t, name, dtype, device=None):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dtype_code(dtype):
+    import torch
+
+    if dtype == torch.bfloat16:
+        return ATTN_BF16
+    if dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError("output dtype must be torch.bfloat16 or torch.float32")
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device error status."""
+    return load_library().attn_get_device_error(_stream_ptr(stream))
+
+
+def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
+                     o=None, lse=None, o_dtype=None, stream=None):
+    """O, LSE of softmax(scale Q K^T + mask) V.  q [b,hq,sq,d], k/v [b,hkv,skv,d] bf16."""
+    import torch
+
+    lib = load_library()
+    _req(q, "q", torch.bfloat16)
+    _req(k, "k", torch.bfloat16, q.device)
+    _req(v, "v", torch.bfloat16, q.device)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [b,hq,sq,d]; k and v [b,hkv,skv,d] with equal shapes")
+    b, hq, sq, d = q.shape
+    _, hkv, skv, dk = k.shape
+    if k.shape[0] != b or dk != d:
+        raise ValueError("q and k disagree on batch or head_dim")
+    if o is None:
+        o = torch.empty((b, hq, sq, d), dtype=o_dtype or torch.bfloat16, device=q.device)
+    _req(o, "o", o.dtype, q.device)
+    if tuple(o.shape) != (b, hq, sq, d):
+        raise ValueError("o has the wrong shape")
+    if lse is not None:
+        _req(lse, "lse", torch.float32, q.device)
+        if tuple(lse.shape) != (b, hq, sq):
+            raise ValueError("lse must be [b,hq,sq]")
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(lib.attn_fwd_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, hq, hkv, sq,
+                                skv, d, sc, int(bool(causal)), int(window), _dtype_code(o.dtype),
+                                _stream_ptr(stream)), "attn_fwd_prefill")
+    return o, lse
+
+
+def attn_decode_workspace_bytes(b: int, hq: int, s_active: int, d: int, max_cache_len: int,
+                                kv_chunk: int = 0) -> int:
+    return int(load_library().attn_decode_workspace_bytes(b, hq, s_active, d, max_cache_len,
+                                                           kv_chunk))
+
+
+def attn_fwd_decode(q, k_cache, v_cache, block_table, cache_len, *, max_cache_len: int,
+                    scale: float | None = None, o=None, lse=None, o_dtype=None, kv_chunk: int = 0,
+                    workspace=None, stream=None):
+    """Decode attention.  q [b,hq,s_active,d] bf16; paged caches [num_pages,hkv,page,d] with
+    block_table int32/uint32-bits [b,max_pages], or flat caches [b,hkv,max_cache_len,d] with
+    block_table None; cache_len int32 [b]."""
+    import torch
+
+    lib = load_library()
+    _req(q, "q", torch.bfloat16)
+    dev = q.device
+    _req(k_cache, "k_cache", torch.bfloat16, dev)
+    _req(v_cache, "v_cache", torch.bfloat16, dev)
+    _req(cache_len, "cache_len", torch.int32, dev)
+    if v_cache.shape != k_cache.shape or q.dim() != 4 or k_cache.dim() != 4:
+        raise ValueError("bad q / cache shapes")
+    b, hq, s_active, d = q.shape
+    if block_table is not None:
+        _req(block_table, "block_table", block_table.dtype, dev)
+        if block_table.dtype not in (torch.int32, torch.uint32):
+            raise TypeError("block_table must hold 32-bit entries (uint32 bit patterns)")
+        if block_table.dim() != 2 or block_table.shape[0] != b:
+            raise ValueError("block_table must be [b, max_pages_per_seq]")
+        num_pages, hkv, page, dk = k_cache.shape
+        max_pages = block_table.shape[1]
+    else:
+        bb, hkv, ml, dk = k_cache.shape
+        if bb != b or ml != max_cache_len:
+            raise ValueError("a flat cache must be [b, hkv, max_cache_len, d]")
+        num_pages, page, max_pages = 0, 0, 0
+    if dk != d or cache_len.shape != (b,):
+        raise ValueError("head_dim or cache_len shape mismatch")
+    if o is None:
+        o = torch.empty((b, hq, s_active, d), dtype=o_dtype or torch.bfloat16, device=dev)
+    _req(o, "o", o.dtype, dev)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, dev)
+    need = attn_decode_workspace_bytes(b, hq, s_active, d, max_cache_len, kv_chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _req(workspace, "workspace", torch.uint8, dev)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(lib.attn_fwd_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                               _ptr(cache_len), b, hq, hkv, d, s_active, page, max_pages,
+                               num_pages, max_cache_len, sc, _ptr(o), _ptr(lse),
+                               _dtype_code(o.dtype), kv_chunk, _ptr(workspace),
+                               workspace.numel(), _stream_ptr(stream)), "attn_fwd_decode")
+    return o, lse
+
+
+def attn_gen_mask_decode(cache_len, hq: int, s_active: int, max_len: int, mask=None,
+                         stream=None):
+    """uint8 [b, hq, s_active, max_len] 0/1 decode mask."""
+    import torch
+
+    lib = load_library()
+    _req(cache_len, "cache_len", torch.int32)
+    b = cache_len.shape[0]
+    if mask is None:
+        mask = torch.empty((b, hq, s_active, max_len), dtype=torch.uint8, device=cache_len.device)
+    _req(mask, "mask", torch.uint8, cache_len.device)
+    _check(lib.attn_gen_mask_decode(_ptr(cache_len), b, hq, s_active, max_len, _ptr(mask),
+                                    _stream_ptr(stream)), "attn_gen_mask_decode")
+    return mask

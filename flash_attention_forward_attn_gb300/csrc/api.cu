@@ -1,0 +1,189 @@
+// api.cu -- the extern "C" entry points of attn.h: host-side argument checks, workspace
+// carving, and dispatch to the kernel translation units.  Nothing here allocates device
+// memory or touches tensor contents.
+#include <math.h>
+#include <stdio.h>
+
+#include "attn_internal.h"
+
+namespace attn {
+
+TensorMapEncodeFn tensor_map_encoder() {
+    static TensorMapEncodeFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<TensorMapEncodeFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box) {
+    TensorMapEncodeFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t d[3], s[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d,
+               s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace attn
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+int resolve_chunk(int kv_chunk) { return kv_chunk == 0 ? attn::kDefaultKvChunk : kv_chunk; }
+
+// Split-KV scratch: partial outputs [rows][max_splits][d] fp32, then (m, l) pairs.
+bool decode_scratch_sizes(int b, int hq, int s_active, int d, int max_cache_len, int kv_chunk,
+                          size_t* o_bytes, size_t* ml_bytes, int* max_splits) {
+    if (b <= 0 || hq <= 0 || s_active <= 0 || !head_dim_ok(d) || max_cache_len <= 0) return false;
+    if (kv_chunk < 0 || (kv_chunk % 32) != 0) return false;
+    const int chunk = resolve_chunk(kv_chunk);
+    const long long splits = (max_cache_len + (long long)chunk - 1) / chunk;
+    const long long rows = (long long)b * hq * s_active;
+    *max_splits = (int)splits;
+    *o_bytes = (size_t)(rows * splits * d * 4);
+    *o_bytes = (*o_bytes + 255) & ~(size_t)255;
+    *ml_bytes = (size_t)(rows * splits * 2 * 4);
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_PAGE_OOB: return "ATTN_ERR_PAGE_OOB";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+        case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+        case ATTN_ERR_CACHE_LEN: return "ATTN_ERR_CACHE_LEN";
+    }
+    return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int b, int hq, int hkv, int sq, int skv, int d, float scale,
+                             int causal, int window, attn_dtype o_dtype, void* stream) {
+    if (b <= 0 || hq <= 0 || hkv <= 0 || sq < 0 || skv < 0 || window < 0) return ATTN_ERR_INVALID_ARG;
+    if (hq % hkv != 0 || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
+    if (window > 0 && !causal) return ATTN_ERR_UNSUPPORTED;  // the window is chained after causal
+    if (sq == 0) return ATTN_OK;
+    if (!q || !o || (skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || (skv > 0 && (!aligned16(k) || !aligned16(v))))
+        return ATTN_ERR_INVALID_ARG;
+    if ((long long)b * hq > 0x7fffffffLL || (long long)b * hkv > 0x7fffffffLL)
+        return ATTN_ERR_UNSUPPORTED;
+    attn::PrefillArgs a{q, k, v, o, lse, b, hq, hkv, sq, skv, d, scale, causal ? 1 : 0, window,
+                        o_dtype};
+    return attn::prefill_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_cache_len,
+                                   int kv_chunk) {
+    size_t ob, mlb;
+    int ms;
+    if (!decode_scratch_sizes(b, hq, s_active, d, max_cache_len, kv_chunk, &ob, &mlb, &ms)) return 0;
+    return ob + mlb;
+}
+
+attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const uint32_t* block_table, const int32_t* cache_len, int b, int hq,
+                            int hkv, int d, int s_active, int page_size, int max_pages_per_seq,
+                            int num_pages, int max_cache_len, float scale, void* o, float* lse,
+                            attn_dtype o_dtype, int kv_chunk, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if (b <= 0 || hq <= 0 || hkv <= 0 || s_active <= 0 || max_cache_len <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (hq % hkv != 0 || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+    if (kv_chunk < 0 || kv_chunk % 32 != 0) return ATTN_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !cache_len || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+        return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
+    if ((hq / hkv) * (long long)s_active > 16) return ATTN_ERR_UNSUPPORTED;
+    if (block_table) {
+        if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0)
+            return ATTN_ERR_INVALID_ARG;
+        if (num_pages <= 0 || max_pages_per_seq <= 0) return ATTN_ERR_INVALID_ARG;
+        if ((long long)max_pages_per_seq * page_size < max_cache_len) return ATTN_ERR_INVALID_ARG;
+        if ((long long)num_pages * hkv * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    } else if ((long long)b * hkv * max_cache_len > 0x7fffffffLL) {
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    size_t ob, mlb;
+    int max_splits;
+    if (!decode_scratch_sizes(b, hq, s_active, d, max_cache_len, kv_chunk, &ob, &mlb, &max_splits))
+        return ATTN_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < ob + mlb) return ATTN_ERR_WORKSPACE;
+    attn::DecodeArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.cache_len = cache_len;
+    a.b = b;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.d = d;
+    a.s_active = s_active;
+    a.page_size = page_size;
+    a.max_pages_per_seq = max_pages_per_seq;
+    a.num_pages = num_pages;
+    a.max_cache_len = max_cache_len;
+    a.scale = scale;
+    a.o = o;
+    a.lse = lse;
+    a.o_dtype = o_dtype;
+    a.kv_chunk = resolve_chunk(kv_chunk);
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ob);
+    a.max_splits = max_splits;
+    return attn::decode_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_gen_mask_decode(const int32_t* cache_len, int b, int hq, int s_active,
+                                 int max_len, uint8_t* mask_out, void* stream) {
+    if (b <= 0 || hq <= 0 || s_active <= 0 || max_len <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!cache_len || !mask_out) return ATTN_ERR_INVALID_ARG;
+    return attn::gen_mask_launch(cache_len, b, hq, s_active, max_len, mask_out,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_get_device_error(void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
+    const unsigned bits = attn::prefill_take_error(st, &e1) | attn::decode_take_error(st, &e2);
+    if (e1 != cudaSuccess || e2 != cudaSuccess) return ATTN_ERR_CUDA;
+    if (bits & attn::kDevErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
+    if (bits & attn::kDevErrPageOOB) return ATTN_ERR_PAGE_OOB;
+    if (bits & attn::kDevErrCacheLen) return ATTN_ERR_CACHE_LEN;
+    return ATTN_OK;
+}
+
+}  // extern "C"

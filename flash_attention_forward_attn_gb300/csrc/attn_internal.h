@@ -1,0 +1,73 @@
+// attn_internal.h -- host-side interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Arguments reaching these functions are already validated.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Bits of the per-translation-unit device error words (read and cleared by the host).
+enum : unsigned {
+    kDevErrPageOOB = 1u,   // a page-table entry >= num_pages was met (page not read)
+    kDevErrTimeout = 2u,   // a pipeline wait ran past its limit (kernel gave up)
+    kDevErrCacheLen = 4u,  // a cache_len outside [s_active, max_cache_len] (sequence skipped)
+};
+
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    int b, hq, hkv, sq, skv, d;
+    float scale;
+    int causal, window;
+    attn_dtype o_dtype;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const uint32_t* block_table;  // NULL for a flat cache
+    const int32_t* cache_len;
+    int b, hq, hkv, d, s_active, page_size, max_pages_per_seq, num_pages, max_cache_len;
+    float scale;
+    void* o;
+    float* lse;
+    attn_dtype o_dtype;
+    int kv_chunk;         // resolved (> 0)
+    float* part_o;        // [b*hq*s_active][max_splits][d]
+    float* part_ml;       // [b*hq*s_active][max_splits][2]
+    int max_splits;
+};
+
+// Tokens per split when the caller passes kv_chunk = 0.
+constexpr int kDefaultKvChunk = 1024;
+
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link against libcuda).
+typedef CUresult (*TensorMapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                      const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                      const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                      CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+TensorMapEncodeFn tensor_map_encoder();
+
+// bf16 tensor map of rank 2 or 3 (innermost dim first), 128-byte swizzle, zero OOB fill.
+bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box);
+
+attn_status prefill_launch(const PrefillArgs& a, cudaStream_t stream);
+attn_status decode_launch(const DecodeArgs& a, cudaStream_t stream);
+attn_status gen_mask_launch(const int32_t* cache_len, int b, int hq, int s_active, int max_len,
+                            uint8_t* mask, cudaStream_t stream);
+
+// Read and clear each translation unit's device error word (bits of attn::kDevErr*).
+unsigned prefill_take_error(cudaStream_t stream, cudaError_t* err);
+unsigned decode_take_error(cudaStream_t stream, cudaError_t* err);
+
+}  // namespace attn

@@ -1,0 +1,488 @@
+// decode_sm103.cu -- memory-bound decode attention over a flat or paged bf16 KV cache.
+//
+// Method ("Flash-Attention: Decode (TKG)"): s_active new tokens per sequence attend the
+// whole cache; the q-head group of one kv head is flattened into one tile of
+// group * s_active <= 16 rows ("GQA / MQA grouped-query broadcast"), so every K/V byte
+// is read once per kv head.  The cache axis is split into chunks of kv_chunk tokens,
+// each chunk keeping its own running max m, sum l and unnormalised output (the online
+// softmax recurrence of "Flash-Attention: Context (CTE)", "The online-softmax
+// recurrence"); a second kernel merges the chunks by log-sum-exp, i.e. the deferred
+// normalise of the TKG flash path.
+//
+// GB300 design: one CTA per (chunk, kv head, sequence).  One producer thread streams
+// 32-token K and V tiles with TMA (128-byte swizzle) into a 4-slot shared-memory ring
+// under mbarriers, fetching each page through the block table ("Paged / block cache");
+// four consumer warps take alternate tiles, each with its own (m, l, O) state, and
+// merge through shared memory at the end.  The 16-row contractions run on the warp
+// MMA (m16n8k16, bf16 in, fp32 accumulate): with 16 rows an fp32 FMA path would need
+// more arithmetic than the CUDA cores deliver at HBM speed.  Slots past cache_len may
+// hold anything: their scores are replaced by -inf (select, so NaN never propagates)
+// and their V rows are zeroed in registers before the P.V product.
+#include "attn_internal.h"
+#include "attn_ptx.cuh"
+
+namespace attn {
+namespace {
+
+__device__ unsigned g_decode_error;
+
+constexpr int kBT = 32;          // tokens per pipeline slot
+constexpr int kConsumers = 4;    // consumer warps
+constexpr int kStages = 4;       // ring slots (one per consumer warp)
+constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// The decode mask (TKG "gen_mask_tkg"): type A keeps j < cache_len; type C gives the
+// s_active new tokens (the last s_active slots) a lower-triangular block, so new token t
+// sees slot j iff j <= cache_len - s_active + t.  Shared by the decode kernel and the
+// mask materialiser.
+__device__ __forceinline__ bool decode_allowed(int j, int len, int s_active, int t) {
+    return j < len && j <= len - s_active + t;
+}
+
+template <int D>
+struct DecodeLayout {
+    static constexpr int kBoxBytes = kBT * 128;         // 32 rows x 128 bytes (64 bf16)
+    static constexpr int kHalf = (D / 64) * kBoxBytes;  // K (or V) tile of one slot
+    static constexpr int kSlot = 2 * kHalf;
+    static constexpr int kPipe = kStages * kSlot;
+    static constexpr int kMerge = kConsumers * 16 * D * 4;
+    static_assert(kMerge <= kPipe, "merge buffer must fit in the pipeline region");
+    static constexpr int kDynBytes = kPipe + 1024;      // + alignment slack
+};
+
+struct DecodeParams {
+    const __nv_bfloat16* q;
+    const uint32_t* table;
+    const int32_t* cache_len;
+    float* part_o;
+    float* part_ml;
+    int hq, hkv, s_active, page_size, max_pages, num_pages, max_cache_len;
+    int group, rows, chunk, max_splits, paged, box_rows;
+    float c;  // scale * log2(e)
+};
+
+__device__ __forceinline__ bool mbar_wait_plain(uint64_t* bar, uint32_t parity,
+                                                long long limit) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > limit) return false;
+    return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const DecodeParams p) {
+    using L = DecodeLayout<D>;
+    extern __shared__ uint8_t dyn_smem[];
+    uint8_t* pipe = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+    __shared__ float m_sh[kConsumers][16], l_sh[kConsumers][16];
+    __shared__ int abort_flag;
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int len = p.cache_len[b];
+    if (len < p.s_active || len > p.max_cache_len) {
+        if (threadIdx.x == 0 && split == 0 && g == 0) atomicOr(&g_decode_error, kDevErrCacheLen);
+        return;
+    }
+    const int tok0 = split * p.chunk;
+    if (tok0 >= len) return;  // this sequence is shorter than the split
+    const int tok1 = min(len, tok0 + p.chunk);
+    const int nblocks = (tok1 - tok0 + kBT - 1) / kBT;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------------ producer
+    if (warp == kConsumers) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const int nbox = kBT / p.box_rows;
+            const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;
+            int issued = 0;
+            for (int i = 0; i < nblocks; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait(&empty_bar[s], ((i / kStages) - 1) & 1, &abort_flag))
+                    break;
+                const int j0 = tok0 + i * kBT;
+                int rows[kBT / 16];
+                uint32_t bytes = 0;
+                for (int bx = 0; bx < nbox; ++bx) {
+                    const int jb = j0 + bx * p.box_rows;
+                    rows[bx] = -1;
+                    if (jb >= len) continue;  // a box wholly past the cache end is not read
+                    if (p.paged) {
+                        const uint32_t pg = __ldg(p.table + (size_t)b * p.max_pages + jb / p.page_size);
+                        if (pg >= (uint32_t)p.num_pages) {
+                            atomicOr(&g_decode_error, kDevErrPageOOB);
+                            continue;  // never dereference an out-of-range page
+                        }
+                        rows[bx] = (int)(((long long)pg * p.hkv + g) * p.page_size + jb % p.page_size);
+                    } else {
+                        rows[bx] = (int)(((long long)b * p.hkv + g) * p.max_cache_len + jb);
+                    }
+                    bytes += 2u * (uint32_t)(D / 64) * box_bytes;
+                }
+                uint8_t* kdst = pipe + s * L::kSlot;
+                uint8_t* vdst = kdst + L::kHalf;
+                mbar_arrive_expect_tx(&full_bar[s], bytes);
+                for (int bx = 0; bx < nbox; ++bx) {
+                    if (rows[bx] < 0) continue;
+#pragma unroll
+                    for (int dc = 0; dc < D / 64; ++dc) {
+                        tma_load_2d(kdst + dc * L::kBoxBytes + bx * box_bytes, &tm_k, dc * 64,
+                                    rows[bx], &full_bar[s]);
+                        tma_load_2d(vdst + dc * L::kBoxBytes + bx * box_bytes, &tm_v, dc * 64,
+                                    rows[bx], &full_bar[s]);
+                    }
+                }
+                issued = i + 1;
+            }
+            if (abort_flag) {  // let copies already in flight land before the CTA exits
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    mbar_wait_plain(&full_bar[i % kStages], (i / kStages) & 1, kWaitLimitCycles);
+                atomicOr(&g_decode_error, kDevErrTimeout);
+            }
+        }
+    } else {
+        // -------------------------------------------------------------- consumers
+        const int gq = lane >> 2, qd = lane & 3;
+        const int r0 = gq, r1 = gq + 8;
+        const bool v0 = r0 < p.rows, v1 = r1 < p.rows;
+        const int t0 = r0 % p.s_active, t1 = r1 % p.s_active;
+        const __nv_bfloat16* q0 = nullptr;
+        const __nv_bfloat16* q1 = nullptr;
+        if (v0) q0 = p.q + ((size_t)(b * p.hq + g * p.group + r0 / p.s_active) * p.s_active + t0) * D;
+        if (v1) q1 = p.q + ((size_t)(b * p.hq + g * p.group + r1 / p.s_active) * p.s_active + t1) * D;
+        uint32_t qf[D / 16][4];
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const int c = ks * 16 + 2 * qd;
+            qf[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c)) : 0u;
+            qf[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c)) : 0u;
+            qf[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c + 8)) : 0u;
+            qf[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c + 8)) : 0u;
+        }
+        float o[D / 8][4];
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+        for (int i = warp; i < nblocks; i += kConsumers) {
+            const int s = i % kStages;
+            if (!mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_flag)) break;
+            const uint32_t kbase = smem_u32(pipe + s * L::kSlot);
+            const uint32_t vbase = kbase + L::kHalf;
+            // S = Q K^T for 16 rows x 32 tokens
+            float sc[4][4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+            for (int kp = 0; kp < D / 32; ++kp) {
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const uint32_t tok = nt * 8 + (lane & 7);
+                    const uint32_t cg = 4 * kp + (lane >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[nt], qf[2 * kp], b0, b1);
+                    mma_bf16_16816(sc[nt], qf[2 * kp + 1], b2, b3);
+                }
+            }
+            const int j0 = tok0 + i * kBT;
+            const bool edge = j0 + kBT > len - p.s_active;  // touches the new tokens or the end
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float x0 = sc[nt][e] * p.c, x1 = sc[nt][2 + e] * p.c;
+                    if (edge) {
+                        const int j = j0 + nt * 8 + 2 * qd + e;
+                        if (!(v0 && decode_allowed(j, len, p.s_active, t0))) x0 = -INFINITY;
+                        if (!(v1 && decode_allowed(j, len, p.s_active, t1))) x1 = -INFINITY;
+                    }
+                    sc[nt][e] = x0;
+                    sc[nt][2 + e] = x1;
+                    mx0 = fmaxf(mx0, x0);
+                    mx1 = fmaxf(mx1, x1);
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+            // a row with nothing allowed yet keeps exponent base 0: exp2(-inf - 0) = 0
+            const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+            const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float a0 = ex2(m_run[0] - mu0), a1 = ex2(m_run[1] - mu1);
+            m_run[0] = mn0;
+            m_run[1] = mn1;
+            l_run[0] *= a0;
+            l_run[1] *= a1;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                sc[nt][0] = ex2(sc[nt][0] - mu0);
+                sc[nt][1] = ex2(sc[nt][1] - mu0);
+                sc[nt][2] = ex2(sc[nt][2] - mu1);
+                sc[nt][3] = ex2(sc[nt][3] - mu1);
+                l_run[0] += sc[nt][0] + sc[nt][1];
+                l_run[1] += sc[nt][2] + sc[nt][3];
+            }
+            // O += P V (P from the score accumulators, V via transposed ldmatrix)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t pa[4];
+                pa[0] = pack_bf16(sc[2 * ks][0], sc[2 * ks][1]);
+                pa[1] = pack_bf16(sc[2 * ks][2], sc[2 * ks][3]);
+                pa[2] = pack_bf16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+                pa[3] = pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+                uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+                if (edge) {  // zero V rows of slots past the cache end (they may hold NaN)
+                    const int jl = j0 + ks * 16 + 2 * qd;
+                    keep_lo = (jl < len ? 0x0000ffffu : 0u) | (jl + 1 < len ? 0xffff0000u : 0u);
+                    keep_hi = (jl + 8 < len ? 0x0000ffffu : 0u) | (jl + 9 < len ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int np = 0; np < D / 16; ++np) {
+                    const uint32_t mi = lane >> 3;
+                    const uint32_t tok = ks * 16 + (mi & 1) * 8 + (lane & 7);
+                    const uint32_t cg = 2 * np + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
+                    b0 &= keep_lo;
+                    b2 &= keep_lo;
+                    b1 &= keep_hi;
+                    b3 &= keep_hi;
+                    mma_bf16_16816(o[2 * np], pa, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+        }
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
+
+        // ---------------------------------------------------------- in-CTA merge
+        // Once all four consumer warps are past their loops, every tile the producer
+        // issued has landed (each was waited on), so the ring can hold the merge data.
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+        float* mo = reinterpret_cast<float*>(pipe);  // [kConsumers][16][D]
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            const int col = n * 8 + 2 * qd;
+            *reinterpret_cast<float2*>(mo + (warp * 16 + r0) * D + col) = make_float2(o[n][0], o[n][1]);
+            *reinterpret_cast<float2*>(mo + (warp * 16 + r1) * D + col) = make_float2(o[n][2], o[n][3]);
+        }
+        if (qd == 0) {
+            m_sh[warp][r0] = m_run[0];
+            l_sh[warp][r0] = l_run[0];
+            m_sh[warp][r1] = m_run[1];
+            l_sh[warp][r1] = l_run[1];
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+        const int ctid = threadIdx.x;  // 0 .. 127
+        for (int idx = ctid; idx < p.rows * D; idx += kConsumers * 32) {
+            const int r = idx / D, x = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, m_sh[w][r]);
+            float acc = 0.f, lsum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumers; ++w) {
+                    const float wt = ex2(m_sh[w][r] - M);
+                    acc += wt * mo[(w * 16 + r) * D + x];
+                    lsum += wt * l_sh[w][r];
+                }
+            }
+            const int h = g * p.group + r / p.s_active, t = r % p.s_active;
+            const size_t rowid = ((size_t)b * p.hq + h) * p.s_active + t;
+            const size_t slot = rowid * p.max_splits + split;
+            p.part_o[slot * D + x] = acc;
+            if (x == 0) {
+                p.part_ml[slot * 2 + 0] = M;
+                p.part_ml[slot * 2 + 1] = lsum;
+            }
+        }
+    }
+}
+
+// Merge the chunks of one (sequence, head, new token) row by log-sum-exp:
+//   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
+//   LSE = (M + log2 L) ln 2   (m_i are in log2 units of the scaled scores).
+template <int D, typename OutT>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __restrict__ cache_len,
+                                                           const float* __restrict__ part_o,
+                                                           const float* __restrict__ part_ml,
+                                                           OutT* __restrict__ o, float* lse,
+                                                           int hq, int s_active, int chunk,
+                                                           int max_splits, int max_cache_len) {
+    const size_t rowid = blockIdx.x;
+    const int b = (int)(rowid / ((size_t)hq * s_active));
+    const int x = threadIdx.x;
+    const int len = cache_len[b];
+    float out = 0.f, lse_v = -INFINITY;
+    if (len >= s_active && len <= max_cache_len) {
+        const int ns = (len + chunk - 1) / chunk;
+        const float* ml = part_ml + rowid * max_splits * 2;
+        float M = -INFINITY;
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
+        if (M != -INFINITY) {
+            float Lsum = 0.f, acc = 0.f;
+            const float* po = part_o + rowid * max_splits * D + x;
+            for (int s = 0; s < ns; ++s) {
+                const float wt = ex2(ml[2 * s] - M);
+                Lsum += wt * ml[2 * s + 1];
+                acc += wt * po[(size_t)s * D];
+            }
+            out = acc / Lsum;
+            lse_v = (M + __log2f(Lsum)) * kLn2;
+        }
+    }
+    if constexpr (sizeof(OutT) == 2)
+        o[rowid * D + x] = __float2bfloat16_rn(out);
+    else
+        o[rowid * D + x] = out;
+    if (lse != nullptr && x == 0) lse[rowid] = lse_v;
+}
+
+// The 0/1 decode mask, one byte per (sequence, head, new token, cache position).
+__global__ void gen_mask_kernel(const int32_t* __restrict__ cache_len, int hq, int s_active,
+                                int max_len, uint8_t* __restrict__ mask, long long total) {
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long row = idx / max_len;
+        const int j = (int)(idx - row * max_len);
+        const int t = (int)(row % s_active);
+        const int b = (int)(row / ((long long)hq * s_active));
+        const int len = cache_len[b];
+        uint8_t v = 0;
+        if (len < s_active || len > max_len) {
+            if (j == 0) atomicOr(&g_decode_error, kDevErrCacheLen);
+        } else {
+            v = decode_allowed(j, len, s_active, t) ? 1 : 0;
+        }
+        mask[idx] = v;
+    }
+}
+
+template <int D>
+attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
+    using L = DecodeLayout<D>;
+    const bool paged = a.block_table != nullptr;
+    const int box_rows = paged ? (a.page_size < kBT ? a.page_size : kBT) : kBT;
+    CUtensorMap tk, tv;
+    uint64_t rows = paged ? (uint64_t)a.num_pages * a.hkv * a.page_size
+                          : (uint64_t)a.b * a.hkv * a.max_cache_len;
+    uint64_t dims[2] = {(uint64_t)D, rows};
+    uint64_t strides[1] = {(uint64_t)D * 2};
+    uint32_t box[2] = {64u, (uint32_t)box_rows};
+    if (!make_bf16_map(&tk, a.k_cache, 2, dims, strides, box) ||
+        !make_bf16_map(&tv, a.v_cache, 2, dims, strides, box))
+        return ATTN_ERR_CUDA;
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.table = a.block_table;
+    p.cache_len = a.cache_len;
+    p.part_o = a.part_o;
+    p.part_ml = a.part_ml;
+    p.hq = a.hq;
+    p.hkv = a.hkv;
+    p.s_active = a.s_active;
+    p.page_size = paged ? a.page_size : 1;
+    p.max_pages = a.max_pages_per_seq;
+    p.num_pages = a.num_pages;
+    p.max_cache_len = a.max_cache_len;
+    p.group = a.hq / a.hkv;
+    p.rows = p.group * a.s_active;
+    p.chunk = a.kv_chunk;
+    p.max_splits = a.max_splits;
+    p.paged = paged ? 1 : 0;
+    p.box_rows = box_rows;
+    p.c = a.scale * kLog2e;
+
+    static bool attr_set = false;  // benign race: every thread sets the same value
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::kDynBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        attr_set = true;
+    }
+    dim3 grid(a.max_splits, a.hkv, a.b);
+    decode_split_kernel<D><<<grid, kThreads, L::kDynBytes, stream>>>(tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    const unsigned nrows = (unsigned)((size_t)a.b * a.hq * a.s_active);
+    if (a.o_dtype == ATTN_BF16)
+        decode_combine_kernel<D, __nv_bfloat16><<<nrows, D, 0, stream>>>(
+            a.cache_len, a.part_o, a.part_ml, static_cast<__nv_bfloat16*>(a.o), a.lse, a.hq,
+            a.s_active, a.kv_chunk, a.max_splits, a.max_cache_len);
+    else
+        decode_combine_kernel<D, float><<<nrows, D, 0, stream>>>(
+            a.cache_len, a.part_o, a.part_ml, static_cast<float*>(a.o), a.lse, a.hq, a.s_active,
+            a.kv_chunk, a.max_splits, a.max_cache_len);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status decode_launch(const DecodeArgs& a, cudaStream_t stream) {
+    switch (a.d) {
+        case 64: return decode_launch_d<64>(a, stream);
+        case 128: return decode_launch_d<128>(a, stream);
+        case 256: return decode_launch_d<256>(a, stream);
+        default: return ATTN_ERR_UNSUPPORTED;
+    }
+}
+
+attn_status gen_mask_launch(const int32_t* cache_len, int b, int hq, int s_active, int max_len,
+                            uint8_t* mask, cudaStream_t stream) {
+    const long long total = (long long)b * hq * s_active * max_len;
+    if (total == 0) return ATTN_OK;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152ll * 64) blocks = 152ll * 64;
+    gen_mask_kernel<<<(unsigned)blocks, 256, 0, stream>>>(cache_len, hq, s_active, max_len, mask,
+                                                          total);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+unsigned decode_take_error(cudaStream_t stream, cudaError_t* err) {
+    unsigned v = 0, zero = 0;
+    *err = cudaMemcpyFromSymbolAsync(&v, g_decode_error, sizeof v, 0, cudaMemcpyDeviceToHost, stream);
+    if (*err == cudaSuccess)
+        *err = cudaMemcpyToSymbolAsync(g_decode_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                       stream);
+    if (*err == cudaSuccess) *err = cudaStreamSynchronize(stream);
+    if (*err != cudaSuccess) cudaGetLastError();
+    return v;
+}
+
+}  // namespace attn

@@ -1,0 +1,162 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) attention-forward library.
+ *
+ * Computes O = softmax(scale * Q K^T + mask) V and the per-row log-sum-exp with the
+ * flash-attention online-softmax recurrence ("Flash-Attention: Context (CTE)",
+ * section "The online-softmax recurrence"; minfer "03 - 8n FA-style tiled prefill
+ * attention", section 2.1 "Online softmax"), for prefill (many queries) and for decode
+ * (a few new queries against a flat or paged KV cache).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library never
+ *     frees, keeps or allocates device memory during a call.  Scratch memory that a
+ *     call needs is passed in by the caller (see attn_decode_workspace_bytes).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Every compute entry point only enqueues work on it and returns; results are
+ *     valid once the stream has reached that point.
+ *   - Arguments are checked on the host before anything is enqueued.  An invalid call
+ *     returns ATTN_ERR_INVALID_ARG or ATTN_ERR_UNSUPPORTED and enqueues nothing.
+ *   - A failed launch returns ATTN_ERR_CUDA; the library clears the pending CUDA error
+ *     (cudaGetLastError) before returning so the caller's stream is not poisoned
+ *     (minfer 8n, section 3.3, on the shared-memory opt-in failure).
+ *   - Faults found by a kernel (a page index past the pool, a wait that never ended)
+ *     never trap: the kernel sets a device error word, skips the faulty access, and the
+ *     caller reads the word with attn_get_device_error() after synchronising.
+ *   - bf16 is IEEE bfloat16 (the top half of an fp32); fp32 is IEEE binary32.
+ *   - All entry points are thread-safe with respect to each other on distinct streams.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,    /* a pointer, size or value violates the contract */
+    ATTN_ERR_UNSUPPORTED = 2,    /* valid in principle, not implemented (e.g. d = 96) */
+    ATTN_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+    ATTN_ERR_PAGE_OOB = 4,       /* device: a block-table entry >= num_pages was met */
+    ATTN_ERR_DEVICE_TIMEOUT = 5, /* device: a pipeline wait exceeded its limit */
+    ATTN_ERR_WORKSPACE = 6,      /* workspace NULL, misaligned or too small */
+    ATTN_ERR_CACHE_LEN = 7       /* device: a cache_len outside [s_active, max_cache_len] */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/*
+ * attn_fwd_prefill -- fused attention forward for sq queries against skv keys.
+ *
+ * Defines ("Flash-Attention: Context (CTE)", Abstract and "The masking"; optimum-neuron
+ * attention AGENTS.md, "Sliding window"; minfer 8n, section 2.1):
+ *   kv(h)     = h / (hq / hkv)                         (GQA, CTE "GQA and multi-head")
+ *   q_pos(i)  = i + (skv - sq)                         (queries sit at the key tail)
+ *   allowed   = j < skv  and (!causal or j <= q_pos(i))
+ *                        and (window == 0 or j >= q_pos(i) - window + 1)
+ *   s_j       = scale * sum_x Q[b,h,i,x] K[b,kv(h),j,x]
+ *   O[b,h,i]  = sum_{allowed j} exp(s_j - M) V[b,kv(h),j] / sum_{allowed j} exp(s_j - M)
+ *   LSE[b,h,i]= M + ln sum_{allowed j} exp(s_j - M),   M = max_{allowed j} s_j
+ * A row with no allowed key gets O = 0 and LSE = -inf (minfer 8n: rows with l == 0
+ * stay 0).  Computed with the online-softmax recurrence: whole KV tiles outside the
+ * causal/window band are skipped ("CTE", "Algorithm - compute-skip"), the mask is applied
+ * only on tiles that straddle a band edge, exp is evaluated as exp2 with scale*log2(e)
+ * folded into one multiply-add, and the accumulator is rescaled lazily.
+ *
+ * Layouts (row-major, contiguous, 16-byte aligned base pointers):
+ *   q : bf16 [b, hq,  sq,  d]      k, v : bf16 [b, hkv, skv, d]
+ *   o : [b, hq, sq, d] in o_dtype (ATTN_BF16 rounds to nearest-even, or ATTN_F32)
+ *   lse : fp32 [b, hq, sq], natural-log units of the scaled scores; may be NULL.
+ * Sizes: b, hq, hkv >= 1, hq % hkv == 0, sq >= 0 (0 = nothing to do), skv >= 0,
+ *   d in {64, 128, 256}, window >= 0 and window > 0 only with causal != 0,
+ *   scale finite.  Rows, heads and batches up to 2^31 - 1 elements per dimension.
+ * Errors: INVALID_ARG / UNSUPPORTED before launch; CUDA if a launch fails;
+ *   a device timeout is reported by attn_get_device_error().
+ */
+attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int b, int hq, int hkv, int sq, int skv, int d, float scale,
+                             int causal, int window, attn_dtype o_dtype, void* stream);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of caller-provided scratch that attn_fwd_decode
+ * needs for these sizes (split-KV partial outputs and their (max, sum) pairs).
+ * kv_chunk as for attn_fwd_decode (0 = library default).  Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_cache_len,
+                                   int kv_chunk);
+
+/*
+ * attn_fwd_decode -- attention of s_active new tokens per sequence against its KV cache.
+ *
+ * Defines ("Flash-Attention: Decode (TKG)", "The single-query decode attention",
+ * "KV-cache layouts and access", "gen_mask_tkg"):
+ *   the cache of sequence b holds cache_len[b] tokens, the last s_active of which are the
+ *   new tokens' own K/V (already appended by the caller);
+ *   new token t sits at q_pos = cache_len[b] - s_active + t and attends cache position j
+ *   iff j <= q_pos (the validity cut j < cache_len plus the tril block among the new
+ *   tokens); the softmax runs over the cache axis; GQA as in attn_fwd_prefill.
+ * It runs as a split-KV pass (each (sequence, kv head, chunk of kv_chunk tokens) keeps
+ * its own running max, sum and unnormalised output) followed by a log-sum-exp combine.
+ *
+ * Layouts:
+ *   q : bf16 [b, hq, s_active, d]        o : [b, hq, s_active, d] in o_dtype
+ *   lse : fp32 [b, hq, s_active] (may be NULL)
+ *   cache_len : int32 [b]
+ *   paged cache (block_table != NULL): k_cache, v_cache bf16 [num_pages, hkv, page_size, d];
+ *     block_table uint32 [b, max_pages_per_seq]; logical token j of sequence b lives in
+ *     page block_table[b][j / page_size], slot j % page_size ("Paged / block cache").
+ *     Entries past ceil(cache_len/page_size) are never read.
+ *   flat cache (block_table == NULL): k_cache, v_cache bf16 [b, hkv, max_cache_len, d].
+ *   Slots past cache_len may hold anything (even NaN); they contribute exactly zero.
+ * Sizes: hq % hkv == 0; (hq / hkv) * s_active <= 16; d in {64, 128, 256};
+ *   1 <= s_active; cache_len[b] in [s_active, max_cache_len];
+ *   paged: page_size a power of two in [16, 256], max_cache_len <=
+ *   max_pages_per_seq * page_size, num_pages >= 1; kv_chunk = 0 (default) or a positive
+ *   multiple of 32 (and of page_size when page_size > 32).
+ * Workspace: device scratch of at least attn_decode_workspace_bytes(...), 16-byte aligned,
+ *   owned by the caller, not read before it is written; calls that share it must not
+ *   overlap on the device.
+ * Errors: INVALID_ARG / UNSUPPORTED / WORKSPACE before launch; CUDA on launch failure.
+ *   A block-table entry >= num_pages or a cache_len outside its range is reported by
+ *   attn_get_device_error() (ATTN_ERR_PAGE_OOB / ATTN_ERR_CACHE_LEN); the offending page
+ *   is not read and the affected outputs are unspecified.
+ */
+attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const uint32_t* block_table, const int32_t* cache_len, int b, int hq,
+                            int hkv, int d, int s_active, int page_size, int max_pages_per_seq,
+                            int num_pages, int max_cache_len, float scale, void* o, float* lse,
+                            attn_dtype o_dtype, int kv_chunk, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
+ * attn_gen_mask_decode -- materialise the decode 0/1 mask that attn_fwd_decode applies
+ * in registers ("Flash-Attention: Decode (TKG)", "gen_mask_tkg": type A `index <
+ * cache length` and type C, the tril(ones(s_active)) block of the new tokens):
+ *   mask[b, h, t, j] = 1 iff j < cache_len[b] and j <= cache_len[b] - s_active + t.
+ * It is evaluated by the same device predicate the decode kernel uses.
+ * mask_out: uint8 [b, hq, s_active, max_len] (device).  cache_len must lie in
+ * [s_active, max_len]; rows of a sequence outside it are left all-zero and flagged
+ * (ATTN_ERR_CACHE_LEN via attn_get_device_error).
+ */
+attn_status attn_gen_mask_decode(const int32_t* cache_len, int b, int hq, int s_active,
+                                 int max_len, uint8_t* mask_out, void* stream);
+
+/*
+ * attn_get_device_error -- synchronise `stream`, then read and clear the device error
+ * words of every kernel in the library on the current device.  Returns ATTN_OK, or the
+ * most severe of ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_PAGE_OOB, ATTN_ERR_CACHE_LEN; returns
+ * ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+attn_status attn_get_device_error(void* stream);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char* attn_status_string(attn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

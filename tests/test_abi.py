@@ -1,0 +1,117 @@
+"""The C-ABI library loads without a GPU, exports every entry point attn.h declares, and
+its host-side checks reject invalid calls before anything reaches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import flash_attention_forward_attn_gb300 as A
+from flash_attention_forward_attn_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return A.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_symbols() == sorted([
+        "attn_fwd_prefill", "attn_decode_workspace_bytes", "attn_fwd_decode",
+        "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ATTN_OK"), (1, "ATTN_ERR_INVALID_ARG"), (2, "ATTN_ERR_UNSUPPORTED"),
+                       (3, "ATTN_ERR_CUDA"), (4, "ATTN_ERR_PAGE_OOB"), (5, "ATTN_ERR_DEVICE_TIMEOUT"),
+                       (6, "ATTN_ERR_WORKSPACE"), (7, "ATTN_ERR_CACHE_LEN")]:
+        assert A.attn_status_string(code) == name
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation first
+
+
+def prefill(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, b=1, hq=4, hkv=2, sq=16, skv=16, d=128,
+             scale=0.1, causal=1, window=0, o_dtype=0)
+    a.update(kw)
+    return lib.attn_fwd_prefill(a["q"], a["k"], a["v"], a["o"], a["lse"], a["b"], a["hq"], a["hkv"],
+                                a["sq"], a["skv"], a["d"], a["scale"], a["causal"], a["window"],
+                                a["o_dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hq=3, hkv=2), 1), (dict(b=0), 1), (dict(sq=-1), 1), (dict(window=-2), 1),
+    (dict(d=96), 2), (dict(d=512), 2), (dict(causal=0, window=8), 2), (dict(q=None), 1),
+    (dict(o=ctypes.c_void_p((1 << 20) + 8)), 1), (dict(scale=float("nan")), 1),
+    (dict(o_dtype=7), 1),
+])
+def test_prefill_rejects_before_launch(lib, kw, status):
+    assert prefill(lib, **kw) == status
+
+
+def test_prefill_zero_queries_is_a_no_op(lib):
+    assert prefill(lib, sq=0) == 0
+
+
+def decode(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, table=FAKE, cl=FAKE, b=2, hq=8, hkv=2, d=128, sa=4, page=32,
+             maxp=4, npages=8, maxlen=128, scale=0.1, o=FAKE, lse=None, odt=0, chunk=0, ws=FAKE,
+             wsb=1 << 30)
+    a.update(kw)
+    return lib.attn_fwd_decode(a["q"], a["k"], a["v"], a["table"], a["cl"], a["b"], a["hq"], a["hkv"],
+                               a["d"], a["sa"], a["page"], a["maxp"], a["npages"], a["maxlen"],
+                               a["scale"], a["o"], a["lse"], a["odt"], a["chunk"], a["ws"], a["wsb"],
+                               None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hq=6, hkv=4), 1), (dict(sa=0), 1), (dict(page=24), 1), (dict(page=8), 1),
+    (dict(maxp=3), 1), (dict(chunk=48), 1), (dict(d=80), 2), (dict(sa=5), 2),
+    (dict(ws=None), 6), (dict(wsb=100), 6), (dict(ws=ctypes.c_void_p((1 << 20) + 4)), 6),
+    (dict(cl=None), 1), (dict(npages=0), 1),
+])
+def test_decode_rejects_before_launch(lib, kw, status):
+    assert decode(lib, **kw) == status
+
+
+def test_workspace_bytes_formula(lib):
+    # rows = b*hq*s_active; splits = ceil(max_len / chunk); O partials (256-byte padded) + (m, l)
+    rows, splits, d = 64 * 32 * 4, 32, 128
+    o = rows * splits * d * 4
+    assert A.attn_decode_workspace_bytes(64, 32, 4, 128, 32768) == o + rows * splits * 8
+    assert A.attn_decode_workspace_bytes(1, 1, 1, 64, 100, 64) == ((2 * 64 * 4 + 255) // 256) * 256 + 16
+    assert A.attn_decode_workspace_bytes(1, 1, 1, 96, 100) == 0
+    assert A.attn_decode_workspace_bytes(1, 1, 1, 64, 100, 33) == 0
+
+
+def test_mask_rejects_before_launch(lib):
+    assert lib.attn_gen_mask_decode(FAKE, 0, 1, 1, 10, FAKE, None) == 1
+    assert lib.attn_gen_mask_decode(None, 1, 1, 1, 10, FAKE, None) == 1
+    assert lib.attn_gen_mask_decode(FAKE, 1, 1, 1, 0, FAKE, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib
+
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(A, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        A.load_library()
+    monkeypatch.setattr(A, "_lib", None)
+    importlib.reload(_build)
