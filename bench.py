@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention forward on GB300.
+
+One step = one fused prefill call (attn_fwd_prefill) on the causal 7B-shaped workload
+(batch 1, 32 heads, 2048 x 2048, head_dim 128, bf16) with inputs resident in HBM.
+The line also carries the other hot-path workloads, each timed the same way:
+the 32K GQA causal prefill with Q outliers, the 8K head_dim-256 sliding-window prefill,
+and the paged decode (split-KV + log-sum-exp combine) with 1 and 4 new tokens.
+
+Timing: W untimed warm-up steps, then exactly K timed steps; every step is bracketed
+by CUDA events on the launching stream, and a 256 MiB buffer is written between steps
+to flush the 129 MB L2.  A barrier plus torch.cuda.synchronize() bracket the timed
+region; with N > 1 ranks each rank runs its own replica and the max over ranks is used.
+SM clocks are sampled with nvidia-smi while the timed regions run.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference that exists for this
+path) on bounded samples of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "prefill attn TFLOPS & decode KV GB/s on 1\u00d7GB300 (fraction of roofline)"
+
+
+# --------------------------------------------------------------------------- ranks
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(
+        os.environ.get("LOCAL_RANK", 0))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar across the job (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, seconds_per_rank: float, world: int, device=None):
+    """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
+    slowest = max_over_ranks(seconds_per_rank, world, device)
+    return units_per_rank * world / slowest, slowest
+
+
+# --------------------------------------------------------------------------- peaks, clocks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"attn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+        load = [x for x in sm if smax is None or x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- traffic record
+def source_sha(*rel_paths) -> str:
+    h = hashlib.sha256()
+    for rel in rel_paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "prefill": ("flash_attention_forward_attn_gb300/csrc/prefill_sm103.cu",
+                "flash_attention_forward_attn_gb300/csrc/attn_ptx.cuh"),
+    "decode": ("flash_attention_forward_attn_gb300/csrc/decode_sm103.cu",
+               "flash_attention_forward_attn_gb300/csrc/attn_ptx.cuh"),
+}
+
+
+def recorded_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("source_sha") != source_sha(*KERNEL_SOURCES[kind]):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- GPU timing
+def time_steps(fn, steps, warmup, flush_buf, stream):
+    """Per-step device time (ms) with CUDA events on `stream`; L2 flushed before each step."""
+    import torch
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush_buf.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush_buf.fill_(i & 0xFF)  # on the timing stream, outside the events
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False):
+    import torch
+
+    import flash_attention_forward_attn_gb300 as A
+    from workloads import configs as C
+
+    q, k, v = C.prefill_inputs_torch(w, dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16 if w.o_dtype == "bf16" else torch.float32,
+                    device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+    def step():
+        A.attn_fwd_prefill(q, k, v, causal=w.causal, window=w.window, scale=w.scale, o=o, lse=lse,
+                           stream=stream)
+
+    ms = time_steps(step, steps, warmup, flush, stream)
+    assert A.attn_get_device_error(stream) == 0
+    mean_ms = sum(ms) / len(ms)
+    flops = w.flops()
+    value, slowest_s = aggregate_throughput(flops * steps, sum(ms) / 1e3, world, dev)
+    tflops = value / 1e12
+    achieved = flops / (mean_ms / 1e3) / 1e12
+    traffic = recorded_traffic("prefill", w.name)
+    ent = {
+        "workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": mean_ms,
+        "ms_min": min(ms), "flops_per_step": flops, "steps": steps, "gpu_launches": steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": traffic, "algorithmic_bytes": w.io_bytes(),
+                     "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
+        "slowest_rank_s": slowest_s,
+    }
+    if e2e:
+        ent["e2e"] = prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev)
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    return ent
+
+
+def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
+    """Same metric through the public API with host buffers: pinned H2D of Q, K, V, the
+    call, and D2H of O and LSE, all inside the timed region."""
+    import torch
+
+    import flash_attention_forward_attn_gb300 as A
+
+    hq_, hk_, hv_ = (x.cpu().pin_memory() for x in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def step():
+        with torch.cuda.stream(stream):
+            q.copy_(hq_, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv_, non_blocking=True)
+            A.attn_fwd_prefill(q, k, v, causal=w.causal, window=w.window, scale=w.scale, o=o,
+                               lse=lse, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    value, _ = aggregate_throughput(w.flops() * steps, s.elapsed_time(e) / 1e3, world, dev)
+    return {"value": value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": s.elapsed_time(e) / steps}
+
+
+def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world):
+    import torch
+
+    import flash_attention_forward_attn_gb300 as A
+    from workloads import configs as C
+
+    t = C.decode_inputs_torch(w, dev)
+    ws = torch.empty(A.attn_decode_workspace_bytes(w.b, w.hq, w.s_active, w.d, t["max_cache_len"]),
+                     dtype=torch.uint8, device=dev)
+    o = torch.empty(t["q"].shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(t["q"].shape[:3], dtype=torch.float32, device=dev)
+
+    def step():
+        A.attn_fwd_decode(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["cache_len"],
+                          max_cache_len=t["max_cache_len"], scale=w.scale, o=o, lse=lse,
+                          workspace=ws, stream=stream)
+
+    ms = time_steps(step, steps, warmup, flush, stream)
+    assert A.attn_get_device_error(stream) == 0
+    mean_ms = sum(ms) / len(ms)
+    nbytes = C.decode_io_bytes(w, t["lens"])
+    value, slowest_s = aggregate_throughput(nbytes * steps, sum(ms) / 1e3, world, dev)
+    achieved = nbytes / (mean_ms / 1e3) / 1e9
+    ent = {
+        "workload": w.name, "value": value / 1e9, "unit": "GB/s", "ms_per_step": mean_ms,
+        "ms_min": min(ms), "bytes_per_step": nbytes, "mean_cache_len": float(t["lens"].mean()),
+        "steps": steps, "gpu_launches": 2 * steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic("decode", w.name),
+                     "timed": "whole call (split-KV kernel + combine kernel)",
+                     "peak_source": f"{peaks['source']} HBM copy (MEASURED_PEAKS.json)"},
+        "slowest_rank_s": slowest_s,
+    }
+    del t, ws, o, lse
+    torch.cuda.empty_cache()
+    return ent
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_prefill_sample(w, n_heads: int, rows_per_head: int, threads: int):
+    """Time the fp64 oracle on a bounded sample of a prefill workload.
+
+    The sample is `n_heads` heads, and in each the last `rows_per_head` query rows (or all
+    rows when rows_per_head >= sq): inputs come from the seeded generator, never from a GPU.
+    Returns (seconds, causal-adjusted FLOPs of the sample, description)."""
+    import numpy as np
+
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from workloads import configs as C
+
+    rows = list(range(max(0, w.sq - rows_per_head), w.sq))
+    jobs = []
+    for idx in range(n_heads):
+        b, h = divmod(idx, w.hq)
+        g = oracle.kv_head(h, w.hq, w.hkv)
+        kh = C.prefill_kv_head_np(w, "k", b, g)
+        vh = C.prefill_kv_head_np(w, "v", b, g)
+        qr = C.prefill_q_rows_np(w, b, h, rows[0], len(rows))
+        jobs.append((qr, kh, vh))
+    qp = np.array([oracle.q_pos(r, w.sq, w.skv) for r in rows])
+    chunks = [(j, s) for j in range(len(jobs)) for s in range(0, len(rows), 16)]
+
+    def run(js):
+        j, s = js
+        qr, kh, vh = jobs[j]
+        oracle.attention_rows(qr[s:s + 16], kh, vh, qp[s:s + 16], w.scale, w.causal, w.window)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, chunks))
+    secs = time.perf_counter() - t0
+    if w.causal:
+        lo = np.maximum(0, qp - w.window + 1) if w.window > 0 else np.zeros_like(qp)
+        pairs = int((np.minimum(qp, w.skv - 1) - lo + 1).clip(0).sum())
+    else:
+        pairs = len(rows) * w.skv
+    flops = 4.0 * w.d * pairs * n_heads
+    desc = (f"{n_heads} head(s) x last {len(rows)} query rows of {w.name} "
+            f"(fp64, full score rows, {threads} threads)")
+    return secs, flops, desc
+
+
+def cpu_baseline(w, threads):
+    # about 10-30 CPU-seconds: all 32 heads x all 2048 rows of the 2K workload
+    secs, flops, desc = oracle_prefill_sample(w, n_heads=w.b * w.hq, rows_per_head=w.sq,
+                                              threads=threads)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "seconds": secs}
+
+
+# --------------------------------------------------------------------------- main
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle on the host cores, rank 0 only."""
+    from workloads import configs as C
+
+    if rank != 0:
+        return 0
+    w = C.CAUSAL_PREFILL_2K
+    threads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle_prefill_sample(w, 1, 16, threads)
+    tot_s, tot_f, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        s, f, desc = oracle_prefill_sample(w, 1, 16, threads)
+        tot_s += s
+        tot_f += f
+    value = tot_f / tot_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "hq": w.hq, "hkv": w.hkv, "sq": w.sq,
+                   "skv": w.skv, "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="only the main workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None,
+                    help="time only this named workload (profiling runs); prints its entry")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+
+    import flash_attention_forward_attn_gb300 as A
+    from workloads import configs as C
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    A.load_library()
+    peaks = measured_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    w = C.CAUSAL_PREFILL_2K
+
+    if args.workload is not None:
+        wx = C.REGISTRY[args.workload]
+        if isinstance(wx, C.PrefillWorkload):
+            ent = prefill_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world)
+        else:
+            ent = decode_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world)
+        if rank == 0:
+            print(json.dumps(ent), flush=True)
+        return 0
+
+    extras = {}
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        main_ent = prefill_entry(w, dev, args.steps, args.warmup, flush, stream, peaks, world,
+                                 e2e=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        if not args.no_extra:
+            ext_steps = max(10, min(args.steps, 30))
+            for wx in (C.GQA_PREFILL_32K, C.SWA_PREFILL_8K):
+                extras[wx.name] = prefill_entry(wx, dev, ext_steps, args.warmup, flush, stream,
+                                                peaks, world)
+            for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4):
+                extras[wx.name] = decode_entry(wx, dev, max(ext_steps, 50), args.warmup, flush,
+                                               stream, peaks, world)
+    clocks = clk.summary()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, os.cpu_count() or 1)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": main_ent["value"], "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_ent["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) rounded to bf16)",
+            "config": {"workload": w.name, "b": w.b, "hq": w.hq, "hkv": w.hkv, "sq": w.sq,
+                       "skv": w.skv, "d": w.d, "causal": w.causal, "o_dtype": w.o_dtype,
+                       "l2": "flushed between steps (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": main_ent["roofline"],
+            "e2e": main_ent["e2e"],
+            "gpu_launches": main_ent["gpu_launches"],
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "workloads": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

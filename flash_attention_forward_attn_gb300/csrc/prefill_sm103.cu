@@ -256,9 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             float x[BN];
             {
                 uint32_t r[BN];
-#pragma unroll
-                for (int c0 = 0; c0 < BN; c0 += 32)
-                    tmem_ld32(tmem + lane_off + C::kSCol + s * BN + c0, r + c0);
+                if constexpr (BN == 128)
+                    tmem_ld128(tmem + lane_off + C::kSCol + s * BN, r);
+                else
+                    tmem_ld64(tmem + lane_off + C::kSCol + s * BN, r);
 #pragma unroll
                 for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(r[i]);
             }
@@ -272,18 +273,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                     if (key < key_lo || key > key_hi) x[i] = -INFINITY;
                 }
             }
-            float tmax = -INFINITY;
-            if (c_pos) {
+            // row max with 8 independent chains (a single chain is latency-bound)
+            float mx[8];
 #pragma unroll
-                for (int i = 0; i < BN; ++i) tmax = fmaxf(tmax, x[i]);
-                tmax *= c;  // -inf stays -inf
-            } else {
+            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+            if (!c_pos) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    x[i] *= c;
-                    tmax = fmaxf(tmax, x[i]);
-                }
+                for (int i = 0; i < BN; ++i) x[i] *= c;
             }
+#pragma unroll
+            for (int i = 0; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+            float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            if (c_pos) tmax *= c;  // -inf stays -inf
             // x holds raw scores when c > 0 (exponent = x*c - m), scaled scores otherwise
             const float m_new = fmaxf(m_used, tmax);
             const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
@@ -311,26 +313,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                 }
             }
             const float m_e = (m_used == -INFINITY) ? 0.f : m_used;
+            const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m_e
             uint8_t* pbuf = sm + C::kPOff + s * C::kPBytes;
+            float ls[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
 #pragma unroll
             for (int ch = 0; ch < BN / 8; ++ch) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    float p0, p1;
-                    if (c_pos) {
-                        p0 = ex2(fmaf(x[ch * 8 + 2 * e], c, -m_e));
-                        p1 = ex2(fmaf(x[ch * 8 + 2 * e + 1], c, -m_e));
-                    } else {
-                        p0 = ex2(x[ch * 8 + 2 * e] - m_e);
-                        p1 = ex2(x[ch * 8 + 2 * e + 1] - m_e);
-                    }
-                    l_sum += p0 + p1;
+                    const float p0 = ex2(fmaf(x[ch * 8 + 2 * e], cm, -m_e));
+                    const float p1 = ex2(fmaf(x[ch * 8 + 2 * e + 1], cm, -m_e));
+                    ls[2 * e] += p0;
+                    ls[2 * e + 1] += p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
                 const uint32_t off = (ch >> 3) * (kBM * 128) + sw128_off(row, ch & 7);
                 *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&p_full[s]);

@@ -1,0 +1,80 @@
+"""Host-side logic of bench.py: the N>1 aggregation over ranks (two gloo ranks on CPU),
+clock-log parsing, peaks and the recorded-traffic guard."""
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # rank r processed 10 units in r + 1 seconds: the job did 20 units in 2 s (the slowest)
+    value, slowest = bench.aggregate_throughput(10.0, rank + 1.0, world)
+    bench.barrier(world)
+    out[rank] = (value, slowest, bench.max_over_ranks(float(rank * 7), world))
+    dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for r in range(2):
+        assert out[r] == (10.0, 2.0, 7.0)
+
+
+def test_single_rank_aggregate_is_identity():
+    assert bench.aggregate_throughput(5.0, 2.0, 1) == (2.5, 2.0)
+
+
+def test_clock_summary_parses_reasons(tmp_path):
+    cs = bench.ClockSampler(0)
+    cs.path = str(tmp_path / "c.csv")
+    cs.proc = object()
+    with open(cs.path, "w") as f:
+        f.write("0, 1900, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+        f.write("0, 1950, 2070, 1100.0, 0x4, Not Active, Not Active, Not Active, Active\n")
+        f.write("0, 300, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+    s = cs.summary()
+    assert s["sm_max_mhz"] == 2070 and s["sm_mhz"] == 1925 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_recorded_traffic_requires_matching_source(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "prefill", ("k.cu",))
+    sha = bench.source_sha("k.cu")
+    (prof / "dram_traffic.json").write_text(json.dumps(
+        {"w": {"source_sha": sha, "dram_bytes_per_launch": 123}}))
+    assert bench.recorded_traffic("prefill", "w") == 123
+    src.write_text("kernel v2")
+    assert bench.recorded_traffic("prefill", "w") is None
+
+
+def test_measured_peaks_reads_driver_file():
+    p = bench.measured_peaks()
+    assert p["hbm_gbs"] > 1000 and p["bf16_tflops"] > 100

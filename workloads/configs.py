@@ -124,6 +124,16 @@ PAGED_DECODE_SPEC4 = DecodeWorkload("paged_decode_b64_h32kv8_d128_sa4", 64, 32, 
 ALL_PREFILL = (TINY_PREFILL, CAUSAL_PREFILL_2K, GQA_PREFILL_32K, SWA_PREFILL_8K)
 ALL_DECODE = (PAGED_DECODE, PAGED_DECODE_SPEC4)
 
+# Reduced variants of the same kernels, sized for profiler captures (a few hundred MB).
+GQA_PREFILL_8K = GQA_PREFILL_32K.with_(name="gqa_causal_prefill_b1_h32kv8_s8192_d128_outliers",
+                                       sq=8192, skv=8192)
+SWA_PREFILL_8K_B1 = SWA_PREFILL_8K.with_(name="swa_prefill_b1_h32kv16_s8192_d256_w1024", b=1)
+PAGED_DECODE_B16 = PAGED_DECODE.with_(name="paged_decode_b16_h32kv8_d128_sa1", b=16)
+PAGED_DECODE_SPEC4_B16 = PAGED_DECODE_SPEC4.with_(name="paged_decode_b16_h32kv8_d128_sa4", b=16)
+
+REGISTRY = {w.name: w for w in ALL_PREFILL + ALL_DECODE + (
+    GQA_PREFILL_8K, SWA_PREFILL_8K_B1, PAGED_DECODE_B16, PAGED_DECODE_SPEC4_B16)}
+
 
 # =========================================================================== prefill
 def _prefill_q_counter(w: PrefillWorkload, b: int, h: int, i0: int) -> int:
