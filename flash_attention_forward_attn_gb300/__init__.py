@@ -18,6 +18,7 @@ __all__ = [
     "AttnError", "ATTN_BF16", "ATTN_F32", "library_path", "load_library",
     "attn_fwd_prefill", "attn_fwd_decode", "attn_decode_workspace_bytes",
     "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
+    "attn_fwd_decode_static_ws",
 ]
 
 ATTN_BF16, ATTN_F32 = 0, 1
@@ -64,6 +65,9 @@ def load_library(build_if_missing: bool = False):
         lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, I, I, P,
                                         S, P]
         lib.attn_fwd_decode.restype = I
+        lib.attn_fwd_decode_static_ws.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F,
+                                                  P, P, I, I, P]
+        lib.attn_fwd_decode_static_ws.restype = I
         lib.attn_gen_mask_decode.argtypes = [P, I, I, I, I, P, P]
         lib.attn_gen_mask_decode.restype = I
         lib.attn_get_device_error.argtypes = [P]
@@ -152,6 +156,60 @@ def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | N
     _check(lib.attn_fwd_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, hq, hkv, sq,
                                 skv, d, sc, int(bool(causal)), int(window), _dtype_code(o.dtype),
                                 _stream_ptr(stream)), "attn_fwd_prefill")
+    return o, lse
+
+
+def _decode_marshal(q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse,
+                    o_dtype):
+    import torch
+
+    _req(q, "q", torch.bfloat16)
+    dev = q.device
+    _req(k_cache, "k_cache", torch.bfloat16, dev)
+    _req(v_cache, "v_cache", torch.bfloat16, dev)
+    _req(cache_len, "cache_len", torch.int32, dev)
+    if v_cache.shape != k_cache.shape or q.dim() != 4 or k_cache.dim() != 4:
+        raise ValueError("bad q / cache shapes")
+    b, hq, s_active, d = q.shape
+    if block_table is not None:
+        _req(block_table, "block_table", block_table.dtype, dev)
+        if block_table.dtype not in (torch.int32, torch.uint32):
+            raise TypeError("block_table must hold 32-bit entries (uint32 bit patterns)")
+        if block_table.dim() != 2 or block_table.shape[0] != b:
+            raise ValueError("block_table must be [b, max_pages_per_seq]")
+        num_pages, hkv, page, dk = k_cache.shape
+        max_pages = block_table.shape[1]
+    else:
+        bb, hkv, ml, dk = k_cache.shape
+        if bb != b or ml != max_cache_len:
+            raise ValueError("a flat cache must be [b, hkv, max_cache_len, d]")
+        num_pages, page, max_pages = 0, 0, 0
+    if dk != d or cache_len.shape != (b,):
+        raise ValueError("head_dim or cache_len shape mismatch")
+    if o is None:
+        o = torch.empty((b, hq, s_active, d), dtype=o_dtype or torch.bfloat16, device=dev)
+    _req(o, "o", o.dtype, dev)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, dev)
+    dims = (b, hq, hkv, d, s_active, page, max_pages, num_pages, max_cache_len)
+    return o, dims
+
+
+def attn_fwd_decode_static_ws(q, k_cache, v_cache, block_table, cache_len, *,
+                              max_cache_len: int, scale: float | None = None, o=None, lse=None,
+                              o_dtype=None, kv_chunk: int = 0, stream=None):
+    """attn_fwd_decode without a workspace argument, for callers that cannot allocate
+    device memory: the split-KV scratch is the library's fixed 64 MiB device array.
+    Calls sharing it must not overlap on the GPU.  Same layouts as attn_fwd_decode."""
+    lib = load_library()
+    o, (b, hq, hkv, d, s_active, page, max_pages, num_pages, mcl) = _decode_marshal(
+        q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse, o_dtype)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(lib.attn_fwd_decode_static_ws(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                         _ptr(cache_len), b, hq, hkv, d, s_active, page, max_pages,
+                                         num_pages, mcl, sc, _ptr(o), _ptr(lse),
+                                         _dtype_code(o.dtype), kv_chunk, _stream_ptr(stream)),
+           "attn_fwd_decode_static_ws")
     return o, lse
 
 

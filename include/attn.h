@@ -132,6 +132,32 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
                             size_t workspace_bytes, void* stream);
 
 /*
+ * attn_fwd_decode_static_ws -- attn_fwd_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point; it exists for callers that
+ * must not call cudaMalloc or any other allocator when they run attention: code held to
+ * a fixed device-memory budget set up once at start-up, plug-ins hosted by a runtime that
+ * owns every device allocation, real-time loops that must stay out of the allocator.
+ *
+ * Same arguments, layouts, semantics and results as attn_fwd_decode, minus the workspace:
+ * the split-KV scratch is a fixed 64 MiB device array compiled into the library (present
+ * on every GPU that loads the library until the process exits).  A call whose scratch,
+ * attn_decode_workspace_bytes(b, hq, s_active, d, max_cache_len, kv_chunk), exceeds
+ * 64 MiB is rejected with ATTN_ERR_WORKSPACE and enqueues nothing.  All calls share the
+ * array, so calls that overlap on the GPU (on different streams, or from host threads
+ * without ordering between them) race and give unspecified results; order them on one
+ * stream.  The array needs no clearing: each call writes every part it later reads.
+ * The first call on a device, with that device current, looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream capture begins.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine is called.
+ */
+attn_status attn_fwd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
+                                      const uint32_t* block_table, const int32_t* cache_len,
+                                      int b, int hq, int hkv, int d, int s_active, int page_size,
+                                      int max_pages_per_seq, int num_pages, int max_cache_len,
+                                      float scale, void* o, float* lse, attn_dtype o_dtype,
+                                      int kv_chunk, void* stream);
+
+/*
  * attn_gen_mask_decode -- materialise the decode 0/1 mask that attn_fwd_decode applies
  * in registers ("Flash-Attention: Decode (TKG)", "gen_mask_tkg": type A `index <
  * cache length` and type C, the tril(ones(s_active)) block of the new tokens):

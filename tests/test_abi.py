@@ -28,7 +28,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted([
         "attn_fwd_prefill", "attn_decode_workspace_bytes", "attn_fwd_decode",
-        "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string"])
+        "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
+        "attn_fwd_decode_static_ws"])
 
 
 def test_library_exports_every_declared_symbol(lib):
