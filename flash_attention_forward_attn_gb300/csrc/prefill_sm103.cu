@@ -12,18 +12,25 @@
 // and multi-head"); head_dim 256 simply widens the MMA contraction, the role the pages
 // give to d-tiling (optimum-neuron AGENTS.md, "flash_fwd_large_d").
 //
-// GB300 design (one CTA per 128-row query tile of one head, 8 warps):
+// GB300 design (one CTA per 128-row query tile of one head):
 //   warp 0    TMA producer: Q once, then K and V tiles through two 2-deep rings.
-//   warp 1    MMA issuer (one thread): S = Q K^T into TMEM (double-buffered), then
-//             O += P V into a TMEM accumulator that lives for the whole KV pass.
+//   warp 1    MMA issuer (one thread): S = Q K^T into one of two TMEM buffers, then
+//             O += P V into a TMEM accumulator that lives for the whole KV pass.  S(j+2)
+//             is issued as soon as the softmax has copied S(j) out of TMEM, so the tensor
+//             pipe holds the next scores while the softmax of tile j runs.
 //   warp 2    owns the TMEM allocation.
-//   warps 4-7 softmax: thread = query row = TMEM lane.  Reads its S row from TMEM,
-//             masks it if the tile crosses a band edge, folds scale*log2(e) into the
-//             exponent, writes P (bf16) into a 128-byte-swizzled shared-memory tile for
-//             the second MMA, and rescales O in TMEM only when the row max has grown by
-//             more than 2^8 since the last rescale (the stale max is used consistently
-//             for P and l, so O / l is unchanged).
-// The accumulator never leaves TMEM until the epilogue, so no O round trip through HBM
+//   softmax   one warpgroup per TMEM accumulator; thread = query row = TMEM lane.  With
+//             head_dim <= 128 two warpgroups take alternate KV tiles, each with its own
+//             running max, sum and O accumulator (S0, S1, O0, O1 fill the 512 TMEM columns),
+//             and the two partial results are merged once in the epilogue -- the
+//             split-KV identity of the online softmax, applied inside the CTA.  With
+//             head_dim 256 one warpgroup takes every tile.  Each thread reads its S row from
+//             TMEM, masks it if the tile crosses a band edge, folds scale*log2(e) into the
+//             exponent, writes P (bf16) into a 128-byte-swizzled shared-memory tile for the
+//             second MMA, and rescales its O in TMEM only when the row max has grown by more
+//             than 2^8 since the last rescale (the stale max is used consistently for P and
+//             l, so O / l is unchanged).
+// The accumulators never leave TMEM until the epilogue, so no O round trip through HBM
 // (the pages' sectioned design) is needed at any sequence length.
 #include <float.h>
 
@@ -35,11 +42,16 @@ namespace {
 
 __device__ unsigned g_prefill_error;
 
-constexpr int kThreads = 256;
 constexpr int kBM = 128;           // query rows per tile (= TMEM lanes)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold, log2 units
+// Registers after re-balancing: the TMA/MMA warpgroup gives up registers to the softmax
+// warpgroups.  128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch3 (the launch budget).
+constexpr int kRegsLaunch3 = 168;
+constexpr int kRegsLow = 64;
+constexpr int kRegsHigh = 216;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * kRegsLaunch3, "register split");
 
 template <int D>
 struct PrefillCfg {
@@ -55,8 +67,10 @@ struct PrefillCfg {
     static constexpr int kDynBytes = kSmem + 1024;
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 0;                    // S buffers at columns [0, 2 BN)
-    static constexpr int kOCol = 2 * BN;               // O at [2 BN, 2 BN + D)
-    static_assert(2 * BN + D <= kTmemCols, "TMEM budget");
+    static constexpr int kOCol = 2 * BN;               // O accumulators from column 2 BN
+    static constexpr int kSWG = 1;  // softmax warpgroups of this kernel
+    static constexpr int kThreads = 128 * (1 + kSWG);
+    static_assert(2 * BN + kSWG * D <= kTmemCols, "TMEM budget");
     static_assert(kDynBytes <= 232448, "shared memory budget");
 };
 
@@ -79,6 +93,11 @@ __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) 
     const int off = p.skv - p.sq;  // queries sit at the tail of the keys
     r.qpos_lo = r.q0 + off;
     r.qpos_hi = r.q0 + r.rows - 1 + off;
+    if (r.rows <= 0) {  // a query tile past the end of the sequence
+        r.kt0 = 0;
+        r.n = 0;
+        return r;
+    }
     const int k_end = p.causal ? min(p.skv, r.qpos_hi + 1) : p.skv;
     const int k_begin = p.window > 0 ? max(0, r.qpos_lo - p.window + 1) : 0;
     if (k_end <= k_begin) {
@@ -91,6 +110,9 @@ __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) 
     return r;
 }
 
+// Whether the accumulator of warpgroup w (tiles j = w, w + nw, ...) receives any tile.
+__device__ __forceinline__ bool have_any(int n, int w, int nw) { return (n - w + nw - 1) / nw > 0; }
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag) {
     return mbar_wait(bar, parity, reinterpret_cast<volatile int*>(abort_flag));
 }
@@ -102,11 +124,12 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
+__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     using C = PrefillCfg<D>;
     constexpr int BN = C::BN;
+    constexpr int NW = C::kSWG;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -148,9 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const uint32_t tmem = tmem_base_sh;
     const int n = tr.n;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n > 0) {
+    if (warp < 4) {
+        if constexpr (NW == 2) regs_dec<kRegsLow>();
+        if (warp == 0 && lane == 0 && n > 0) {
+            // -------------------------------------------------------- TMA producer
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
@@ -186,14 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                 for (int j = max(0, kdone - 2); j < kdone; ++j) wait_bounded(&k_full[j & 1], (j >> 1) & 1);
                 for (int j = max(0, vdone - 2); j < vdone; ++j) wait_bounded(&v_full[j & 1], (j >> 1) & 1);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n > 0) {
+        } else if (warp == 1 && lane == 0 && n > 0) {
+            // -------------------------------------------------------- MMA issuer
+            // S(0), S(1); then per tile j: O += P(j) V(j) once P(j) is in shared memory,
+            // followed by S(j+2) into the S buffer tile j has released.
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
             const uint32_t q_base = smem_u32(sm + C::kQOff);
-            const uint32_t tm_o = tmem + C::kOCol;
             bool ok = wait_or_abort(&q_full, 0, &abort_flag);
             tc_fence_after();
             auto issue_s = [&](int t) -> bool {
@@ -216,39 +239,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             if (ok && n > 1) ok = issue_s(1);
             for (int j = 0; ok && j < n; ++j) {
                 const int s = j & 1;
-                if (!wait_or_abort(&p_full[s], (j >> 1) & 1, &abort_flag)) break;
-                if (!wait_or_abort(&v_full[s], (j >> 1) & 1, &abort_flag)) break;
+                const uint32_t ph = (j >> 1) & 1;
+                if (!wait_or_abort(&p_full[s], ph, &abort_flag)) break;
+                if (!wait_or_abort(&v_full[s], ph, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t p_base = smem_u32(sm + C::kPOff + s * C::kPBytes);
                 const uint32_t v_base = smem_u32(sm + C::kVOff + s * C::kKVBytes);
+                const uint32_t tm_o = tmem + C::kOCol + (j % NW) * D;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t a = sw128_desc(p_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = sw128_desc(v_base + kk * (16 * 128), BN * 128, 1024);
-                    tc_mma_ss(tm_o, a, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ss(tm_o, a, b, idesc_o, (j >= NW || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&o_done[s]);
                 tc_commit(&v_empty[s]);
+                // S(j + 2) reuses the S buffer of tile j, which the softmax has read by now
                 if (j + 2 < n) ok = issue_s(j + 2);
             }
             tc_commit(&mma_drain);
             wait_bounded(&mma_drain, 0);
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ softmax
+        if constexpr (NW == 2) regs_inc<kRegsHigh>();
+        const int wg = (warp >> 2) - 1;  // this warpgroup takes tiles j with j % NW == wg
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tm_o = tmem + lane_off + C::kOCol + wg * D;
         const int q_row = tr.q0 + row;
         const int qpos = tr.qpos_lo + row;
         const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
         const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
         const float c = p.c;
         const bool c_pos = c > 0.f;
+        const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
+        for (int j = wg; j < n; j += NW) {
             const int s = j & 1;
-            if (!wait_or_abort(&s_full[s], (j >> 1) & 1, &abort_flag)) {
+            const uint32_t ph = (j >> 1) & 1;
+            if (!wait_or_abort(&s_full[s], ph, &abort_flag)) {
                 ok = false;
                 break;
             }
@@ -273,38 +304,42 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                     if (key < key_lo || key > key_hi) x[i] = -INFINITY;
                 }
             }
-            // row max with 8 independent chains (a single chain is latency-bound)
-            float mx[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
             if (!c_pos) {
 #pragma unroll
                 for (int i = 0; i < BN; ++i) x[i] *= c;
             }
+            // row max with 8 independent chains (a single chain is latency-bound)
+            float mx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
 #pragma unroll
             for (int i = 0; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
             float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             if (c_pos) tmax *= c;  // -inf stays -inf
-            // x holds raw scores when c > 0 (exponent = x*c - m), scaled scores otherwise
             const float m_new = fmaxf(m_used, tmax);
             const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
             if (m_used == -INFINITY) m_used = m_new;  // nothing accumulated yet for this row
+            // previous tile of this warpgroup: its PV wrote O_wg and read P buffer (j & 1)
+            const int jp = j - 2;
+            bool prev_done = jp < 0;
             if (__any_sync(0xffffffffu, need)) {
-                // O holds PV of the previous tile only after that MMA is done
-                if (!wait_or_abort(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, &abort_flag)) {
+                // O_wg holds this warpgroup's previous PV only once that MMA has finished
+                const int jo = j - NW;
+                if (!wait_or_abort(&o_done[jo & 1], (jo >> 1) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
+                if (NW == 2) prev_done = true;
                 tc_fence_after();
                 const float alpha = need ? ex2(m_used - m_new) : 1.0f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_off + C::kOCol + c0, r);
+                    tmem_ld32(tm_o + c0, r);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st32(tmem + lane_off + C::kOCol + c0, r);
+                    tmem_st32(tm_o + c0, r);
                 }
                 tmem_wait_st();
                 if (need) {
@@ -313,67 +348,110 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                 }
             }
             const float m_e = (m_used == -INFINITY) ? 0.f : m_used;
-            const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m_e
-            uint8_t* pbuf = sm + C::kPOff + s * C::kPBytes;
+            uint32_t pk[BN / 2];
             float ls[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) ls[u] = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < BN / 8; ++ch) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2(fmaf(x[ch * 8 + 2 * e], cm, -m_e));
-                    const float p1 = ex2(fmaf(x[ch * 8 + 2 * e + 1], cm, -m_e));
-                    ls[2 * e] += p0;
-                    ls[2 * e + 1] += p1;
-                    pk[e] = pack_bf16(p0, p1);
-                }
-                const uint32_t off = (ch >> 3) * (kBM * 128) + sw128_off(row, ch & 7);
-                *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int i = 0; i < BN / 2; ++i) {
+                const float p0 = ex2(fmaf(x[2 * i], cm, -m_e));
+                const float p1 = ex2(fmaf(x[2 * i + 1], cm, -m_e));
+                ls[(2 * i) & 7] += p0;
+                ls[(2 * i + 1) & 7] += p1;
+                pk[i] = pack_bf16(p0, p1);
             }
             l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            // P buffer (j & 1) was last read by PV(j - 2)
+            if (!prev_done && !wait_or_abort(&o_done[jp & 1], (jp >> 1) & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            uint8_t* pbuf = sm + C::kPOff + s * C::kPBytes;
+#pragma unroll
+            for (int ch = 0; ch < BN / 8; ++ch) {
+                const uint32_t off = (ch >> 3) * (kBM * 128) + sw128_off(row, ch & 7);
+                *reinterpret_cast<uint4*>(pbuf + off) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&p_full[s]);
         }
         // ------------------------------------------------------------ epilogue
-        bool have_o = false;
-        if (ok && n > 0) {
-            have_o = wait_or_abort(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, &abort_flag);
-            tc_fence_after();
+        // Warpgroup wg owns output columns [wg*D/NW, (wg+1)*D/NW) and merges every
+        // warpgroup's (m, l, O) for them:  M = max m_w, w_w = 2^(m_w - M),
+        // O = sum_w w_w O_w / sum_w w_w l_w,  LSE = (M + log2 sum_w w_w l_w) ln 2.
+        // The merge scratch lives in the Q tile: every S MMA (the only reader of Q) has
+        // finished once any PV commit has been observed after the last S was issued.
+        float* xch = reinterpret_cast<float*>(sm + C::kQOff);  // [NW][2][kBM]
+        bool have = ok;
+        for (int w = 0; w < NW; ++w) {  // wait for the last PV into every accumulator
+            const int nw = (n - w + NW - 1) / NW;
+            if (nw > 0) {
+                const int jl = w + (nw - 1) * NW;
+                have = wait_or_abort(&o_done[jl & 1], (jl >> 1) & 1, &abort_flag) && have;
+            }
+        }
+        tc_fence_after();
+        if constexpr (NW == 2) {
+            xch[(wg * 2 + 0) * kBM + row] = m_used;
+            xch[(wg * 2 + 1) * kBM + row] = l_sum;
+            asm volatile("bar.sync 1, %0;" ::"n"(256) : "memory");
+        }
+        float M = -INFINITY, wts[NW], L = 0.f;
+        bool has_o[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float mw = (NW == 2) ? xch[(w * 2 + 0) * kBM + row] : m_used;
+            M = fmaxf(M, mw);
+        }
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float mw = (NW == 2) ? xch[(w * 2 + 0) * kBM + row] : m_used;
+            const float lw = (NW == 2) ? xch[(w * 2 + 1) * kBM + row] : l_sum;
+            has_o[w] = (n - w + NW - 1) / NW > 0;  // this accumulator received at least one PV
+            wts[w] = (has_o[w] && mw != -INFINITY) ? ex2(mw - M) : 0.f;
+            L += wts[w] * lw;
         }
         const bool row_valid = q_row < p.sq;
-        const bool live = have_o && l_sum > 0.f;
-        const float inv = live ? 1.0f / l_sum : 0.f;
+        const bool live = have && L > 0.f;
+        const float inv = live ? 1.0f / L : 0.f;
         const size_t orow = (size_t)bh * p.sq + q_row;
-        if (row_valid && p.lse != nullptr)
-            p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+        if (wg == 0 && row_valid && p.lse != nullptr)
+            p.lse[orow] = live ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        constexpr int OC = D / NW;  // output columns per warpgroup
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            if (have_o) {
-                tmem_ld32(tmem + lane_off + C::kOCol + c0, r);
-            } else {
+        for (int c0 = 0; c0 < OC; c0 += 32) {
+            float acc[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                if (n > 0 && have_any(n, w, NW)) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_off + C::kOCol + w * D + wg * OC + c0, r);
+                    if (wts[w] != 0.f) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[i] = fmaf(wts[w], __uint_as_float(r[i]), acc[i]);
+                    }
+                }
             }
             if (!row_valid) continue;
+            const int oc = wg * OC + c0;
             if (p.o_f32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + oc);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                         __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                    dst[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv,
+                                         acc[4 * i + 3] * inv);
             } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + oc);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(
-                        pack_bf16(__uint_as_float(r[8 * i]) * inv, __uint_as_float(r[8 * i + 1]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv));
+                    dst[i] = make_uint4(pack_bf16(acc[8 * i] * inv, acc[8 * i + 1] * inv),
+                                        pack_bf16(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                                        pack_bf16(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
+                                        pack_bf16(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
             }
         }
     }
@@ -382,6 +460,357 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     tc_fence_after();
     if (threadIdx.x == 0 && abort_flag) atomicOr(&g_prefill_error, kDevErrTimeout);
     if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// =========================================================================== two q-tiles
+// Shared-memory / TMEM plan of the two-q-tile kernel (head_dim 64 or 128, BN = 128):
+// Q_A, Q_B stay resident; K and V tiles stream through one ring of kSlots slots in the
+// order K(j), V(j), K(j+1), ...; S_A, S_B, O_A, O_B fill the 512 TMEM columns and P_X is
+// written back into the first BN/2 columns of S_X as packed bf16 pairs.
+template <int D>
+struct Cfg2Q {
+    static constexpr int BN = 128;
+    static constexpr int kQBytes = D * kBM * 2;
+    static constexpr int kSlotBytes = D * BN * 2;
+    static constexpr int kSlots = (D == 128) ? 5 : 8;
+    static constexpr int kQAOff = 0;
+    static constexpr int kQBOff = kQBytes;
+    static constexpr int kRingOff = 2 * kQBytes;
+    static constexpr int kSmem = kRingOff + kSlots * kSlotBytes;
+    static constexpr int kDynBytes = kSmem + 1024;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kThreads = 384;
+    static_assert(2 * BN + 2 * D <= kTmemCols, "TMEM budget");
+    static_assert(kDynBytes + 512 <= 232448, "shared memory budget");
+};
+
+// One CTA = query rows [256 p, 256 p + 256) of one head, as tiles A (first 128 rows) and B.
+// Warps 0-3: TMA producer (warp 0), MMA issuer (warp 1), TMEM owner (warp 2).
+// Warps 4-7: softmax of tile A; warps 8-11: softmax of tile B (thread = row = TMEM lane).
+// Per KV tile j the MMA issuer runs  O_A += P_A(j-1) V(j-1),  S_A = Q_A K(j)^T,
+// O_B += P_B(j-1) V(j-1),  S_B = Q_B K(j)^T, so while one softmax warpgroup works on its
+// scores the tensor pipe holds the other tile's two products.  P_X(j-1) lives in S_X's
+// TMEM columns; the product that reads it is issued before the one that overwrites S_X,
+// and the two run in issue order on the tensor pipe.
+template <int D>
+__global__ void __launch_bounds__(384, 1) prefill2q_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+    using C = Cfg2Q<D>;
+    constexpr int BN = C::BN;
+    constexpr int NS = C::kSlots;
+    extern __shared__ uint8_t dyn_smem[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t q_full, ring_full[NS], ring_empty[NS];
+    __shared__ uint64_t s_full[2], p_full[2], o_done[2], mma_drain;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int npairs = (p.nqt + 1) / 2;
+    const int nbh = gridDim.x / npairs;
+    const int pair = npairs - 1 - (int)(blockIdx.x / nbh);  // heaviest causal pairs first
+    const int bh = (int)(blockIdx.x % nbh);
+    const int bidx = bh / p.hq, h = bh % p.hq;
+    const int kvz = bidx * p.hkv + h / p.group;
+    TileRange tx[2];
+    tx[0] = tile_range<BN>(p, 2 * pair);
+    tx[1] = tile_range<BN>(p, 2 * pair + 1);  // rows <= 0 (past sq) gives n = 0
+    // union of the two KV ranges
+    int u0 = INT_MAX, u1 = INT_MIN;
+    for (int x = 0; x < 2; ++x)
+        if (tx[x].n > 0) {
+            u0 = min(u0, tx[x].kt0);
+            u1 = max(u1, tx[x].kt0 + tx[x].n);
+        }
+    const int nu = (u1 > u0) ? u1 - u0 : 0;
+    const bool has_b = tx[1].rows > 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&q_full, 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&ring_full[i], 1);
+            mbar_init(&ring_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(&mma_drain, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(&tmem_base_sh, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    const uint32_t col_s[2] = {0u, (uint32_t)BN};
+    const uint32_t col_o[2] = {(uint32_t)(2 * BN), (uint32_t)(2 * BN + D)};
+
+    if (warp < 4) {
+        regs_dec<kRegsLow>();
+        if (warp == 0 && lane == 0 && nu > 0) {
+            // -------------------------------------------------------- TMA producer
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(&q_full, (has_b ? 2 : 1) * C::kQBytes);
+            for (int x = 0; x < (has_b ? 2 : 1); ++x)
+#pragma unroll
+                for (int dc = 0; dc < D / 64; ++dc)
+                    tma_load_3d(sm + (x ? C::kQBOff : C::kQAOff) + dc * (kBM * 128), &tm_q, dc * 64,
+                                tx[x].q0, bh, &q_full);
+            int issued = 0;
+            for (int L = 0; L < 2 * nu; ++L) {
+                const int slot = L % NS;
+                if (L >= NS && !wait_or_abort(&ring_empty[slot], ((L / NS) - 1) & 1, &abort_flag)) break;
+                const int k0 = (u0 + (L >> 1)) * BN;
+                mbar_arrive_expect_tx(&ring_full[slot], C::kSlotBytes);
+                const CUtensorMap* tm = (L & 1) ? &tm_v : &tm_k;
+#pragma unroll
+                for (int dc = 0; dc < D / 64; ++dc)
+                    tma_load_3d(sm + C::kRingOff + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64,
+                                k0, kvz, &ring_full[slot]);
+                issued = L + 1;
+            }
+            if (abort_flag) {  // let copies in flight land before the CTA exits
+                wait_bounded(&q_full, 0);
+                for (int L = max(0, issued - NS); L < issued; ++L)
+                    wait_bounded(&ring_full[L % NS], (L / NS) & 1);
+            }
+        } else if (warp == 1 && lane == 0 && nu > 0) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
+            bool ok = wait_or_abort(&q_full, 0, &abort_flag);
+            tc_fence_after();
+            int cnt[2] = {0, 0};  // tiles of A / B whose S has been issued
+            for (int j = u0; ok && j <= u1; ++j) {
+                const int jj = j - u0;
+                const bool have_k = j < u1;
+                if (have_k) {
+                    const int L = 2 * jj;
+                    ok = wait_or_abort(&ring_full[L % NS], (L / NS) & 1, &abort_flag);
+                    if (!ok) break;
+                }
+                const bool have_v = j > u0;
+                if (have_v) {
+                    const int L = 2 * (jj - 1) + 1;
+                    ok = wait_or_abort(&ring_full[L % NS], (L / NS) & 1, &abort_flag);
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(sm + C::kRingOff + ((2 * jj) % NS) * C::kSlotBytes);
+                const uint32_t v_base = smem_u32(sm + C::kRingOff + ((2 * jj - 1 + NS) % NS) * C::kSlotBytes);
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const TileRange& t = tx[x];
+                    // O_X += P_X(j-1) V(j-1)
+                    if (have_v && j - 1 >= t.kt0 && j - 1 < t.kt0 + t.n) {
+                        const int i = (j - 1) - t.kt0;  // this tile's index within X's range
+                        if (!wait_or_abort(&p_full[x], i & 1, &abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint64_t b = sw128_desc(v_base + kk * (16 * 128), BN * 128, 1024);
+                            tc_mma_ts(tmem + col_o[x], tmem + col_s[x] + kk * 8, b, idesc_o,
+                                      (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (i == t.n - 1) tc_commit(&o_done[x]);  // the last product into O_X
+                    }
+                    // S_X = Q_X K(j)^T
+                    if (have_k && j >= t.kt0 && j < t.kt0 + t.n) {
+                        const uint32_t q_base = smem_u32(sm + (x ? C::kQBOff : C::kQAOff));
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t a = sw128_desc(q_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+                            const uint64_t b = sw128_desc(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+                            tc_mma_ss(tmem + col_s[x], a, b, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(&s_full[x]);
+                        ++cnt[x];
+                    }
+                }
+                if (!ok) break;
+                if (have_k) tc_commit(&ring_empty[(2 * jj) % NS]);           // K(j) consumed
+                if (have_v) tc_commit(&ring_empty[(2 * jj - 1 + NS) % NS]);  // V(j-1) consumed
+            }
+            tc_commit(&mma_drain);
+            wait_bounded(&mma_drain, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        regs_inc<kRegsHigh>();
+        const int x = (warp >> 2) - 1;  // 0: tile A, 1: tile B
+        const TileRange t = x ? tx[1] : tx[0];
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tm_s = tmem + lane_off + (x ? col_s[1] : col_s[0]);
+        const uint32_t tm_o = tmem + lane_off + (x ? col_o[1] : col_o[0]);
+        const int q_row = t.q0 + row;
+        const int qpos = t.qpos_lo + row;
+        const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
+        const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+        const float c = p.c;
+        const bool c_pos = c > 0.f;
+        const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
+        float m_used = -INFINITY, l_sum = 0.f;
+        bool ok = true;
+        for (int i = 0; i < t.n; ++i) {
+            if (!wait_or_abort(x ? &s_full[1] : &s_full[0], i & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float v[BN];
+            {
+                uint32_t r[BN];
+                tmem_ld128(tm_s, r);
+#pragma unroll
+                for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(r[e]);
+            }
+            const int k0 = (t.kt0 + i) * BN;
+            const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
+                              (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
+            if (edge) {
+#pragma unroll
+                for (int e = 0; e < BN; ++e) {
+                    const int key = k0 + e;
+                    if (key < key_lo || key > key_hi) v[e] = -INFINITY;
+                }
+            }
+            if (!c_pos) {
+#pragma unroll
+                for (int e = 0; e < BN; ++e) v[e] *= c;
+            }
+            float mx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
+            float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            if (c_pos) tmax *= c;  // -inf stays -inf
+            const float m_new = fmaxf(m_used, tmax);
+            const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
+            if (m_used == -INFINITY) m_used = m_new;  // nothing accumulated yet for this row
+            if (__any_sync(0xffffffffu, need)) {
+                // O_X = previous PVs: all finished, since S_X(i) was issued after them
+                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tm_o + c0, r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_st32(tm_o + c0, r);
+                }
+                if (need) {
+                    l_sum *= alpha;
+                    m_used = m_new;
+                }
+            }
+            const float m_e = (m_used == -INFINITY) ? 0.f : m_used;
+            uint32_t pk[BN / 2];
+            float ls[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+            for (int e = 0; e < BN / 2; ++e) {
+                const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
+                const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
+                ls[(2 * e) & 7] += p0;
+                ls[(2 * e + 1) & 7] += p1;
+                pk[e] = pack_bf16(p0, p1);
+            }
+            l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            tmem_st64(tm_s, pk);  // P_X over the first BN/2 columns of S_X
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(x ? &p_full[1] : &p_full[0]);
+        }
+        // ------------------------------------------------------------ epilogue
+        bool have_o = false;
+        if (ok && t.n > 0) {
+            have_o = wait_or_abort(x ? &o_done[1] : &o_done[0], 0, &abort_flag);
+            tc_fence_after();
+        }
+        const bool row_valid = t.rows > 0 && row < t.rows;
+        const bool live = have_o && l_sum > 0.f;
+        const float inv = live ? 1.0f / l_sum : 0.f;
+        const size_t orow = (size_t)bh * p.sq + q_row;
+        if (row_valid && p.lse != nullptr)
+            p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            if (t.n > 0) {
+                tmem_ld32(tm_o + c0, r);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = 0u;
+            }
+            if (!row_valid) continue;
+            if (p.o_f32) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                         __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_uint4(
+                        pack_bf16(__uint_as_float(r[8 * e]) * inv, __uint_as_float(r[8 * e + 1]) * inv),
+                        pack_bf16(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv),
+                        pack_bf16(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv),
+                        pack_bf16(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0 && abort_flag) atomicOr(&g_prefill_error, kDevErrTimeout);
+    if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D>
+attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
+    using C = Cfg2Q<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(prefill2q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kDynBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        // setmaxnreg.inc waits until the launch's register pool can serve it; the split is
+        // sized for exactly kRegsLaunch3 registers per thread at launch.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, prefill2q_kernel<D>) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        if (fa.numRegs != kRegsLaunch3) return ATTN_ERR_UNSUPPORTED;
+        attr_set = true;
+    }
+    const long long grid = (long long)((p.nqt + 1) / 2) * a.b * a.hq;
+    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    prefill2q_kernel<D><<<(unsigned)grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 template <int D>
@@ -413,6 +842,9 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     p.causal = a.causal;
     p.o_f32 = a.o_dtype == ATTN_F32 ? 1 : 0;
     p.c = a.scale * kLog2e;
+    if constexpr (D <= 128) {
+        return prefill2q_launch<D>(a, tq, tk, tv, p, stream);
+    } else {
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -420,13 +852,24 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
+        if (C::kSWG == 2) {
+            // setmaxnreg.inc waits until the launch's register pool can serve it; the split
+            // above is sized for exactly kRegsLaunch3 registers per thread at launch.
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, prefill_kernel<D>) != cudaSuccess) {
+                cudaGetLastError();
+                return ATTN_ERR_CUDA;
+            }
+            if (fa.numRegs != kRegsLaunch3) return ATTN_ERR_UNSUPPORTED;
+        }
         attr_set = true;
     }
     const long long grid = (long long)p.nqt * a.b * a.hq;
     if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    prefill_kernel<D><<<(unsigned)grid, kThreads, C::kDynBytes, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D><<<(unsigned)grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
+    }
 }
 
 }  // namespace
