@@ -12,7 +12,10 @@
 // and multi-head"); head_dim 256 simply widens the MMA contraction, the role the pages
 // give to d-tiling (optimum-neuron AGENTS.md, "flash_fwd_large_d").
 //
-// GB300 design (one CTA per 128-row query tile of one head):
+// GB300 design.  Two kernels share the method: for head_dim 64 and 128 a CTA owns two
+// 128-row query tiles that share every K/V tile (the two-q-tile kernel below); for
+// head_dim 256 the two accumulators would not fit TMEM, so a CTA owns one tile (the
+// one-q-tile kernel).  The common structure, per CTA:
 //   warp 0    TMA producer: Q once, then K and V tiles through two 2-deep rings.
 //   warp 1    MMA issuer (one thread): S = Q K^T into one of two TMEM buffers, then
 //             O += P V into a TMEM accumulator that lives for the whole KV pass.  S(j+2)
@@ -53,27 +56,6 @@ constexpr int kRegsLow = 64;
 constexpr int kRegsHigh = 216;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * kRegsLaunch3, "register split");
 
-template <int D>
-struct PrefillCfg {
-    static constexpr int BN = (D == 256) ? 64 : 128;   // keys per tile
-    static constexpr int kQBytes = D * kBM * 2;        // D/64 boxes of 128 rows x 128 B
-    static constexpr int kKVBytes = D * BN * 2;        // D/64 boxes of BN rows x 128 B
-    static constexpr int kPBytes = BN * kBM * 2;       // BN/64 boxes of 128 rows x 128 B
-    static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + kQBytes;
-    static constexpr int kVOff = kKOff + 2 * kKVBytes;
-    static constexpr int kPOff = kVOff + 2 * kKVBytes;
-    static constexpr int kSmem = kPOff + 2 * kPBytes;
-    static constexpr int kDynBytes = kSmem + 1024;
-    static constexpr int kTmemCols = 512;
-    static constexpr int kSCol = 0;                    // S buffers at columns [0, 2 BN)
-    static constexpr int kOCol = 2 * BN;               // O accumulators from column 2 BN
-    static constexpr int kSWG = 1;  // softmax warpgroups of this kernel
-    static constexpr int kThreads = 128 * (1 + kSWG);
-    static_assert(2 * BN + kSWG * D <= kTmemCols, "TMEM budget");
-    static_assert(kDynBytes <= 232448, "shared memory budget");
-};
-
 struct PrefillParams {
     void* o;
     float* lse;
@@ -110,9 +92,6 @@ __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) 
     return r;
 }
 
-// Whether the accumulator of warpgroup w (tiles j = w, w + nw, ...) receives any tile.
-__device__ __forceinline__ bool have_any(int n, int w, int nw) { return (n - w + nw - 1) / nw > 0; }
-
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag) {
     return mbar_wait(bar, parity, reinterpret_cast<volatile int*>(abort_flag));
 }
@@ -123,17 +102,50 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
         if (clock64() - t0 > kWaitLimitCycles) return;
 }
 
+// =========================================================================== one q-tile
+// Shared-memory / TMEM plan of the one-q-tile kernel (head_dim 256, BN = 64): Q stays
+// resident; K streams through a 3-slot ring (two tiles ahead) and V through a 2-slot
+// ring, each fed by its own producer thread so a K load never waits behind a V slot;
+// S is double-buffered in TMEM (2 x BN columns), O takes D columns, and P(j) is written
+// back into the first BN/2 columns of S(j)'s buffer as packed bf16 pairs.
 template <int D>
-__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
+struct Cfg1Q {
+    static constexpr int BN = 64;
+    static constexpr int kQBytes = D * kBM * 2;
+    static constexpr int kSlotBytes = D * BN * 2;
+    static constexpr int kKSlots = 3;      // K runs two tiles ahead of the tile in use
+    static constexpr int kVSlots = 2;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQBytes;
+    static constexpr int kVOff = kKOff + kKSlots * kSlotBytes;
+    static constexpr int kSmem = kVOff + kVSlots * kSlotBytes;
+    static constexpr int kDynBytes = kSmem + 1024;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSCol = 0;        // S buffers at [0, 2 BN)
+    static constexpr int kOCol = 2 * BN;   // O at [2 BN, 2 BN + D)
+    static constexpr int kThreads = 256;
+    static_assert(2 * BN + D <= kTmemCols, "TMEM budget");
+    static_assert(kDynBytes + 512 <= 232448, "shared memory budget");
+};
+
+// One CTA = one 128-row query tile of one head.  Warp 0: TMA producer of Q and K; warp 3:
+// TMA producer of V; warp 1: MMA issuer; warp 2: TMEM owner; warps 4-7: softmax (thread =
+// row = TMEM lane).  MMA order:
+// S(0), S(1), then per tile j: O += P(j) V(j) (P from TMEM), S(j+2) into the buffer that
+// held S(j) and P(j) -- the product reading P(j) is issued first and the tensor pipe runs
+// them in issue order.  The softmax of tile j+1 overlaps PV(j) and S(j+2).
+template <int D>
+__global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using C = PrefillCfg<D>;
+    using C = Cfg1Q<D>;
     constexpr int BN = C::BN;
-    constexpr int NW = C::kSWG;
+    constexpr int NK = C::kKSlots;
+    constexpr int NV = C::kVSlots;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2];
+    __shared__ uint64_t q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[2], p_full[2], o_done[2], mma_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
@@ -145,14 +157,19 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
     const int bidx = bh / p.hq, h = bh % p.hq;
     const int kvz = bidx * p.hkv + h / p.group;
     const TileRange tr = tile_range<BN>(p, qt);
+    const int n = tr.n;
 
     if (threadIdx.x == 0) {
         mbar_init(&q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NK; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < NV; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
             mbar_init(&o_done[i], 1);
@@ -169,104 +186,95 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    const int n = tr.n;
 
-    if (warp < 4) {
-        if constexpr (NW == 2) regs_dec<kRegsLow>();
-        if (warp == 0 && lane == 0 && n > 0) {
-            // -------------------------------------------------------- TMA producer
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(&q_full, C::kQBytes);
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------------------ TMA producers
+        if (lane == 0 && n > 0) {
+            const bool is_k = warp == 0;
+            const int ns = is_k ? NK : NV;
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
+            if (is_k) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                mbar_arrive_expect_tx(&q_full, C::kQBytes);
 #pragma unroll
-            for (int dc = 0; dc < D / 64; ++dc)
-                tma_load_3d(sm + C::kQOff + dc * (kBM * 128), &tm_q, dc * 64, tr.q0, bh, &q_full);
+                for (int dc = 0; dc < D / 64; ++dc)
+                    tma_load_3d(sm + C::kQOff + dc * (kBM * 128), &tm_q, dc * 64, tr.q0, bh, &q_full);
+            } else {
+                tma_prefetch_desc(&tm_v);
+            }
             int issued = 0;
             for (int j = 0; j < n; ++j) {
-                const int s = j & 1;
+                const int slot = j % ns;
+                if (j >= ns && !wait_or_abort(&empty[slot], ((j / ns) - 1) & 1, &abort_flag)) break;
                 const int k0 = (tr.kt0 + j) * BN;
-                if (j >= 2 && !wait_or_abort(&k_empty[s], ((j >> 1) - 1) & 1, &abort_flag)) break;
-                mbar_arrive_expect_tx(&k_full[s], C::kKVBytes);
+                mbar_arrive_expect_tx(&full[slot], C::kSlotBytes);
 #pragma unroll
                 for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(sm + C::kKOff + s * C::kKVBytes + dc * (BN * 128), &tm_k, dc * 64,
-                                k0, kvz, &k_full[s]);
-                if (j >= 2 && !wait_or_abort(&v_empty[s], ((j >> 1) - 1) & 1, &abort_flag)) {
-                    issued = -(j + 1);  // K of tile j issued, V not
-                    break;
-                }
-                mbar_arrive_expect_tx(&v_full[s], C::kKVBytes);
-#pragma unroll
-                for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(sm + C::kVOff + s * C::kKVBytes + dc * (BN * 128), &tm_v, dc * 64,
-                                k0, kvz, &v_full[s]);
+                    tma_load_3d(ring + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64, k0, kvz,
+                                &full[slot]);
                 issued = j + 1;
             }
             if (abort_flag) {  // let copies in flight land before the CTA exits
-                wait_bounded(&q_full, 0);
-                const int kdone = issued < 0 ? -issued : issued;
-                const int vdone = issued < 0 ? -issued - 1 : issued;
-                for (int j = max(0, kdone - 2); j < kdone; ++j) wait_bounded(&k_full[j & 1], (j >> 1) & 1);
-                for (int j = max(0, vdone - 2); j < vdone; ++j) wait_bounded(&v_full[j & 1], (j >> 1) & 1);
+                if (is_k) wait_bounded(&q_full, 0);
+                for (int j = max(0, issued - ns); j < issued; ++j)
+                    wait_bounded(&full[j % ns], (j / ns) & 1);
             }
-        } else if (warp == 1 && lane == 0 && n > 0) {
-            // -------------------------------------------------------- MMA issuer
-            // S(0), S(1); then per tile j: O += P(j) V(j) once P(j) is in shared memory,
-            // followed by S(j+2) into the S buffer tile j has released.
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
             const uint32_t q_base = smem_u32(sm + C::kQOff);
             bool ok = wait_or_abort(&q_full, 0, &abort_flag);
             tc_fence_after();
             auto issue_s = [&](int t) -> bool {
-                const int s = t & 1;
-                if (!wait_or_abort(&k_full[s], (t >> 1) & 1, &abort_flag)) return false;
+                const int slot = t % NK;
+                if (!wait_or_abort(&k_full[slot], (t / NK) & 1, &abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(sm + C::kKOff + s * C::kKVBytes);
-                const uint32_t tm_s = tmem + C::kSCol + s * BN;
+                const uint32_t k_base = smem_u32(sm + C::kKOff + slot * C::kSlotBytes);
+                const uint32_t tm_s = tmem + C::kSCol + (t & 1) * BN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t a = sw128_desc(q_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = sw128_desc(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
                     tc_mma_ss(tm_s, a, b, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(&s_full[s]);
-                tc_commit(&k_empty[s]);
+                tc_commit(&s_full[t & 1]);
+                tc_commit(&k_empty[slot]);  // K(t) consumed once this product is done
                 return true;
             };
             if (ok) ok = issue_s(0);
             if (ok && n > 1) ok = issue_s(1);
             for (int j = 0; ok && j < n; ++j) {
                 const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!wait_or_abort(&p_full[s], ph, &abort_flag)) break;
-                if (!wait_or_abort(&v_full[s], ph, &abort_flag)) break;
+                if (!wait_or_abort(&p_full[s], (j >> 1) & 1, &abort_flag)) break;
+                const int slot = j % NV;
+                if (!wait_or_abort(&v_full[slot], (j / NV) & 1, &abort_flag)) break;
                 tc_fence_after();
-                const uint32_t p_base = smem_u32(sm + C::kPOff + s * C::kPBytes);
-                const uint32_t v_base = smem_u32(sm + C::kVOff + s * C::kKVBytes);
-                const uint32_t tm_o = tmem + C::kOCol + (j % NW) * D;
+                const uint32_t v_base = smem_u32(sm + C::kVOff + slot * C::kSlotBytes);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t a = sw128_desc(p_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = sw128_desc(v_base + kk * (16 * 128), BN * 128, 1024);
-                    tc_mma_ss(tm_o, a, b, idesc_o, (j >= NW || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + C::kOCol, tmem + C::kSCol + s * BN + kk * 8, b, idesc_o,
+                              (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&o_done[s]);
-                tc_commit(&v_empty[s]);
-                // S(j + 2) reuses the S buffer of tile j, which the softmax has read by now
+                tc_commit(&v_empty[slot]);  // V(j) consumed
                 if (j + 2 < n) ok = issue_s(j + 2);
             }
             tc_commit(&mma_drain);
             wait_bounded(&mma_drain, 0);
         }
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax
-        if constexpr (NW == 2) regs_inc<kRegsHigh>();
-        const int wg = (warp >> 2) - 1;  // this warpgroup takes tiles j with j % NW == wg
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tm_o = tmem + lane_off + C::kOCol + wg * D;
+        const uint32_t tm_o = tmem + lane_off + C::kOCol;
         const int q_row = tr.q0 + row;
         const int qpos = tr.qpos_lo + row;
         const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
@@ -276,61 +284,52 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
         const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
-        for (int j = wg; j < n; j += NW) {
+        for (int j = 0; j < n; ++j) {
             const int s = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
-            if (!wait_or_abort(&s_full[s], ph, &abort_flag)) {
+            if (!wait_or_abort(&s_full[s], (j >> 1) & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float x[BN];
+            const uint32_t tm_s = tmem + lane_off + C::kSCol + s * BN;
+            float v[BN];
             {
                 uint32_t r[BN];
-                if constexpr (BN == 128)
-                    tmem_ld128(tmem + lane_off + C::kSCol + s * BN, r);
-                else
-                    tmem_ld64(tmem + lane_off + C::kSCol + s * BN, r);
+                tmem_ld64(tm_s, r);
 #pragma unroll
-                for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(r[i]);
+                for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(r[e]);
             }
             const int k0 = (tr.kt0 + j) * BN;
             const bool edge = (p.causal && k0 + BN - 1 > tr.qpos_lo) || (k0 + BN > p.skv) ||
                               (p.window > 0 && k0 < tr.qpos_hi - p.window + 1);
             if (edge) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    const int key = k0 + i;
-                    if (key < key_lo || key > key_hi) x[i] = -INFINITY;
+                for (int e = 0; e < BN; ++e) {
+                    const int key = k0 + e;
+                    if (key < key_lo || key > key_hi) v[e] = -INFINITY;
                 }
             }
             if (!c_pos) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) x[i] *= c;
+                for (int e = 0; e < BN; ++e) v[e] *= c;
             }
-            // row max with 8 independent chains (a single chain is latency-bound)
             float mx[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+            for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
             float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             if (c_pos) tmax *= c;  // -inf stays -inf
             const float m_new = fmaxf(m_used, tmax);
             const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
             if (m_used == -INFINITY) m_used = m_new;  // nothing accumulated yet for this row
-            // previous tile of this warpgroup: its PV wrote O_wg and read P buffer (j & 1)
-            const int jp = j - 2;
-            bool prev_done = jp < 0;
             if (__any_sync(0xffffffffu, need)) {
-                // O_wg holds this warpgroup's previous PV only once that MMA has finished
-                const int jo = j - NW;
-                if (!wait_or_abort(&o_done[jo & 1], (jo >> 1) & 1, &abort_flag)) {
+                // O holds PV(j-1) only once that product has finished
+                if (!wait_or_abort(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (NW == 2) prev_done = true;
                 tc_fence_after();
                 const float alpha = need ? ex2(m_used - m_new) : 1.0f;
 #pragma unroll 1
@@ -338,10 +337,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
                     uint32_t r[32];
                     tmem_ld32(tm_o + c0, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
                     tmem_st32(tm_o + c0, r);
                 }
-                tmem_wait_st();
                 if (need) {
                     l_sum *= alpha;
                     m_used = m_new;
@@ -353,105 +351,56 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
 #pragma unroll
             for (int u = 0; u < 8; ++u) ls[u] = 0.f;
 #pragma unroll
-            for (int i = 0; i < BN / 2; ++i) {
-                const float p0 = ex2(fmaf(x[2 * i], cm, -m_e));
-                const float p1 = ex2(fmaf(x[2 * i + 1], cm, -m_e));
-                ls[(2 * i) & 7] += p0;
-                ls[(2 * i + 1) & 7] += p1;
-                pk[i] = pack_bf16(p0, p1);
+            for (int e = 0; e < BN / 2; ++e) {
+                const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
+                const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
+                ls[(2 * e) & 7] += p0;
+                ls[(2 * e + 1) & 7] += p1;
+                pk[e] = pack_bf16(p0, p1);
             }
             l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-            // P buffer (j & 1) was last read by PV(j - 2)
-            if (!prev_done && !wait_or_abort(&o_done[jp & 1], (jp >> 1) & 1, &abort_flag)) {
-                ok = false;
-                break;
-            }
-            uint8_t* pbuf = sm + C::kPOff + s * C::kPBytes;
-#pragma unroll
-            for (int ch = 0; ch < BN / 8; ++ch) {
-                const uint32_t off = (ch >> 3) * (kBM * 128) + sw128_off(row, ch & 7);
-                *reinterpret_cast<uint4*>(pbuf + off) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            }
-            fence_proxy_async_smem();
+            tmem_st32(tm_s, pk);  // P(j) over the first BN/2 columns of S(j)'s buffer
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_full[s]);
         }
         // ------------------------------------------------------------ epilogue
-        // Warpgroup wg owns output columns [wg*D/NW, (wg+1)*D/NW) and merges every
-        // warpgroup's (m, l, O) for them:  M = max m_w, w_w = 2^(m_w - M),
-        // O = sum_w w_w O_w / sum_w w_w l_w,  LSE = (M + log2 sum_w w_w l_w) ln 2.
-        // The merge scratch lives in the Q tile: every S MMA (the only reader of Q) has
-        // finished once any PV commit has been observed after the last S was issued.
-        float* xch = reinterpret_cast<float*>(sm + C::kQOff);  // [NW][2][kBM]
-        bool have = ok;
-        for (int w = 0; w < NW; ++w) {  // wait for the last PV into every accumulator
-            const int nw = (n - w + NW - 1) / NW;
-            if (nw > 0) {
-                const int jl = w + (nw - 1) * NW;
-                have = wait_or_abort(&o_done[jl & 1], (jl >> 1) & 1, &abort_flag) && have;
-            }
-        }
-        tc_fence_after();
-        if constexpr (NW == 2) {
-            xch[(wg * 2 + 0) * kBM + row] = m_used;
-            xch[(wg * 2 + 1) * kBM + row] = l_sum;
-            asm volatile("bar.sync 1, %0;" ::"n"(256) : "memory");
-        }
-        float M = -INFINITY, wts[NW], L = 0.f;
-        bool has_o[NW];
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float mw = (NW == 2) ? xch[(w * 2 + 0) * kBM + row] : m_used;
-            M = fmaxf(M, mw);
-        }
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float mw = (NW == 2) ? xch[(w * 2 + 0) * kBM + row] : m_used;
-            const float lw = (NW == 2) ? xch[(w * 2 + 1) * kBM + row] : l_sum;
-            has_o[w] = (n - w + NW - 1) / NW > 0;  // this accumulator received at least one PV
-            wts[w] = (has_o[w] && mw != -INFINITY) ? ex2(mw - M) : 0.f;
-            L += wts[w] * lw;
+        bool have_o = false;
+        if (ok && n > 0) {
+            have_o = wait_or_abort(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, &abort_flag);
+            tc_fence_after();
         }
         const bool row_valid = q_row < p.sq;
-        const bool live = have && L > 0.f;
-        const float inv = live ? 1.0f / L : 0.f;
+        const bool live = have_o && l_sum > 0.f;
+        const float inv = live ? 1.0f / l_sum : 0.f;
         const size_t orow = (size_t)bh * p.sq + q_row;
-        if (wg == 0 && row_valid && p.lse != nullptr)
-            p.lse[orow] = live ? (M + __log2f(L)) * kLn2 : -INFINITY;
-        constexpr int OC = D / NW;  // output columns per warpgroup
+        if (row_valid && p.lse != nullptr)
+            p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
 #pragma unroll 1
-        for (int c0 = 0; c0 < OC; c0 += 32) {
-            float acc[32];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            if (n > 0) {
+                tmem_ld32(tm_o + c0, r);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                if (n > 0 && have_any(n, w, NW)) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_off + C::kOCol + w * D + wg * OC + c0, r);
-                    if (wts[w] != 0.f) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[i] = fmaf(wts[w], __uint_as_float(r[i]), acc[i]);
-                    }
-                }
+                for (int e = 0; e < 32; ++e) r[e] = 0u;
             }
             if (!row_valid) continue;
-            const int oc = wg * OC + c0;
             if (p.o_f32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + oc);
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv,
-                                         acc[4 * i + 3] * inv);
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                         __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
             } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + oc);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pack_bf16(acc[8 * i] * inv, acc[8 * i + 1] * inv),
-                                        pack_bf16(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
-                                        pack_bf16(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
-                                        pack_bf16(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_uint4(
+                        pack_bf16(__uint_as_float(r[8 * e]) * inv, __uint_as_float(r[8 * e + 1]) * inv),
+                        pack_bf16(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv),
+                        pack_bf16(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv),
+                        pack_bf16(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv));
             }
         }
     }
@@ -460,6 +409,26 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1) prefill_kernel(
     tc_fence_after();
     if (threadIdx.x == 0 && abort_flag) atomicOr(&g_prefill_error, kDevErrTimeout);
     if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D>
+attn_status prefill1q_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
+    using C = Cfg1Q<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(prefill1q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kDynBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        attr_set = true;
+    }
+    const long long grid = (long long)p.nqt * a.b * a.hq;
+    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    prefill1q_kernel<D><<<(unsigned)grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 // =========================================================================== two q-tiles
@@ -815,7 +784,7 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
 
 template <int D>
 attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
-    using C = PrefillCfg<D>;
+    constexpr int BN = (D <= 128) ? Cfg2Q<(D <= 128 ? D : 128)>::BN : Cfg1Q<(D > 128 ? D : 256)>::BN;
     CUtensorMap tq, tk, tv;
     const uint64_t skv = a.skv > 0 ? (uint64_t)a.skv : 1u;
     uint64_t qd[3] = {(uint64_t)D, (uint64_t)a.sq, (uint64_t)a.b * a.hq};
@@ -823,7 +792,7 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     uint32_t qb[3] = {64u, (uint32_t)kBM, 1u};
     uint64_t kd[3] = {(uint64_t)D, skv, (uint64_t)a.b * a.hkv};
     uint64_t ks[2] = {(uint64_t)D * 2, skv * D * 2};
-    uint32_t kb[3] = {64u, (uint32_t)C::BN, 1u};
+    uint32_t kb[3] = {64u, (uint32_t)BN, 1u};
     const void* kp = a.skv > 0 ? a.k : a.q;  // never read when skv == 0
     const void* vp = a.skv > 0 ? a.v : a.q;
     if (!make_bf16_map(&tq, a.q, 3, qd, qs, qb) || !make_bf16_map(&tk, kp, 3, kd, ks, kb) ||
@@ -842,34 +811,10 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     p.causal = a.causal;
     p.o_f32 = a.o_dtype == ATTN_F32 ? 1 : 0;
     p.c = a.scale * kLog2e;
-    if constexpr (D <= 128) {
+    if constexpr (D <= 128)
         return prefill2q_launch<D>(a, tq, tk, tv, p, stream);
-    } else {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kDynBytes) != cudaSuccess) {
-            cudaGetLastError();
-            return ATTN_ERR_CUDA;
-        }
-        if (C::kSWG == 2) {
-            // setmaxnreg.inc waits until the launch's register pool can serve it; the split
-            // above is sized for exactly kRegsLaunch3 registers per thread at launch.
-            cudaFuncAttributes fa;
-            if (cudaFuncGetAttributes(&fa, prefill_kernel<D>) != cudaSuccess) {
-                cudaGetLastError();
-                return ATTN_ERR_CUDA;
-            }
-            if (fa.numRegs != kRegsLaunch3) return ATTN_ERR_UNSUPPORTED;
-        }
-        attr_set = true;
-    }
-    const long long grid = (long long)p.nqt * a.b * a.hq;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    prefill_kernel<D><<<(unsigned)grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, p);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_OK;
-    }
+    else
+        return prefill1q_launch<D>(a, tq, tk, tv, p, stream);
 }
 
 }  // namespace
