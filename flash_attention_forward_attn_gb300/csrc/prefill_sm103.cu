@@ -52,16 +52,29 @@ constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold, log2 units
 // Registers after re-balancing: the TMA/MMA warpgroup gives up registers to the softmax
 // warpgroups.  128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch3 (the launch budget).
 constexpr int kRegsLaunch3 = 168;
-constexpr int kRegsLow = 64;
-constexpr int kRegsHigh = 216;
+constexpr int kRegsLow = 96;
+constexpr int kRegsHigh = 200;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * kRegsLaunch3, "register split");
 
 struct PrefillParams {
     void* o;
     float* lse;
     int hq, hkv, sq, skv, group, nqt, window, causal, o_f32;
-    float c;  // scale * log2(e)
+    int nbh;     // b * hq
+    int nunits;  // work units of the persistent kernel
+    float c;     // scale * log2(e)
 };
+
+// Persistent schedule.  Units are numbered heaviest first (for a causal mask the last
+// query tiles see the most keys), and CTA c of G takes units c, 2G-1-c, 2G+c, 4G-1-c, ...
+// (a zig-zag over the sorted list), so heavy and light units pair up on every CTA.
+__device__ __forceinline__ int zigzag_unit(int cta, int round, int grid) {
+    return (round & 1) ? round * grid + (grid - 1 - cta) : round * grid + cta;
+}
+
+// Shared-memory descriptors advance along a tile by adding the byte offset / 16 to the
+// address field in the low bits (tiles never straddle the 256 KB field range).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) { return d + (byte_off >> 4); }
 
 struct TileRange {
     int q0, rows, qpos_lo, qpos_hi, kt0, n;
@@ -229,20 +242,22 @@ __global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
         if (lane == 0 && n > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-            const uint32_t q_base = smem_u32(sm + C::kQOff);
+            const uint64_t qd = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
+            const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
+            const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
             bool ok = wait_or_abort(&q_full, 0, &abort_flag);
             tc_fence_after();
             auto issue_s = [&](int t) -> bool {
                 const int slot = t % NK;
                 if (!wait_or_abort(&k_full[slot], (t / NK) & 1, &abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(sm + C::kKOff + slot * C::kSlotBytes);
+                const uint64_t kd = desc_add(kd0, (uint32_t)(slot * C::kSlotBytes));
                 const uint32_t tm_s = tmem + C::kSCol + (t & 1) * BN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = sw128_desc(q_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sw128_desc(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-                    tc_mma_ss(tm_s, a, b, idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                    const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+                    tc_mma_ss(tm_s, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[t & 1]);
                 tc_commit(&k_empty[slot]);  // K(t) consumed once this product is done
@@ -256,13 +271,11 @@ __global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
                 const int slot = j % NV;
                 if (!wait_or_abort(&v_full[slot], (j / NV) & 1, &abort_flag)) break;
                 tc_fence_after();
-                const uint32_t v_base = smem_u32(sm + C::kVOff + slot * C::kSlotBytes);
+                const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t b = sw128_desc(v_base + kk * (16 * 128), BN * 128, 1024);
-                    tc_mma_ts(tmem + C::kOCol, tmem + C::kSCol + s * BN + kk * 8, b, idesc_o,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    tc_mma_ts(tmem + C::kOCol, tmem + C::kSCol + s * BN + kk * 8,
+                              desc_add(vd, kk * 16 * 128), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(&o_done[s]);
                 tc_commit(&v_empty[slot]);  // V(j) consumed
                 if (j + 2 < n) ok = issue_s(j + 2);
@@ -433,19 +446,21 @@ attn_status prefill1q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
 
 // =========================================================================== two q-tiles
 // Shared-memory / TMEM plan of the two-q-tile kernel (head_dim 64 or 128, BN = 128):
-// Q_A, Q_B stay resident; K and V tiles stream through one ring of kSlots slots in the
-// order K(j), V(j), K(j+1), ...; S_A, S_B, O_A, O_B fill the 512 TMEM columns and P_X is
-// written back into the first BN/2 columns of S_X as packed bf16 pairs.
+// Q_A, Q_B stay resident; K and V tiles stream through their own rings (K two tiles
+// ahead), each fed by its own producer thread; S_A, S_B, O_A, O_B fill the 512 TMEM
+// columns and P_X is written back into the first BN/2 columns of S_X as packed bf16 pairs.
 template <int D>
 struct Cfg2Q {
     static constexpr int BN = 128;
     static constexpr int kQBytes = D * kBM * 2;
     static constexpr int kSlotBytes = D * BN * 2;
-    static constexpr int kSlots = (D == 128) ? 5 : 8;
+    static constexpr int kKSlots = (D == 128) ? 3 : 5;  // K runs two tiles ahead
+    static constexpr int kVSlots = (D == 128) ? 2 : 3;
     static constexpr int kQAOff = 0;
     static constexpr int kQBOff = kQBytes;
-    static constexpr int kRingOff = 2 * kQBytes;
-    static constexpr int kSmem = kRingOff + kSlots * kSlotBytes;
+    static constexpr int kKOff = 2 * kQBytes;
+    static constexpr int kVOff = kKOff + kKSlots * kSlotBytes;
+    static constexpr int kSmem = kVOff + kVSlots * kSlotBytes;
     static constexpr int kDynBytes = kSmem + 1024;
     static constexpr int kTmemCols = 512;
     static constexpr int kThreads = 384;
@@ -453,59 +468,81 @@ struct Cfg2Q {
     static_assert(kDynBytes + 512 <= 232448, "shared memory budget");
 };
 
-// One CTA = query rows [256 p, 256 p + 256) of one head, as tiles A (first 128 rows) and B.
-// Warps 0-3: TMA producer (warp 0), MMA issuer (warp 1), TMEM owner (warp 2).
-// Warps 4-7: softmax of tile A; warps 8-11: softmax of tile B (thread = row = TMEM lane).
+// Persistent: each CTA loops over work units; a unit = query rows [256 p, 256 p + 256) of
+// one head, as tiles A (first 128 rows) and B.  TMEM and the barriers are set up once.
+// Warp 0: K producer; warp 2 (also the TMEM owner): V producer -- each streams every
+// unit's tiles through its ring; warp 3: Q producer (loads the next unit's Q_A, Q_B once
+// the current unit's last S product is done); warp 1: MMA issuer; warps 4-7 / 8-11:
+// softmax of tile A / B (thread = row = TMEM lane), which also run the unit's epilogue.
 // Per KV tile j the MMA issuer runs  O_A += P_A(j-1) V(j-1),  S_A = Q_A K(j)^T,
 // O_B += P_B(j-1) V(j-1),  S_B = Q_B K(j)^T, so while one softmax warpgroup works on its
 // scores the tensor pipe holds the other tile's two products.  P_X(j-1) lives in S_X's
 // TMEM columns; the product that reads it is issued before the one that overwrites S_X,
-// and the two run in issue order on the tensor pipe.
+// and the two run in issue order on the tensor pipe.  The first PV of a unit into O_X
+// waits until the previous unit's epilogue has read O_X out of TMEM.  The issuing thread
+// is nearly synchronous with the tensor pipe (its queue is short), so its per-product work
+// is kept to a constant descriptor add.
 template <int D>
 __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     using C = Cfg2Q<D>;
     constexpr int BN = C::BN;
-    constexpr int NS = C::kSlots;
+    constexpr int NK = C::kKSlots;
+    constexpr int NV = C::kVSlots;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full, ring_full[NS], ring_empty[NS];
-    __shared__ uint64_t s_full[2], p_full[2], o_done[2], mma_drain;
+    __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
+    __shared__ uint64_t s_full[2], p_full[2], o_done[2], o_free[2], mma_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int npairs = (p.nqt + 1) / 2;
-    const int nbh = gridDim.x / npairs;
-    const int pair = npairs - 1 - (int)(blockIdx.x / nbh);  // heaviest causal pairs first
-    const int bh = (int)(blockIdx.x % nbh);
-    const int bidx = bh / p.hq, h = bh % p.hq;
-    const int kvz = bidx * p.hkv + h / p.group;
-    TileRange tx[2];
-    tx[0] = tile_range<BN>(p, 2 * pair);
-    tx[1] = tile_range<BN>(p, 2 * pair + 1);  // rows <= 0 (past sq) gives n = 0
-    // union of the two KV ranges
-    int u0 = INT_MAX, u1 = INT_MIN;
-    for (int x = 0; x < 2; ++x)
-        if (tx[x].n > 0) {
-            u0 = min(u0, tx[x].kt0);
-            u1 = max(u1, tx[x].kt0 + tx[x].n);
-        }
-    const int nu = (u1 > u0) ? u1 - u0 : 0;
-    const bool has_b = tx[1].rows > 0;
+    const int G = gridDim.x, cta = blockIdx.x;
+
+    struct Unit {
+        int bh, kvz, u0, u1;
+        bool has_b;
+        TileRange t[2];
+    };
+    auto unit_at = [&](int w) -> Unit {
+        Unit u;
+        const int pair = npairs - 1 - w / p.nbh;
+        u.bh = w % p.nbh;
+        const int bidx = u.bh / p.hq, h = u.bh % p.hq;
+        u.kvz = bidx * p.hkv + h / p.group;
+        u.t[0] = tile_range<BN>(p, 2 * pair);
+        u.t[1] = tile_range<BN>(p, 2 * pair + 1);  // rows <= 0 (past sq) gives n = 0
+        u.has_b = u.t[1].rows > 0;
+        u.u0 = INT_MAX;
+        u.u1 = INT_MIN;
+        for (int x = 0; x < 2; ++x)
+            if (u.t[x].n > 0) {
+                u.u0 = min(u.u0, u.t[x].kt0);
+                u.u1 = max(u.u1, u.t[x].kt0 + u.t[x].n);
+            }
+        if (u.u1 <= u.u0) u.u0 = u.u1 = 0;
+        return u;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&q_full, 1);
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&ring_full[i], 1);
-            mbar_init(&ring_empty[i], 1);
+        mbar_init(&q_empty, 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
             mbar_init(&o_done[i], 1);
+            mbar_init(&o_free[i], 128);
         }
         mbar_init(&mma_drain, 1);
         abort_flag = 0;
@@ -519,232 +556,297 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    const uint32_t col_s[2] = {0u, (uint32_t)BN};
-    const uint32_t col_o[2] = {(uint32_t)(2 * BN), (uint32_t)(2 * BN + D)};
 
     if (warp < 4) {
         regs_dec<kRegsLow>();
-        if (warp == 0 && lane == 0 && nu > 0) {
-            // -------------------------------------------------------- TMA producer
+        if (warp == 3 && lane == 0) {
+            // -------------------------------------------------------- Q producer
             tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(&q_full, (has_b ? 2 : 1) * C::kQBytes);
-            for (int x = 0; x < (has_b ? 2 : 1); ++x)
+            int rq = 0;  // Q loads issued
+            for (int r = 0;; ++r) {
+                const int w = zigzag_unit(cta, r, G);
+                if (w >= p.nunits) break;
+                const Unit u = unit_at(w);
+                if (r > 0 && !wait_or_abort(&q_empty, (r - 1) & 1, &abort_flag)) break;
+                ++rq;
+                mbar_arrive_expect_tx(&q_full, (u.has_b ? 2 : 1) * C::kQBytes);
+                for (int x = 0; x < (u.has_b ? 2 : 1); ++x)
 #pragma unroll
-                for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(sm + (x ? C::kQBOff : C::kQAOff) + dc * (kBM * 128), &tm_q, dc * 64,
-                                tx[x].q0, bh, &q_full);
-            int issued = 0;
-            for (int L = 0; L < 2 * nu; ++L) {
-                const int slot = L % NS;
-                if (L >= NS && !wait_or_abort(&ring_empty[slot], ((L / NS) - 1) & 1, &abort_flag)) break;
-                const int k0 = (u0 + (L >> 1)) * BN;
-                mbar_arrive_expect_tx(&ring_full[slot], C::kSlotBytes);
-                const CUtensorMap* tm = (L & 1) ? &tm_v : &tm_k;
+                    for (int dc = 0; dc < D / 64; ++dc)
+                        tma_load_3d(sm + (x ? C::kQBOff : C::kQAOff) + dc * (kBM * 128), &tm_q,
+                                    dc * 64, u.t[x].q0, u.bh, &q_full);
+            }
+            if (abort_flag && rq > 0) wait_bounded(&q_full, (rq - 1) & 1);  // the last Q copy lands
+        } else if ((warp == 0 || warp == 2) && lane == 0) {
+            // -------------------------------------------------------- K / V producers
+            const bool is_k = warp == 0;
+            const int ns = is_k ? NK : NV;
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
+            tma_prefetch_desc(tm);
+            int L = 0;  // tiles issued so far into this ring
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int w = zigzag_unit(cta, r, G);
+                if (w >= p.nunits) break;
+                const Unit u = unit_at(w);
+                for (int j = u.u0; j < u.u1; ++j, ++L) {
+                    const int slot = L % ns;
+                    if (L >= ns && !wait_or_abort(&empty[slot], ((L / ns) - 1) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[slot], C::kSlotBytes);
 #pragma unroll
-                for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(sm + C::kRingOff + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64,
-                                k0, kvz, &ring_full[slot]);
-                issued = L + 1;
+                    for (int dc = 0; dc < D / 64; ++dc)
+                        tma_load_3d(ring + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64, j * BN,
+                                    u.kvz, &full[slot]);
+                }
             }
             if (abort_flag) {  // let copies in flight land before the CTA exits
-                wait_bounded(&q_full, 0);
-                for (int L = max(0, issued - NS); L < issued; ++L)
-                    wait_bounded(&ring_full[L % NS], (L / NS) & 1);
+                for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
             }
-        } else if (warp == 1 && lane == 0 && nu > 0) {
+        } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-            bool ok = wait_or_abort(&q_full, 0, &abort_flag);
-            tc_fence_after();
-            int cnt[2] = {0, 0};  // tiles of A / B whose S has been issued
-            for (int j = u0; ok && j <= u1; ++j) {
-                const int jj = j - u0;
-                const bool have_k = j < u1;
-                if (have_k) {
-                    const int L = 2 * jj;
-                    ok = wait_or_abort(&ring_full[L % NS], (L / NS) & 1, &abort_flag);
-                    if (!ok) break;
-                }
-                const bool have_v = j > u0;
-                if (have_v) {
-                    const int L = 2 * (jj - 1) + 1;
-                    ok = wait_or_abort(&ring_full[L % NS], (L / NS) & 1, &abort_flag);
-                    if (!ok) break;
-                }
+            const uint64_t qd[2] = {sw128_desc(smem_u32(sm + C::kQAOff), 16, 1024),
+                                    sw128_desc(smem_u32(sm + C::kQBOff), 16, 1024)};
+            const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
+            const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
+            const uint32_t col_s[2] = {0u, (uint32_t)BN};
+            const uint32_t col_o[2] = {(uint32_t)(2 * BN), (uint32_t)(2 * BN + D)};
+            int Lbase = 0;        // ring index (K and V alike) of the unit's first tile
+            int cnt[2] = {0, 0};  // S products issued so far per tile (phase of s/p_full)
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int w = zigzag_unit(cta, r, G);
+                if (w >= p.nunits) break;
+                const Unit u = unit_at(w);
+                if (!wait_or_abort(&q_full, r & 1, &abort_flag)) break;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(sm + C::kRingOff + ((2 * jj) % NS) * C::kSlotBytes);
-                const uint32_t v_base = smem_u32(sm + C::kRingOff + ((2 * jj - 1 + NS) % NS) * C::kSlotBytes);
+                bool freed[2] = {r == 0, r == 0};  // previous unit's O_X read out?
+                const int cbase[2] = {cnt[0], cnt[1]};
+                const int nu = u.u1 - u.u0;
+                if (nu == 0) tc_commit(&q_empty);
+                for (int j = u.u0; ok && j <= u.u1 && nu > 0; ++j) {
+                    const int jj = j - u.u0;
+                    const int Lk = Lbase + jj, Lv = Lk - 1;  // K(j), V(j-1)
+                    bool in_k[2], in_v[2];
 #pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const TileRange& t = tx[x];
-                    // O_X += P_X(j-1) V(j-1)
-                    if (have_v && j - 1 >= t.kt0 && j - 1 < t.kt0 + t.n) {
-                        const int i = (j - 1) - t.kt0;  // this tile's index within X's range
-                        if (!wait_or_abort(&p_full[x], i & 1, &abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            const uint64_t b = sw128_desc(v_base + kk * (16 * 128), BN * 128, 1024);
-                            tc_mma_ts(tmem + col_o[x], tmem + col_s[x] + kk * 8, b, idesc_o,
-                                      (i > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        if (i == t.n - 1) tc_commit(&o_done[x]);  // the last product into O_X
+                    for (int x = 0; x < 2; ++x) {
+                        in_k[x] = j < u.u1 && j >= u.t[x].kt0 && j < u.t[x].kt0 + u.t[x].n;
+                        in_v[x] = j > u.u0 && j - 1 >= u.t[x].kt0 && j - 1 < u.t[x].kt0 + u.t[x].n;
                     }
-                    // S_X = Q_X K(j)^T
-                    if (have_k && j >= t.kt0 && j < t.kt0 + t.n) {
-                        const uint32_t q_base = smem_u32(sm + (x ? C::kQBOff : C::kQAOff));
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t a = sw128_desc(q_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-                            const uint64_t b = sw128_desc(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-                            tc_mma_ss(tmem + col_s[x], a, b, idesc_s, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(&s_full[x]);
-                        ++cnt[x];
+                    const bool have_k = j < u.u1, have_v = j > u.u0;
+                    if (have_k && !wait_or_abort(&k_full[Lk % NK], (Lk / NK) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    if (have_v && !wait_or_abort(&v_full[Lv % NV], (Lv / NV) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t kd = desc_add(kd0, (uint32_t)((Lk % NK) * C::kSlotBytes));
+                    const uint64_t vd = desc_add(vd0, (uint32_t)(((Lv + NV) % NV) * C::kSlotBytes));
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (in_v[x]) {
+                            // O_X += P_X(j-1) V(j-1)
+                            const int i = (j - 1) - u.t[x].kt0;
+                            if (!freed[x]) {
+                                if (!wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                freed[x] = true;
+                            }
+                            if (!wait_or_abort(&p_full[x], (cbase[x] + i) & 1, &abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+#pragma unroll
+                            for (int kk = 0; kk < BN / 16; ++kk)
+                                tc_mma_ts(tmem + col_o[x], tmem + col_s[x] + kk * 8,
+                                          desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                            if (i == u.t[x].n - 1) tc_commit(&o_done[x]);  // the unit's last into O_X
+                        }
+                        // V(j-1) is free once the last product reading it is done
+                        if (have_v && (x == 1 || !in_v[1])) {
+                            if (x == 1 ? in_v[1] : true) tc_commit(&v_empty[(Lv + NV) % NV]);
+                        }
+                        if (in_k[x]) {
+                            // S_X = Q_X K(j)^T
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                                const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+                                tc_mma_ss(tmem + col_s[x], desc_add(qd[x], off_a), desc_add(kd, off_b),
+                                          idesc_s, kk > 0 ? 1u : 0u);
+                            }
+                            tc_commit(&s_full[x]);
+                            ++cnt[x];
+                        }
+                    }
+                    if (!ok) break;
+                    if (have_k) tc_commit(&k_empty[Lk % NK]);  // K(j) consumed
+                    if (j == u.u1 - 1) tc_commit(&q_empty);   // every S of this unit issued
                 }
-                if (!ok) break;
-                if (have_k) tc_commit(&ring_empty[(2 * jj) % NS]);           // K(j) consumed
-                if (have_v) tc_commit(&ring_empty[(2 * jj - 1 + NS) % NS]);  // V(j-1) consumed
+                // a tile with no product this unit still consumes the epilogue's o_free phase
+                for (int x = 0; ok && x < 2; ++x)
+                    if (!freed[x] && !wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag)) ok = false;
+                Lbase += nu;
             }
             tc_commit(&mma_drain);
             wait_bounded(&mma_drain, 0);
         }
     } else {
-        // ------------------------------------------------------------ softmax
+        // ------------------------------------------------------------ softmax + epilogue
         regs_inc<kRegsHigh>();
         const int x = (warp >> 2) - 1;  // 0: tile A, 1: tile B
-        const TileRange t = x ? tx[1] : tx[0];
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tm_s = tmem + lane_off + (x ? col_s[1] : col_s[0]);
-        const uint32_t tm_o = tmem + lane_off + (x ? col_o[1] : col_o[0]);
-        const int q_row = t.q0 + row;
-        const int qpos = t.qpos_lo + row;
-        const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
-        const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+        const uint32_t tm_s = tmem + lane_off + (x ? (uint32_t)BN : 0u);
+        const uint32_t tm_o = tmem + lane_off + (uint32_t)(2 * BN) + (x ? (uint32_t)D : 0u);
+        uint64_t* sfull = x ? &s_full[1] : &s_full[0];
+        uint64_t* pfull = x ? &p_full[1] : &p_full[0];
+        uint64_t* odone = x ? &o_done[1] : &o_done[0];
+        uint64_t* ofree = x ? &o_free[1] : &o_free[0];
         const float c = p.c;
         const bool c_pos = c > 0.f;
         const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
-        float m_used = -INFINITY, l_sum = 0.f;
+        int cnt = 0;   // S tiles consumed so far (phase of s_full)
+        int ocnt = 0;  // units with at least one product into O_X (phase of o_done)
         bool ok = true;
-        for (int i = 0; i < t.n; ++i) {
-            if (!wait_or_abort(x ? &s_full[1] : &s_full[0], i & 1, &abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float v[BN];
-            {
-                uint32_t r[BN];
-                tmem_ld128(tm_s, r);
-#pragma unroll
-                for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(r[e]);
-            }
-            const int k0 = (t.kt0 + i) * BN;
-            const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
-                              (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
-            if (edge) {
-#pragma unroll
-                for (int e = 0; e < BN; ++e) {
-                    const int key = k0 + e;
-                    if (key < key_lo || key > key_hi) v[e] = -INFINITY;
+        for (int r = 0;; ++r) {
+            const int w = zigzag_unit(cta, r, G);
+            if (w >= p.nunits) break;
+            const Unit u = unit_at(w);
+            const TileRange t = x ? u.t[1] : u.t[0];
+            const int q_row = t.q0 + row;
+            const int qpos = t.qpos_lo + row;
+            const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
+            const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+            float m_used = -INFINITY, l_sum = 0.f;
+            for (int i = 0; ok && i < t.n; ++i, ++cnt) {
+                if (!wait_or_abort(sfull, cnt & 1, &abort_flag)) {
+                    ok = false;
+                    break;
                 }
-            }
-            if (!c_pos) {
+                tc_fence_after();
+                float v[BN];
+                {
+                    uint32_t rr[BN];
+                    tmem_ld128(tm_s, rr);
 #pragma unroll
-                for (int e = 0; e < BN; ++e) v[e] *= c;
-            }
-            float mx[8];
+                    for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(rr[e]);
+                }
+                const int k0 = (t.kt0 + i) * BN;
+                const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
+                                  (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
+                if (edge) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+                    for (int e = 0; e < BN; ++e) {
+                        const int key = k0 + e;
+                        if (key < key_lo || key > key_hi) v[e] = -INFINITY;
+                    }
+                }
+                if (!c_pos) {
 #pragma unroll
-            for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
-            float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            if (c_pos) tmax *= c;  // -inf stays -inf
-            const float m_new = fmaxf(m_used, tmax);
-            const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
-            if (m_used == -INFINITY) m_used = m_new;  // nothing accumulated yet for this row
-            if (__any_sync(0xffffffffu, need)) {
-                // O_X = previous PVs: all finished, since S_X(i) was issued after them
-                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                    for (int e = 0; e < BN; ++e) v[e] *= c;
+                }
+                float mx[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
+                float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                if (c_pos) tmax *= c;  // -inf stays -inf
+                const float m_new = fmaxf(m_used, tmax);
+                const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
+                if (m_used == -INFINITY) m_used = m_new;  // nothing accumulated yet for this row
+                if (__any_sync(0xffffffffu, need)) {
+                    // O_X = this unit's previous PVs: all finished, since S_X(i) was issued after
+                    const float alpha = need ? ex2(m_used - m_new) : 1.0f;
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tm_o + c0, r);
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t rr[32];
+                        tmem_ld32(tm_o + c0, rr);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st32(tm_o + c0, r);
+                        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                        tmem_st32(tm_o + c0, rr);
+                    }
+                    if (need) {
+                        l_sum *= alpha;
+                        m_used = m_new;
+                    }
                 }
-                if (need) {
-                    l_sum *= alpha;
-                    m_used = m_new;
+                const float m_e = (m_used == -INFINITY) ? 0.f : m_used;
+                uint32_t pk[BN / 2];
+                float ls[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+#pragma unroll
+                for (int e = 0; e < BN / 2; ++e) {
+                    const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
+                    const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
+                    ls[(2 * e) & 7] += p0;
+                    ls[(2 * e + 1) & 7] += p1;
+                    pk[e] = pack_bf16(p0, p1);
                 }
+                l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                tmem_st64(tm_s, pk);  // P_X over the first BN/2 columns of S_X
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(pfull);
             }
-            const float m_e = (m_used == -INFINITY) ? 0.f : m_used;
-            uint32_t pk[BN / 2];
-            float ls[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-#pragma unroll
-            for (int e = 0; e < BN / 2; ++e) {
-                const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
-                const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
-                ls[(2 * e) & 7] += p0;
-                ls[(2 * e + 1) & 7] += p1;
-                pk[e] = pack_bf16(p0, p1);
-            }
-            l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-            tmem_st64(tm_s, pk);  // P_X over the first BN/2 columns of S_X
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(x ? &p_full[1] : &p_full[0]);
-        }
-        // ------------------------------------------------------------ epilogue
-        bool have_o = false;
-        if (ok && t.n > 0) {
-            have_o = wait_or_abort(x ? &o_done[1] : &o_done[0], 0, &abort_flag);
-            tc_fence_after();
-        }
-        const bool row_valid = t.rows > 0 && row < t.rows;
-        const bool live = have_o && l_sum > 0.f;
-        const float inv = live ? 1.0f / l_sum : 0.f;
-        const size_t orow = (size_t)bh * p.sq + q_row;
-        if (row_valid && p.lse != nullptr)
-            p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
+            // ------------------------------------------------------------ epilogue
+            bool have_o = false;
             if (t.n > 0) {
-                tmem_ld32(tm_o + c0, r);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = 0u;
+                have_o = ok && wait_or_abort(odone, ocnt & 1, &abort_flag);
+                ++ocnt;
+                tc_fence_after();
             }
-            if (!row_valid) continue;
-            if (p.o_f32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
+            const bool row_valid = t.rows > 0 && row < t.rows;
+            const bool live = have_o && l_sum > 0.f;
+            const float inv = live ? 1.0f / l_sum : 0.f;
+            const size_t orow = (size_t)u.bh * p.sq + q_row;
+            if (row_valid && p.lse != nullptr)
+                p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t rr[32];
+                if (t.n > 0) {
+                    tmem_ld32(tm_o + c0, rr);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                         __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
-            } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
+                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                }
+                if (!row_valid) continue;
+                if (p.o_f32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_uint4(
-                        pack_bf16(__uint_as_float(r[8 * e]) * inv, __uint_as_float(r[8 * e + 1]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv));
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(rr[4 * e]) * inv, __uint_as_float(rr[4 * e + 1]) * inv,
+                                             __uint_as_float(rr[4 * e + 2]) * inv, __uint_as_float(rr[4 * e + 3]) * inv);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(
+                            pack_bf16(__uint_as_float(rr[8 * e]) * inv, __uint_as_float(rr[8 * e + 1]) * inv),
+                            pack_bf16(__uint_as_float(rr[8 * e + 2]) * inv, __uint_as_float(rr[8 * e + 3]) * inv),
+                            pack_bf16(__uint_as_float(rr[8 * e + 4]) * inv, __uint_as_float(rr[8 * e + 5]) * inv),
+                            pack_bf16(__uint_as_float(rr[8 * e + 6]) * inv, __uint_as_float(rr[8 * e + 7]) * inv));
+                }
             }
+            tc_fence_before();
+            mbar_arrive(ofree);  // O_X has been read: the next unit may overwrite it
         }
     }
     tc_fence_before();
@@ -752,6 +854,25 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     tc_fence_after();
     if (threadIdx.x == 0 && abort_flag) atomicOr(&g_prefill_error, kDevErrTimeout);
     if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 148;
+    }
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 148;
+        }
+        cached[dev] = n;
+    }
+    return cached[dev];
 }
 
 template <int D>
@@ -775,9 +896,12 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
         if (fa.numRegs != kRegsLaunch3) return ATTN_ERR_UNSUPPORTED;
         attr_set = true;
     }
-    const long long grid = (long long)((p.nqt + 1) / 2) * a.b * a.hq;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    prefill2q_kernel<D><<<(unsigned)grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, p);
+    const long long units = (long long)((p.nqt + 1) / 2) * a.b * a.hq;
+    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    PrefillParams pp = p;
+    pp.nunits = (int)units;
+    const int grid = (int)(units < num_sms() ? units : num_sms());
+    prefill2q_kernel<D><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, pp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
@@ -811,6 +935,8 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     p.causal = a.causal;
     p.o_f32 = a.o_dtype == ATTN_F32 ? 1 : 0;
     p.c = a.scale * kLog2e;
+    p.nbh = a.b * a.hq;
+    p.nunits = 0;
     if constexpr (D <= 128)
         return prefill2q_launch<D>(a, tq, tk, tv, p, stream);
     else
