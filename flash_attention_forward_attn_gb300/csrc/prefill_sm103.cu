@@ -446,21 +446,24 @@ attn_status prefill1q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
 
 // =========================================================================== two q-tiles
 // Shared-memory / TMEM plan of the two-q-tile kernel (head_dim 64 or 128, BN = 128):
-// Q_A, Q_B stay resident; K and V tiles stream through their own rings (K two tiles
-// ahead), each fed by its own producer thread; S_A, S_B, O_A, O_B fill the 512 TMEM
-// columns and P_X is written back into the first BN/2 columns of S_X as packed bf16 pairs.
+// Q_A, Q_B stay resident; K and V tiles stream through their own rings, each fed by its
+// own producer thread; S_A, S_B, O_A, O_B fill the 512 TMEM columns and P_X is written
+// back into the first BN/2 columns of S_X as packed bf16 pairs.  A bf16 output tile is
+// staged in shared memory and written back with one TMA store per 64 columns.
 template <int D>
 struct Cfg2Q {
     static constexpr int BN = 128;
     static constexpr int kQBytes = D * kBM * 2;
     static constexpr int kSlotBytes = D * BN * 2;
-    static constexpr int kKSlots = (D == 128) ? 3 : 5;  // K runs two tiles ahead
+    static constexpr int kKSlots = (D == 128) ? 2 : 5;
     static constexpr int kVSlots = (D == 128) ? 2 : 3;
     static constexpr int kQAOff = 0;
     static constexpr int kQBOff = kQBytes;
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kKSlots * kSlotBytes;
-    static constexpr int kSmem = kVOff + kVSlots * kSlotBytes;
+    static constexpr int kOStOff = kVOff + kVSlots * kSlotBytes;  // bf16 O staging tile
+    static constexpr int kOStBytes = kBM * D * 2;
+    static constexpr int kSmem = kOStOff + kOStBytes;
     static constexpr int kDynBytes = kSmem + 1024;
     static constexpr int kTmemCols = 512;
     static constexpr int kThreads = 384;
@@ -485,7 +488,8 @@ struct Cfg2Q {
 template <int D>
 __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+    const PrefillParams p) {
     using C = Cfg2Q<D>;
     constexpr int BN = C::BN;
     constexpr int NK = C::kKSlots;
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
-    __shared__ uint64_t s_full[2], p_full[2], o_done[2], o_free[2], mma_drain;
+    __shared__ uint64_t s_full[2], p_full[2], o_done[2], o_free[2], mma_drain, stage_free;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -545,6 +549,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             mbar_init(&o_free[i], 128);
         }
         mbar_init(&mma_drain, 1);
+        mbar_init(&stage_free, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -721,12 +726,17 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
         const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
         int cnt = 0;   // S tiles consumed so far (phase of s_full)
         int ocnt = 0;  // units with at least one product into O_X (phase of o_done)
+        int ebase = 0; // staged output tiles of earlier units (order: A then B per unit)
+        const bool store_thread = (warp & 3) == 0 && lane == 0;
         bool ok = true;
         for (int r = 0;; ++r) {
             const int w = zigzag_unit(cta, r, G);
             if (w >= p.nunits) break;
             const Unit u = unit_at(w);
             const TileRange t = x ? u.t[1] : u.t[0];
+            // this tile's position in the CTA's sequence of staged output tiles
+            const int eidx = ebase + ((x == 1 && u.t[0].rows > 0) ? 1 : 0);
+            ebase += (u.t[0].rows > 0 ? 1 : 0) + (u.t[1].rows > 0 ? 1 : 0);
             const int q_row = t.q0 + row;
             const int qpos = t.qpos_lo + row;
             const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
@@ -818,36 +828,72 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             const size_t orow = (size_t)u.bh * p.sq + q_row;
             if (row_valid && p.lse != nullptr)
                 p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t rr[32];
-                if (t.n > 0) {
-                    tmem_ld32(tm_o + c0, rr);
-                } else {
+            if (!p.o_f32) {
+                // bf16: O_X -> registers (then O_X is free), scale, stage in shared memory in
+                // the 128-byte-swizzled box layout, and one thread stores the boxes with TMA
+                // (rows past sq are clipped by the store).
+                uint32_t ob[D / 2];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t rr[32];
+                    if (t.n > 0) {
+                        tmem_ld32(tm_o + c0, rr);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        ob[c0 / 2 + e] = pack_bf16(__uint_as_float(rr[2 * e]) * inv,
+                                                   __uint_as_float(rr[2 * e + 1]) * inv);
                 }
-                if (!row_valid) continue;
-                if (p.o_f32) {
+                tc_fence_before();
+                mbar_arrive(ofree);  // O_X has been read: the next unit may overwrite it
+                if (t.rows > 0) {
+                    if (eidx > 0) ok = wait_or_abort(&stage_free, (eidx - 1) & 1, &abort_flag) && ok;
+                    uint8_t* st = sm + C::kOStOff;
+#pragma unroll
+                    for (int ch = 0; ch < D / 8; ++ch) {
+                        const uint32_t off = (ch >> 3) * (kBM * 128) + sw128_off(row, ch & 7);
+                        *reinterpret_cast<uint4*>(st + off) =
+                            make_uint4(ob[4 * ch], ob[4 * ch + 1], ob[4 * ch + 2], ob[4 * ch + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    if (x == 0)
+                        asm volatile("bar.sync 1, 128;" ::: "memory");
+                    else
+                        asm volatile("bar.sync 2, 128;" ::: "memory");
+                    if (store_thread) {
+#pragma unroll
+                        for (int dc = 0; dc < D / 64; ++dc)
+                            tma_store_3d(&tm_out, st + dc * (kBM * 128), dc * 64, t.q0, u.bh);
+                        bulk_commit();
+                        bulk_wait_read0();  // the staging tile may be reused once read
+                        mbar_arrive(&stage_free);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t rr[32];
+                    if (t.n > 0) {
+                        tmem_ld32(tm_o + c0, rr);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                    }
+                    if (!row_valid) continue;
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         dst[e] = make_float4(__uint_as_float(rr[4 * e]) * inv, __uint_as_float(rr[4 * e + 1]) * inv,
                                              __uint_as_float(rr[4 * e + 2]) * inv, __uint_as_float(rr[4 * e + 3]) * inv);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(
-                            pack_bf16(__uint_as_float(rr[8 * e]) * inv, __uint_as_float(rr[8 * e + 1]) * inv),
-                            pack_bf16(__uint_as_float(rr[8 * e + 2]) * inv, __uint_as_float(rr[8 * e + 3]) * inv),
-                            pack_bf16(__uint_as_float(rr[8 * e + 4]) * inv, __uint_as_float(rr[8 * e + 5]) * inv),
-                            pack_bf16(__uint_as_float(rr[8 * e + 6]) * inv, __uint_as_float(rr[8 * e + 7]) * inv));
                 }
+                tc_fence_before();
+                mbar_arrive(ofree);  // O_X has been read: the next unit may overwrite it
             }
-            tc_fence_before();
-            mbar_arrive(ofree);  // O_X has been read: the next unit may overwrite it
         }
+        if (store_thread) bulk_wait0();  // every staged tile has reached global memory
     }
     tc_fence_before();
     __syncthreads();
@@ -901,7 +947,16 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
     PrefillParams pp = p;
     pp.nunits = (int)units;
     const int grid = (int)(units < num_sms() ? units : num_sms());
-    prefill2q_kernel<D><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, pp);
+    CUtensorMap to;  // bf16 O for the TMA stores (unused, never dereferenced, for fp32 O)
+    if (a.o_dtype == ATTN_BF16) {
+        uint64_t od[3] = {(uint64_t)D, (uint64_t)a.sq, (uint64_t)a.b * a.hq};
+        uint64_t os[2] = {(uint64_t)D * 2, (uint64_t)a.sq * D * 2};
+        uint32_t ob[3] = {64u, (uint32_t)kBM, 1u};
+        if (!make_bf16_map(&to, a.o, 3, od, os, ob)) return ATTN_ERR_CUDA;
+    } else {
+        to = tq;
+    }
+    prefill2q_kernel<D><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, to, pp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
