@@ -748,41 +748,49 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     break;
                 }
                 tc_fence_after();
-                float v[BN];
-                {
+                const int k0 = (t.kt0 + i) * BN;
+                const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
+                                  (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
+                // S row of this tile from TMEM, masked (edge tiles) and, for scale <= 0, scaled
+                auto load_s = [&](float* v) {
                     uint32_t rr[BN];
                     tmem_ld128(tm_s, rr);
 #pragma unroll
                     for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(rr[e]);
-                }
-                const int k0 = (t.kt0 + i) * BN;
-                const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
-                                  (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
-                if (edge) {
+                    if (edge) {
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) {
-                        const int key = k0 + e;
-                        if (key < key_lo || key > key_hi) v[e] = -INFINITY;
+                        for (int e = 0; e < BN; ++e) {
+                            const int key = k0 + e;
+                            if (key < key_lo || key > key_hi) v[e] = -INFINITY;
+                        }
                     }
-                }
-                if (!c_pos) {
+                    if (!c_pos) {
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) v[e] *= c;
-                }
-                float mx[8];
+                        for (int e = 0; e < BN; ++e) v[e] *= c;
+                    }
+                };
+                // P = 2^(v * cm - m_e) packed to bf16 pairs; returns its row sum
+                auto exps = [&](const float* v, float m_e, uint32_t* pk) -> float {
+                    float ls[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+                    for (int e = 0; e < 8; ++e) ls[e] = 0.f;
 #pragma unroll
-                for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
-                float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                if (c_pos) tmax *= c;  // -inf stays -inf
-                const float m_new = fmaxf(m_used, tmax);
-                const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
-                if (m_used == -INFINITY) m_used = m_new;  // nothing accumulated yet for this row
-                if (__any_sync(0xffffffffu, need)) {
-                    // O_X = this unit's previous PVs: all finished, since S_X(i) was issued after
-                    const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                    for (int e = 0; e < BN / 2; ++e) {
+                        const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
+                        const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
+                        ls[(2 * e) & 7] += p0;
+                        ls[(2 * e + 1) & 7] += p1;
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                };
+                auto reduce8 = [](const float* mx) {
+                    return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                };
+                // O_X *= alpha in TMEM (the unit's previous PVs have finished: S_X(i) was
+                // issued after them)
+                auto rescale_o = [&](float alpha) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t rr[32];
@@ -791,25 +799,59 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                         for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
                         tmem_st32(tm_o + c0, rr);
                     }
-                    if (need) {
-                        l_sum *= alpha;
-                        m_used = m_new;
-                    }
-                }
-                const float m_e = (m_used == -INFINITY) ? 0.f : m_used;
+                };
                 uint32_t pk[BN / 2];
-                float ls[8];
+                float l_tile = 0.f;
+                bool redo = __any_sync(0xffffffffu, m_used == -INFINITY);
+                if (!redo) {
+                    // Common case: one pass of exponents against the running max m_used.  The
+                    // row's max grew by more than 2^kRescaleLog2 exactly when some exponent
+                    // exceeds 2^kRescaleLog2, which is read off the packed bf16 values (an
+                    // unsigned 16-bit max orders non-negative bf16 values by size).
+                    float v[BN];
+                    load_s(v);
+                    float ls[8];
+                    uint32_t pmax = 0u;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+                    for (int e = 0; e < 8; ++e) ls[e] = 0.f;
 #pragma unroll
-                for (int e = 0; e < BN / 2; ++e) {
-                    const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
-                    const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
-                    ls[(2 * e) & 7] += p0;
-                    ls[(2 * e + 1) & 7] += p1;
-                    pk[e] = pack_bf16(p0, p1);
+                    for (int e = 0; e < BN / 2; ++e) {
+                        const float p0 = ex2(fmaf(v[2 * e], cm, -m_used));
+                        const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_used));
+                        ls[(2 * e) & 7] += p0;
+                        ls[(2 * e + 1) & 7] += p1;
+                        pk[e] = pack_bf16(p0, p1);
+                        pmax = __vmaxu2(pmax, pk[e]);
+                    }
+                    l_tile = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                    constexpr uint32_t kTwoPow8 = 0x4380u;  // bf16 bits of 2^kRescaleLog2 = 256
+                    const bool big = (pmax & 0xFFFFu) > kTwoPow8 || (pmax >> 16) > kTwoPow8;
+                    redo = __any_sync(0xffffffffu, big);
                 }
-                l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                if (redo) {
+                    // First tile of a row, or its max grew by more than 2^kRescaleLog2: take the
+                    // exact tile max from S (still in TMEM: P has not been written over it),
+                    // rescale O and l where the max moved, and recompute the exponents.
+                    float v[BN];
+                    load_s(v);
+                    float mx[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
+                    float tmax = reduce8(mx);
+                    if (c_pos) tmax *= c;  // -inf stays -inf
+                    const float m_new = fmaxf(m_used, tmax);
+                    const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                        rescale_o(alpha);
+                        if (need) l_sum *= alpha;
+                    }
+                    if (m_used == -INFINITY || need) m_used = m_new;  // nothing accumulated yet
+                    l_tile = exps(v, (m_used == -INFINITY) ? 0.f : m_used, pk);
+                }
+                l_sum += l_tile;
                 tmem_st64(tm_s, pk);  // P_X over the first BN/2 columns of S_X
                 tmem_wait_st();
                 tc_fence_before();
