@@ -473,18 +473,16 @@ struct Cfg2Q {
 
 // Persistent: each CTA loops over work units; a unit = query rows [256 p, 256 p + 256) of
 // one head, as tiles A (first 128 rows) and B.  TMEM and the barriers are set up once.
-// Warp 0: K producer; warp 2 (also the TMEM owner): V producer -- each streams every
-// unit's tiles through its ring; warp 3: Q producer (loads the next unit's Q_A, Q_B once
-// the current unit's last S product is done); warp 1: MMA issuer; warps 4-7 / 8-11:
-// softmax of tile A / B (thread = row = TMEM lane), which also run the unit's epilogue.
-// Per KV tile j the MMA issuer runs  O_A += P_A(j-1) V(j-1),  S_A = Q_A K(j)^T,
-// O_B += P_B(j-1) V(j-1),  S_B = Q_B K(j)^T, so while one softmax warpgroup works on its
-// scores the tensor pipe holds the other tile's two products.  P_X(j-1) lives in S_X's
-// TMEM columns; the product that reads it is issued before the one that overwrites S_X,
-// and the two run in issue order on the tensor pipe.  The first PV of a unit into O_X
-// waits until the previous unit's epilogue has read O_X out of TMEM.  The issuing thread
-// is nearly synchronous with the tensor pipe (its queue is short), so its per-product work
-// is kept to a constant descriptor add.
+// Warp 0: K producer; warp 2 (also the TMEM owner): Q and V producer (the next unit's
+// Q_A, Q_B once the current unit's last S products are done, and every unit's V tiles);
+// warps 1 / 3: MMA issuers of tile A / B; warps 4-7 / 8-11: softmax of tile A / B
+// (thread = row = TMEM lane), which also run the unit's epilogue.  Per KV tile j the
+// issuer of tile X runs  O_X += P_X(j-1) V(j-1)  then  S_X = Q_X K(j)^T, so while one
+// softmax warpgroup works on its scores the tensor pipe holds the other tile's products.
+// P_X(j-1) lives in S_X's TMEM columns; the product that reads it is issued before the one
+// that overwrites S_X by the same thread, and one thread's products run in issue order on
+// the tensor pipe.  The first PV of a unit into O_X waits until the previous unit's
+// epilogue has read O_X out of TMEM.
 template <int D>
 __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -499,6 +497,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[2], p_full[2], o_done[2], o_free[2], mma_drain, stage_free;
+    __shared__ uint64_t turn[2];  // MMA issue turns of tiles A and B
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -533,14 +532,14 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
 
     if (threadIdx.x == 0) {
         mbar_init(&q_full, 1);
-        mbar_init(&q_empty, 1);
+        mbar_init(&q_empty, 2);  // both MMA issuers
         for (int i = 0; i < NK; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
+            mbar_init(&k_empty[i], 2);
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], 2);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
@@ -548,8 +547,11 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             mbar_init(&o_done[i], 1);
             mbar_init(&o_free[i], 128);
         }
-        mbar_init(&mma_drain, 1);
+        mbar_init(&mma_drain, 2);
         mbar_init(&stage_free, 1);
+        mbar_init(&turn[0], 1);
+        mbar_init(&turn[1], 1);
+        mbar_arrive(&turn[0]);  // tile A takes the first turn
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -564,26 +566,11 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
 
     if (warp < 4) {
         regs_dec<kRegsLow>();
-        if (warp == 3 && lane == 0) {
-            // -------------------------------------------------------- Q producer
-            tma_prefetch_desc(&tm_q);
-            int rq = 0;  // Q loads issued
-            for (int r = 0;; ++r) {
-                const int w = zigzag_unit(cta, r, G);
-                if (w >= p.nunits) break;
-                const Unit u = unit_at(w);
-                if (r > 0 && !wait_or_abort(&q_empty, (r - 1) & 1, &abort_flag)) break;
-                ++rq;
-                mbar_arrive_expect_tx(&q_full, (u.has_b ? 2 : 1) * C::kQBytes);
-                for (int x = 0; x < (u.has_b ? 2 : 1); ++x)
-#pragma unroll
-                    for (int dc = 0; dc < D / 64; ++dc)
-                        tma_load_3d(sm + (x ? C::kQBOff : C::kQAOff) + dc * (kBM * 128), &tm_q,
-                                    dc * 64, u.t[x].q0, u.bh, &q_full);
-            }
-            if (abort_flag && rq > 0) wait_bounded(&q_full, (rq - 1) & 1);  // the last Q copy lands
-        } else if ((warp == 0 || warp == 2) && lane == 0) {
-            // -------------------------------------------------------- K / V producers
+        if ((warp == 0 || warp == 2) && lane == 0) {
+            // ---------------------------------------------- K producer / Q + V producer
+            // K(j) streams through its own ring so it never waits behind a V slot; the V
+            // producer also loads each unit's Q tiles once every S of the previous unit is
+            // done (V(u0) is needed only after S(u0) and its softmax, so it can wait).
             const bool is_k = warp == 0;
             const int ns = is_k ? NK : NV;
             uint64_t* full = is_k ? k_full : v_full;
@@ -591,12 +578,24 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
             uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
             tma_prefetch_desc(tm);
-            int L = 0;  // tiles issued so far into this ring
+            if (!is_k) tma_prefetch_desc(&tm_q);
+            int L = 0;   // tiles issued so far into this ring
+            int rq = 0;  // Q loads issued
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int w = zigzag_unit(cta, r, G);
                 if (w >= p.nunits) break;
                 const Unit u = unit_at(w);
+                if (!is_k) {
+                    if (r > 0 && !wait_or_abort(&q_empty, (r - 1) & 1, &abort_flag)) break;
+                    ++rq;
+                    mbar_arrive_expect_tx(&q_full, (u.has_b ? 2 : 1) * C::kQBytes);
+                    for (int x = 0; x < (u.has_b ? 2 : 1); ++x)
+#pragma unroll
+                        for (int dc = 0; dc < D / 64; ++dc)
+                            tma_load_3d(sm + (x ? C::kQBOff : C::kQAOff) + dc * (kBM * 128), &tm_q,
+                                        dc * 64, u.t[x].q0, u.bh, &q_full);
+                }
                 for (int j = u.u0; j < u.u1; ++j, ++L) {
                     const int slot = L % ns;
                     if (L >= ns && !wait_or_abort(&empty[slot], ((L / ns) - 1) & 1, &abort_flag)) {
@@ -612,98 +611,96 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             }
             if (abort_flag) {  // let copies in flight land before the CTA exits
                 for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
+                if (rq > 0) wait_bounded(&q_full, (rq - 1) & 1);
             }
-        } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
+        } else if ((warp == 1 || warp == 3) && lane == 0) {
+            // ------------------------------------------------ MMA issuers, one per Q tile
+            // One thread issues tcgen05.mma at about one per 80-100 cycles, slower than the
+            // tensor pipe runs an M=128 N=128 K=16 product, and every wait or commit it makes
+            // between products leaves the pipe idle.  So tile A's products come from warp 1
+            // and tile B's from warp 3, taking turns per KV tile (a token passed through the
+            // turn barriers keeps the pipe order PV_A S_A | PV_B S_B | ...): each issuer does
+            // its waits while the other one issues, then its turn's products back to back.
+            // K and V slots are released once both have arrived (count-2 barriers).
+            const int x = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-            const uint64_t qd[2] = {sw128_desc(smem_u32(sm + C::kQAOff), 16, 1024),
-                                    sw128_desc(smem_u32(sm + C::kQBOff), 16, 1024)};
+            const uint64_t qd = sw128_desc(smem_u32(sm + (x ? C::kQBOff : C::kQAOff)), 16, 1024);
             const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
             const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
-            const uint32_t col_s[2] = {0u, (uint32_t)BN};
-            const uint32_t col_o[2] = {(uint32_t)(2 * BN), (uint32_t)(2 * BN + D)};
-            int Lbase = 0;        // ring index (K and V alike) of the unit's first tile
-            int cnt[2] = {0, 0};  // S products issued so far per tile (phase of s/p_full)
+            const uint32_t tm_sx = tmem + (x ? (uint32_t)BN : 0u);
+            const uint32_t tm_ox = tmem + (uint32_t)(2 * BN) + (x ? (uint32_t)D : 0u);
+            uint64_t* const sfull = &s_full[x];
+            uint64_t* const pfull = &p_full[x];
+            int Lbase = 0;  // ring index (K and V alike) of the unit's first tile
+            int cnt = 0;    // S products of this tile issued so far (phase of s/p_full)
+            int turns = 0;  // turns taken so far (phase of turn[x])
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int w = zigzag_unit(cta, r, G);
                 if (w >= p.nunits) break;
                 const Unit u = unit_at(w);
+                const TileRange t = x ? u.t[1] : u.t[0];
                 if (!wait_or_abort(&q_full, r & 1, &abort_flag)) break;
-                tc_fence_after();
-                bool freed[2] = {r == 0, r == 0};  // previous unit's O_X read out?
-                const int cbase[2] = {cnt[0], cnt[1]};
+                bool freed = r == 0;  // previous unit's O_X read out?
+                const int cbase = cnt;
                 const int nu = u.u1 - u.u0;
                 if (nu == 0) tc_commit(&q_empty);
                 for (int j = u.u0; ok && j <= u.u1 && nu > 0; ++j) {
-                    const int jj = j - u.u0;
-                    const int Lk = Lbase + jj, Lv = Lk - 1;  // K(j), V(j-1)
-                    bool in_k[2], in_v[2];
-#pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        in_k[x] = j < u.u1 && j >= u.t[x].kt0 && j < u.t[x].kt0 + u.t[x].n;
-                        in_v[x] = j > u.u0 && j - 1 >= u.t[x].kt0 && j - 1 < u.t[x].kt0 + u.t[x].n;
-                    }
+                    const int Lk = Lbase + (j - u.u0), Lv = Lk - 1;  // K(j), V(j-1)
                     const bool have_k = j < u.u1, have_v = j > u.u0;
-                    if (have_k && !wait_or_abort(&k_full[Lk % NK], (Lk / NK) & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (have_v && !wait_or_abort(&v_full[Lv % NV], (Lv / NV) & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t kd = desc_add(kd0, (uint32_t)((Lk % NK) * C::kSlotBytes));
-                    const uint64_t vd = desc_add(vd0, (uint32_t)(((Lv + NV) % NV) * C::kSlotBytes));
-#pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        if (in_v[x]) {
-                            // O_X += P_X(j-1) V(j-1)
-                            const int i = (j - 1) - u.t[x].kt0;
-                            if (!freed[x]) {
-                                if (!wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag)) {
-                                    ok = false;
-                                    break;
-                                }
-                                freed[x] = true;
-                            }
-                            if (!wait_or_abort(&p_full[x], (cbase[x] + i) & 1, &abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-#pragma unroll
-                            for (int kk = 0; kk < BN / 16; ++kk)
-                                tc_mma_ts(tmem + col_o[x], tmem + col_s[x] + kk * 8,
-                                          desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-                            if (i == u.t[x].n - 1) tc_commit(&o_done[x]);  // the unit's last into O_X
-                        }
-                        // V(j-1) is free once the last product reading it is done
-                        if (have_v && (x == 1 || !in_v[1])) {
-                            if (x == 1 ? in_v[1] : true) tc_commit(&v_empty[(Lv + NV) % NV]);
-                        }
-                        if (in_k[x]) {
-                            // S_X = Q_X K(j)^T
-#pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                                const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-                                tc_mma_ss(tmem + col_s[x], desc_add(qd[x], off_a), desc_add(kd, off_b),
-                                          idesc_s, kk > 0 ? 1u : 0u);
-                            }
-                            tc_commit(&s_full[x]);
-                            ++cnt[x];
-                        }
-                    }
+                    const bool in_k = have_k && j >= t.kt0 && j < t.kt0 + t.n;
+                    const bool in_v = have_v && j - 1 >= t.kt0 && j - 1 < t.kt0 + t.n;
+                    const int ks = Lk % NK, vs = (Lv + NV) % NV;
+                    // everything this turn's products need, before taking the turn
+                    if (have_v) ok = wait_or_abort(&v_full[vs], (Lv / NV) & 1, &abort_flag);
+                    if (ok && in_v && !freed) ok = freed = wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag);
+                    const int i = (j - 1) - t.kt0;  // index of V(j-1) within this tile's range
+                    if (ok && in_v) ok = wait_or_abort(pfull, (cbase + i) & 1, &abort_flag);
+                    if (ok && have_k) ok = wait_or_abort(&k_full[ks], (Lk / NK) & 1, &abort_flag);
+                    if (ok) ok = wait_or_abort(&turn[x], turns & 1, &abort_flag);
                     if (!ok) break;
-                    if (have_k) tc_commit(&k_empty[Lk % NK]);  // K(j) consumed
-                    if (j == u.u1 - 1) tc_commit(&q_empty);   // every S of this unit issued
+                    ++turns;
+                    tc_fence_after();
+                    if (in_v) {
+                        // O_X += P_X(j-1) V(j-1)
+                        const uint64_t vd = desc_add(vd0, (uint32_t)(vs * C::kSlotBytes));
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            tc_mma_ts(tm_ox, tm_sx + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
+                                      (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (in_k) {
+                        // S_X = Q_X K(j)^T
+                        const uint64_t kd = desc_add(kd0, (uint32_t)(ks * C::kSlotBytes));
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                            const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+                            tc_mma_ss(tm_sx, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s,
+                                      kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    mbar_arrive(&turn[x ^ 1]);  // the other tile's turn
+                    if (in_k) {
+                        tc_commit(sfull);
+                        ++cnt;
+                    }
+                    if (in_v && i == t.n - 1) tc_commit(&o_done[x]);  // the unit's last into O_X
+                    // this tile is done with V(j-1) and K(j) once the products above finish
+                    // (or at once if it never reads them)
+                    if (have_v) {
+                        if (in_v) tc_commit(&v_empty[vs]);
+                        else mbar_arrive(&v_empty[vs]);
+                    }
+                    if (have_k) {
+                        if (in_k) tc_commit(&k_empty[ks]);
+                        else mbar_arrive(&k_empty[ks]);
+                    }
+                    if (j == u.u1 - 1) tc_commit(&q_empty);  // every S of this tile issued
                 }
                 // a tile with no product this unit still consumes the epilogue's o_free phase
-                for (int x = 0; ok && x < 2; ++x)
-                    if (!freed[x] && !wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag)) ok = false;
+                if (ok && !freed && !wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag)) ok = false;
                 Lbase += nu;
             }
             tc_commit(&mma_drain);
