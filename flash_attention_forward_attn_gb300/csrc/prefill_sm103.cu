@@ -315,16 +315,17 @@ __global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
             const int k0 = (tr.kt0 + j) * BN;
             const bool edge = (p.causal && k0 + BN - 1 > tr.qpos_lo) || (k0 + BN > p.skv) ||
                               (p.window > 0 && k0 < tr.qpos_hi - p.window + 1);
+            // scale first (for scale <= 0), then mask: a masked key is -inf whatever the sign
+            if (!c_pos) {
+#pragma unroll
+                for (int e = 0; e < BN; ++e) v[e] *= c;
+            }
             if (edge) {
 #pragma unroll
                 for (int e = 0; e < BN; ++e) {
                     const int key = k0 + e;
                     if (key < key_lo || key > key_hi) v[e] = -INFINITY;
                 }
-            }
-            if (!c_pos) {
-#pragma unroll
-                for (int e = 0; e < BN; ++e) v[e] *= c;
             }
             float mx[8];
 #pragma unroll
@@ -748,22 +749,23 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 const int k0 = (t.kt0 + i) * BN;
                 const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
                                   (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
-                // S row of this tile from TMEM, masked (edge tiles) and, for scale <= 0, scaled
+                // S row of this tile from TMEM, scaled for scale <= 0, then masked (edge tiles;
+                // a masked key is -inf whatever the sign of the scale)
                 auto load_s = [&](float* v) {
                     uint32_t rr[BN];
                     tmem_ld128(tm_s, rr);
 #pragma unroll
                     for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(rr[e]);
+                    if (!c_pos) {
+#pragma unroll
+                        for (int e = 0; e < BN; ++e) v[e] *= c;
+                    }
                     if (edge) {
 #pragma unroll
                         for (int e = 0; e < BN; ++e) {
                             const int key = k0 + e;
                             if (key < key_lo || key > key_hi) v[e] = -INFINITY;
                         }
-                    }
-                    if (!c_pos) {
-#pragma unroll
-                        for (int e = 0; e < BN; ++e) v[e] *= c;
                     }
                 };
                 // P = 2^(v * cm - m_e) packed to bf16 pairs; returns its row sum

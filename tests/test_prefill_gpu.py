@@ -58,6 +58,20 @@ def test_prefill_small_all_rows(case, cuda_device):
         assert (o.float().cpu().numpy()[masked] == 0).all()
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.07])
+@pytest.mark.parametrize("d,window", [(128, 0), (64, 40), (256, 90)])
+def test_prefill_nonpositive_scale(scale, d, window, cuda_device):
+    """scale <= 0 is a valid finite scale: masked keys still get zero weight (scale 0 gives a
+    uniform average over the allowed keys, a negative scale favours the least similar)."""
+    w = C.PrefillWorkload("nonpos", 1, 2, 1, 200, 260, d, True, window, seed=0x5CA1E + d)
+    qb, kb, vb = C.prefill_inputs_np(w)
+    q, k, v = (tensor_of_bits(x, cuda_device) for x in (qb, kb, vb))
+    o, lse = run_gpu(q, k, v, True, window, scale, torch.float32)
+    o_ref, lse_ref = oracle.prefill(qb, kb, vb, scale, True, window)
+    assert_o_close(o.cpu().numpy(), o_ref, f"scale={scale}")
+    assert_lse_close(lse.cpu().numpy(), lse_ref, f"scale={scale}")
+
+
 def test_prefill_empty_keys(cuda_device):
     q = torch.randn(1, 2, 50, 128, device=cuda_device).bfloat16()
     k = torch.empty(1, 2, 0, 128, device=cuda_device, dtype=torch.bfloat16)
