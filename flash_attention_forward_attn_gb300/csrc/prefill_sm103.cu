@@ -115,18 +115,19 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
         if (clock64() - t0 > kWaitLimitCycles) return;
 }
 
-// =========================================================================== one q-tile
-// Shared-memory / TMEM plan of the one-q-tile kernel (head_dim 256, BN = 64): Q stays
-// resident; K streams through a 3-slot ring (two tiles ahead) and V through a 2-slot
-// ring, each fed by its own producer thread so a K load never waits behind a V slot;
-// S is double-buffered in TMEM (2 x BN columns), O takes D columns, and P(j) is written
-// back into the first BN/2 columns of S(j)'s buffer as packed bf16 pairs.
+// =========================================================================== head_dim 256
+// Shared-memory / TMEM plan of the head_dim-256 kernel (BN = 64).  Shared memory: the Q
+// tile (64 KB), a 3-slot K ring and a 2-slot V ring (32 KB slots).  TMEM:
+//   S0 [0, BN)  S1 [BN, 2BN)  P0 [2BN, 2BN + BN/2)  P1 [2BN + BN/2, 3BN)  O [256, 256 + D)
+// P(T) has columns of its own, so S(T+2) may overwrite S buffer T % 2 as soon as the
+// softmax has read S(T), while PV(T) still reads P(T): the S products and the PV products
+// form two independent chains.
 template <int D>
-struct Cfg1Q {
+struct CfgW {
     static constexpr int BN = 64;
     static constexpr int kQBytes = D * kBM * 2;
     static constexpr int kSlotBytes = D * BN * 2;
-    static constexpr int kKSlots = 3;      // K runs two tiles ahead of the tile in use
+    static constexpr int kKSlots = 3;
     static constexpr int kVSlots = 2;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQBytes;
@@ -134,46 +135,54 @@ struct Cfg1Q {
     static constexpr int kSmem = kVOff + kVSlots * kSlotBytes;
     static constexpr int kDynBytes = kSmem + 1024;
     static constexpr int kTmemCols = 512;
-    static constexpr int kSCol = 0;        // S buffers at [0, 2 BN)
-    static constexpr int kOCol = 2 * BN;   // O at [2 BN, 2 BN + D)
-    static constexpr int kThreads = 256;
-    static_assert(2 * BN + D <= kTmemCols, "TMEM budget");
+    static constexpr uint32_t kColP = 2 * BN;  // P buffers at [2 BN, 3 BN)
+    static constexpr uint32_t kColO = 256;     // O at [256, 256 + D)
+    static constexpr int kThreads = 384;
+    static_assert(3 * BN <= (int)kColO && kColO + D <= kTmemCols, "TMEM budget");
     static_assert(kDynBytes + 512 <= 232448, "shared memory budget");
 };
 
-// One CTA = one 128-row query tile of one head.  Warp 0: TMA producer of Q and K; warp 3:
-// TMA producer of V; warp 1: MMA issuer; warp 2: TMEM owner; warps 4-7: softmax (thread =
-// row = TMEM lane).  MMA order:
-// S(0), S(1), then per tile j: O += P(j) V(j) (P from TMEM), S(j+2) into the buffer that
-// held S(j) and P(j) -- the product reading P(j) is issued first and the tensor pipe runs
-// them in issue order.  The softmax of tile j+1 overlaps PV(j) and S(j+2).
+// Persistent: each CTA loops over work units (one 128-row query tile of one head, heaviest
+// first, zig-zag over CTAs).  Roles:
+//   warp 0: Q and K producer      warp 2: V producer (and TMEM owner)
+//   warps 1 / 4: S issuers of the even / odd KV tiles   S(T) = Q K(T)^T into buffer T % 2
+//   warp 3: PV issuer  O += P(T) V(T)
+//   warps 8-11: softmax (thread = query row = TMEM lane) and the unit's epilogue.
+// An S tile of head_dim 256 takes 16 products of N = BN; two issuers keep that chain ahead
+// of the softmax.  The first PV of a unit waits until the previous unit's epilogue has
+// read O out of TMEM.
 template <int D>
-__global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
+__global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using C = Cfg1Q<D>;
+    using C = CfgW<D>;
     constexpr int BN = C::BN;
     constexpr int NK = C::kKSlots;
     constexpr int NV = C::kVSlots;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
-    __shared__ uint64_t s_full[2], p_full[2], o_done[2], mma_drain;
+    __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
+    __shared__ uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+    __shared__ uint64_t o_done, o_free, mma_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbh = gridDim.x / p.nqt;
-    const int qt = p.nqt - 1 - (int)(blockIdx.x / nbh);  // heaviest causal tiles first
-    const int bh = (int)(blockIdx.x % nbh);
-    const int bidx = bh / p.hq, h = bh % p.hq;
-    const int kvz = bidx * p.hkv + h / p.group;
-    const TileRange tr = tile_range<BN>(p, qt);
-    const int n = tr.n;
+    const int G = gridDim.x, cta = blockIdx.x;
+
+    // unit w -> (query tile, batch*head, kv batch*head) and its KV tile range
+    auto unit_at = [&](int w, int& bh, int& kvz) -> TileRange {
+        const int qt = p.nqt - 1 - w / p.nbh;
+        bh = w % p.nbh;
+        const int bidx = bh / p.hq, h = bh % p.hq;
+        kvz = bidx * p.hkv + h / p.group;
+        return tile_range<BN>(p, qt);
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&q_full, 1);
+        mbar_init(&q_empty, 2);  // both S issuers, after their last product of the unit
         for (int i = 0; i < NK; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
@@ -184,10 +193,13 @@ __global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 128);
             mbar_init(&p_full[i], 128);
-            mbar_init(&o_done[i], 1);
+            mbar_init(&p_free[i], 1);
         }
-        mbar_init(&mma_drain, 1);
+        mbar_init(&o_done, 1);
+        mbar_init(&o_free, 128);
+        mbar_init(&mma_drain, 3);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -200,222 +212,321 @@ __global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 0 || warp == 3) {
-        // ------------------------------------------------------------ TMA producers
-        if (lane == 0 && n > 0) {
-            const bool is_k = warp == 0;
-            const int ns = is_k ? NK : NV;
-            uint64_t* full = is_k ? k_full : v_full;
-            uint64_t* empty = is_k ? k_empty : v_empty;
-            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
-            uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
+    if ((warp == 0 || warp == 2) && lane == 0) {
+        // -------------------------------------------- Q + K producer / V producer
+        const bool is_k = warp == 0;
+        uint64_t* full = is_k ? k_full : v_full;
+        uint64_t* empty = is_k ? k_empty : v_empty;
+        const int ns = is_k ? NK : NV;
+        const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+        uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
+        tma_prefetch_desc(tm);
+        if (is_k) tma_prefetch_desc(&tm_q);
+        int L = 0;   // tiles issued into this ring
+        int rq = 0;  // Q tiles issued
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int w = zigzag_unit(cta, r, G);
+            if (w >= p.nunits) break;
+            int bh, kvz;
+            const TileRange t = unit_at(w, bh, kvz);
+            if (t.n == 0) continue;
             if (is_k) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
+                // the Q tile is free once every S product of the previous unit is done
+                if (rq > 0 && !wait_or_abort(&q_empty, (rq - 1) & 1, &abort_flag)) break;
+                ++rq;
                 mbar_arrive_expect_tx(&q_full, C::kQBytes);
 #pragma unroll
                 for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(sm + C::kQOff + dc * (kBM * 128), &tm_q, dc * 64, tr.q0, bh, &q_full);
-            } else {
-                tma_prefetch_desc(&tm_v);
+                    tma_load_3d(sm + C::kQOff + dc * (kBM * 128), &tm_q, dc * 64, t.q0, bh, &q_full);
             }
-            int issued = 0;
-            for (int j = 0; j < n; ++j) {
-                const int slot = j % ns;
-                if (j >= ns && !wait_or_abort(&empty[slot], ((j / ns) - 1) & 1, &abort_flag)) break;
-                const int k0 = (tr.kt0 + j) * BN;
+            for (int i = 0; i < t.n; ++i, ++L) {
+                const int slot = L % ns;
+                if (L >= ns && !wait_or_abort(&empty[slot], ((L / ns) - 1) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive_expect_tx(&full[slot], C::kSlotBytes);
 #pragma unroll
                 for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(ring + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64, k0, kvz,
-                                &full[slot]);
-                issued = j + 1;
-            }
-            if (abort_flag) {  // let copies in flight land before the CTA exits
-                if (is_k) wait_bounded(&q_full, 0);
-                for (int j = max(0, issued - ns); j < issued; ++j)
-                    wait_bounded(&full[j % ns], (j / ns) & 1);
+                    tma_load_3d(ring + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64,
+                                (t.kt0 + i) * BN, kvz, &full[slot]);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-            const uint64_t qd = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
-            const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
-            const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
-            bool ok = wait_or_abort(&q_full, 0, &abort_flag);
-            tc_fence_after();
-            auto issue_s = [&](int t) -> bool {
-                const int slot = t % NK;
-                if (!wait_or_abort(&k_full[slot], (t / NK) & 1, &abort_flag)) return false;
-                tc_fence_after();
-                const uint64_t kd = desc_add(kd0, (uint32_t)(slot * C::kSlotBytes));
-                const uint32_t tm_s = tmem + C::kSCol + (t & 1) * BN;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                    const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-                    tc_mma_ss(tm_s, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(&s_full[t & 1]);
-                tc_commit(&k_empty[slot]);  // K(t) consumed once this product is done
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && n > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n; ++j) {
-                const int s = j & 1;
-                if (!wait_or_abort(&p_full[s], (j >> 1) & 1, &abort_flag)) break;
-                const int slot = j % NV;
-                if (!wait_or_abort(&v_full[slot], (j / NV) & 1, &abort_flag)) break;
-                tc_fence_after();
-                const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    tc_mma_ts(tmem + C::kOCol, tmem + C::kSCol + s * BN + kk * 8,
-                              desc_add(vd, kk * 16 * 128), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&o_done[s]);
-                tc_commit(&v_empty[slot]);  // V(j) consumed
-                if (j + 2 < n) ok = issue_s(j + 2);
-            }
-            tc_commit(&mma_drain);
-            wait_bounded(&mma_drain, 0);
+        if (abort_flag) {  // let copies in flight land before the CTA exits
+            for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
+            if (rq > 0) wait_bounded(&q_full, (rq - 1) & 1);
         }
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ softmax
-        const int row = (warp & 3) * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tm_o = tmem + lane_off + C::kOCol;
-        const int q_row = tr.q0 + row;
-        const int qpos = tr.qpos_lo + row;
-        const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
-        const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
-        const float c = p.c;
-        const bool c_pos = c > 0.f;
-        const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
-        float m_used = -INFINITY, l_sum = 0.f;
+    } else if ((warp == 1 || warp == 4) && lane == 0) {
+        // --------------------------------------------- S issuers (even / odd tiles)
+        const int par = warp == 1 ? 0 : 1;
+        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
+        const uint64_t qd = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
+        const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
+        int T = 0;   // tiles of all units so far (= K ring index)
+        int uq = 0;  // units with tiles so far (phase of q_full)
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            const int s = j & 1;
-            if (!wait_or_abort(&s_full[s], (j >> 1) & 1, &abort_flag)) {
-                ok = false;
-                break;
-            }
+        for (int r = 0; ok; ++r) {
+            const int w = zigzag_unit(cta, r, G);
+            if (w >= p.nunits) break;
+            int bh, kvz;
+            const TileRange t = unit_at(w, bh, kvz);
+            if (t.n == 0) continue;
+            if (!wait_or_abort(&q_full, uq & 1, &abort_flag)) break;
+            ++uq;
             tc_fence_after();
-            const uint32_t tm_s = tmem + lane_off + C::kSCol + s * BN;
-            float v[BN];
-            {
-                uint32_t r[BN];
-                tmem_ld64(tm_s, r);
-#pragma unroll
-                for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(r[e]);
-            }
-            const int k0 = (tr.kt0 + j) * BN;
-            const bool edge = (p.causal && k0 + BN - 1 > tr.qpos_lo) || (k0 + BN > p.skv) ||
-                              (p.window > 0 && k0 < tr.qpos_hi - p.window + 1);
-            // scale first (for scale <= 0), then mask: a masked key is -inf whatever the sign
-            if (!c_pos) {
-#pragma unroll
-                for (int e = 0; e < BN; ++e) v[e] *= c;
-            }
-            if (edge) {
-#pragma unroll
-                for (int e = 0; e < BN; ++e) {
-                    const int key = k0 + e;
-                    if (key < key_lo || key > key_hi) v[e] = -INFINITY;
+            for (int i = 0; i < t.n; ++i, ++T) {
+                if ((T & 1) != par) continue;
+                const int b = T & 1, slot = T % NK;
+                // S buffer b is free once the softmax has read S(T-2) out of it
+                if (T >= 2 && !wait_or_abort(&s_free[b], ((T >> 1) - 1) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
                 }
-            }
-            float mx[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
-            float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            if (c_pos) tmax *= c;  // -inf stays -inf
-            const float m_new = fmaxf(m_used, tmax);
-            const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
-            if (m_used == -INFINITY) m_used = m_new;  // nothing accumulated yet for this row
-            if (__any_sync(0xffffffffu, need)) {
-                // O holds PV(j-1) only once that product has finished
-                if (!wait_or_abort(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, &abort_flag)) {
+                if (!wait_or_abort(&k_full[slot], (T / NK) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                const uint64_t kd = desc_add(kd0, (uint32_t)(slot * C::kSlotBytes));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                    const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+                    tc_mma_ss(tmem + b * BN, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s,
+                              kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[b]);
+                tc_commit(&k_empty[slot]);  // K(T) consumed once this product is done
+            }
+            if (ok) tc_commit(&q_empty);  // this issuer's products of the unit read Q no more
+        }
+        tc_commit(&mma_drain);
+        wait_bounded(&mma_drain, 0);
+    } else if (warp == 3 && lane == 0) {
+        // ----------------------------------------------------------- PV issuer
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
+        const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
+        int T = 0;
+        int uo = 0;  // units with tiles so far (o_free completes once per such unit)
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int w = zigzag_unit(cta, r, G);
+            if (w >= p.nunits) break;
+            int bh, kvz;
+            const TileRange t = unit_at(w, bh, kvz);
+            if (t.n == 0) continue;
+            // the previous unit's epilogue must have read O before it is overwritten
+            if (uo > 0 && !wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag)) break;
+            ++uo;
+            for (int i = 0; i < t.n; ++i, ++T) {
+                const int b = T & 1, slot = T % NV;
+                if (!wait_or_abort(&p_full[b], (T >> 1) & 1, &abort_flag) ||
+                    !wait_or_abort(&v_full[slot], (T / NV) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    tc_mma_ts(tmem + C::kColO, tmem + C::kColP + b * (BN / 2) + kk * 8,
+                              desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&p_free[b]);      // P buffer b may be rewritten; O holds PV(T)
+                tc_commit(&v_empty[slot]);  // V(T) consumed
+                if (i == t.n - 1) tc_commit(&o_done);
+            }
+        }
+        tc_commit(&mma_drain);
+        wait_bounded(&mma_drain, 0);
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t tm_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t tm_o = tm_row + C::kColO;
+        const float c = p.c;
+        const bool c_pos = c > 0.f;
+        const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
+        int T = 0;      // S tiles consumed so far (across units)
+        int ocnt = 0;   // units with tiles so far (phase of o_done)
+        bool ok = true;
+        // Waits end with a warp-uniform verdict, so that a wait given up on never leaves
+        // part of a warp ahead of a warp-collective tcgen05 access.
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_or_abort(bar, parity, &abort_flag));
+        };
+        for (int r = 0;; ++r) {
+            const int w = zigzag_unit(cta, r, G);
+            if (w >= p.nunits) break;
+            int bh, kvz;
+            const TileRange t = unit_at(w, bh, kvz);
+            const int q_row = t.q0 + row;
+            const int qpos = t.qpos_lo + row;
+            const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
+            const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+            float m_used = -INFINITY, l_sum = 0.f;
+            for (int i = 0; ok && i < t.n; ++i, ++T) {
+                const int b = T & 1;
+                if (!wait_warp(&s_full[b], (T >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tm_s = tm_row + b * BN;
+                const int k0 = (t.kt0 + i) * BN;
+                const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
+                                  (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
+                // the S row from TMEM, scaled for scale <= 0, then masked (edge tiles; a
+                // masked key is -inf whatever the sign of the scale)
+                auto load_s = [&](float* v) {
+                    uint32_t rr[BN];
+                    tmem_ld64(tm_s, rr);
+#pragma unroll
+                    for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(rr[e]);
+                    if (!c_pos) {
+#pragma unroll
+                        for (int e = 0; e < BN; ++e) v[e] *= c;
+                    }
+                    if (edge) {
+#pragma unroll
+                        for (int e = 0; e < BN; ++e) {
+                            const int key = k0 + e;
+                            if (key < key_lo || key > key_hi) v[e] = -INFINITY;
+                        }
+                    }
+                };
+                // P = 2^(v * cm - m_e) packed to bf16 pairs; returns its sum, and the packed
+                // maximum through pmax
+                auto exps = [&](const float* v, float m_e, uint32_t* pk, uint32_t& pmax) -> float {
+                    float ls[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+                    pmax = 0u;
+#pragma unroll
+                    for (int e = 0; e < BN / 2; ++e) {
+                        const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
+                        const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
+                        ls[(2 * e) & 7] += p0;
+                        ls[(2 * e + 1) & 7] += p1;
+                        pk[e] = pack_bf16(p0, p1);
+                        pmax = __vmaxu2(pmax, pk[e]);
+                    }
+                    return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                };
+                uint32_t pk[BN / 2];
+                float l_tile = 0.f;
+                // Common case: one pass of exponents against the running max m_used.  The
+                // row's max grew by more than 2^kRescaleLog2 exactly when an exponent exceeds
+                // 2^kRescaleLog2, read off the packed bf16 values (an unsigned 16-bit max
+                // orders non-negative bf16 values by size).  A row without a finite max yet
+                // takes the exact path; decided per warp, as the TMEM loads are collective.
+                bool redo = __any_sync(0xffffffffu, m_used == -INFINITY);
+                if (!redo) {
+                    float v[BN];
+                    load_s(v);
+                    uint32_t pmax;
+                    l_tile = exps(v, m_used, pk, pmax);
+                    constexpr uint32_t kTwoPow8 = 0x4380u;  // bf16 bits of 2^kRescaleLog2 = 256
+                    redo = __any_sync(0xffffffffu,
+                                      (pmax & 0xFFFFu) > kTwoPow8 || (pmax >> 16) > kTwoPow8);
+                }
+                if (redo) {
+                    // Exact path: the tile max (S(T) is still in TMEM), O and l rescaled where
+                    // the max moves, the exponents recomputed.
+                    float v[BN];
+                    load_s(v);
+                    float mx[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
+                    float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    if (c_pos) tmax *= c;  // -inf stays -inf
+                    const float m_new = fmaxf(m_used, tmax);
+                    const bool need = (m_used != -INFINITY) && (m_new > m_used + kRescaleLog2);
+                    if (__any_sync(0xffffffffu, need)) {
+                        // O holds the unit's products up to PV(T-1): let it land, then scale
+                        // it in place
+                        if (!wait_warp(&p_free[(T - 1) & 1], ((T - 1) >> 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const float alpha = need ? ex2(m_used - m_new) : 1.0f;
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tm_o + c0, r);
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t rr[32];
+                            tmem_ld32(tm_o + c0, rr);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st32(tm_o + c0, r);
+                            for (int e = 0; e < 32; ++e)
+                                rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                            tmem_st32(tm_o + c0, rr);
+                        }
+                        tmem_wait_st();
+                        if (need) l_sum *= alpha;
+                    }
+                    if (m_used == -INFINITY || need) m_used = m_new;  // nothing accumulated yet
+                    uint32_t pmax;
+                    l_tile = exps(v, (m_used == -INFINITY) ? 0.f : m_used, pk, pmax);
                 }
-                if (need) {
-                    l_sum *= alpha;
-                    m_used = m_new;
+                l_sum += l_tile;
+                tc_fence_before();
+                mbar_arrive(&s_free[b]);  // S(T) has been read
+                // P buffer b is free once PV(T-2) is done
+                if (T >= 2 && !wait_warp(&p_free[b], ((T >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st32(tm_row + C::kColP + b * (BN / 2), pk);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full[b]);
+            }
+            // ------------------------------------------------------------ epilogue
+            bool have_o = false;
+            if (t.n > 0) {
+                have_o = ok && wait_warp(&o_done, ocnt & 1);
+                ++ocnt;
+                tc_fence_after();
+            }
+            const bool row_valid = t.rows > 0 && row < t.rows;
+            const bool live = have_o && l_sum > 0.f;
+            const float inv = live ? 1.0f / l_sum : 0.f;
+            const size_t orow = (size_t)bh * p.sq + q_row;
+            if (row_valid && p.lse != nullptr)
+                p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t rr[32];
+                if (t.n > 0) {
+                    tmem_ld32(tm_o + c0, rr);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                }
+                if (row_valid) {
+                    if (p.o_f32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(rr[4 * e]) * inv, __uint_as_float(rr[4 * e + 1]) * inv,
+                                                 __uint_as_float(rr[4 * e + 2]) * inv, __uint_as_float(rr[4 * e + 3]) * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(
+                                pack_bf16(__uint_as_float(rr[8 * e]) * inv, __uint_as_float(rr[8 * e + 1]) * inv),
+                                pack_bf16(__uint_as_float(rr[8 * e + 2]) * inv, __uint_as_float(rr[8 * e + 3]) * inv),
+                                pack_bf16(__uint_as_float(rr[8 * e + 4]) * inv, __uint_as_float(rr[8 * e + 5]) * inv),
+                                pack_bf16(__uint_as_float(rr[8 * e + 6]) * inv, __uint_as_float(rr[8 * e + 7]) * inv));
+                    }
                 }
             }
-            const float m_e = (m_used == -INFINITY) ? 0.f : m_used;
-            uint32_t pk[BN / 2];
-            float ls[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-#pragma unroll
-            for (int e = 0; e < BN / 2; ++e) {
-                const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
-                const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
-                ls[(2 * e) & 7] += p0;
-                ls[(2 * e + 1) & 7] += p1;
-                pk[e] = pack_bf16(p0, p1);
-            }
-            l_sum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-            tmem_st32(tm_s, pk);  // P(j) over the first BN/2 columns of S(j)'s buffer
-            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_full[s]);
-        }
-        // ------------------------------------------------------------ epilogue
-        bool have_o = false;
-        if (ok && n > 0) {
-            have_o = wait_or_abort(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, &abort_flag);
-            tc_fence_after();
-        }
-        const bool row_valid = q_row < p.sq;
-        const bool live = have_o && l_sum > 0.f;
-        const float inv = live ? 1.0f / l_sum : 0.f;
-        const size_t orow = (size_t)bh * p.sq + q_row;
-        if (row_valid && p.lse != nullptr)
-            p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            if (n > 0) {
-                tmem_ld32(tm_o + c0, r);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = 0u;
-            }
-            if (!row_valid) continue;
-            if (p.o_f32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                         __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
-            } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_uint4(
-                        pack_bf16(__uint_as_float(r[8 * e]) * inv, __uint_as_float(r[8 * e + 1]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv),
-                        pack_bf16(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv));
-            }
+            if (t.n > 0) mbar_arrive(&o_free);  // O has been read: the next unit may overwrite it
         }
     }
     tc_fence_before();
@@ -423,26 +534,6 @@ __global__ void __launch_bounds__(Cfg1Q<D>::kThreads, 1) prefill1q_kernel(
     tc_fence_after();
     if (threadIdx.x == 0 && abort_flag) atomicOr(&g_prefill_error, kDevErrTimeout);
     if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
-}
-
-template <int D>
-attn_status prefill1q_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                             const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
-    using C = Cfg1Q<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(prefill1q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kDynBytes) != cudaSuccess) {
-            cudaGetLastError();
-            return ATTN_ERR_CUDA;
-        }
-        attr_set = true;
-    }
-    const long long grid = (long long)p.nqt * a.b * a.hq;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    prefill1q_kernel<D><<<(unsigned)grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, p);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_OK;
 }
 
 // =========================================================================== two q-tiles
@@ -963,6 +1054,29 @@ int num_sms() {
 }
 
 template <int D>
+attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
+    using C = CfgW<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(prefill_wide_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kDynBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        attr_set = true;
+    }
+    const long long units = (long long)p.nqt * a.b * a.hq;
+    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    PrefillParams pp = p;
+    pp.nunits = (int)units;
+    const int grid = (int)(units < num_sms() ? units : num_sms());
+    prefill_wide_kernel<D><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, pp);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+template <int D>
 attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
     using C = Cfg2Q<D>;
@@ -1004,7 +1118,7 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
 
 template <int D>
 attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
-    constexpr int BN = (D <= 128) ? Cfg2Q<(D <= 128 ? D : 128)>::BN : Cfg1Q<(D > 128 ? D : 256)>::BN;
+    constexpr int BN = (D <= 128) ? Cfg2Q<(D <= 128 ? D : 128)>::BN : CfgW<(D > 128 ? D : 256)>::BN;
     CUtensorMap tq, tk, tv;
     const uint64_t skv = a.skv > 0 ? (uint64_t)a.skv : 1u;
     uint64_t qd[3] = {(uint64_t)D, (uint64_t)a.sq, (uint64_t)a.b * a.hq};
@@ -1036,7 +1150,7 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     if constexpr (D <= 128)
         return prefill2q_launch<D>(a, tq, tk, tv, p, stream);
     else
-        return prefill1q_launch<D>(a, tq, tk, tv, p, stream);
+        return prefill_wide_launch<D>(a, tq, tk, tv, p, stream);
 }
 
 }  // namespace
