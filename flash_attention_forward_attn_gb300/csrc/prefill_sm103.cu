@@ -137,7 +137,7 @@ struct CfgW {
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kColP = 2 * BN;  // P buffers at [2 BN, 3 BN)
     static constexpr uint32_t kColO = 256;     // O at [256, 256 + D)
-    static constexpr int kThreads = 384;
+    static constexpr int kThreads = 512;
     static_assert(3 * BN <= (int)kColO && kColO + D <= kTmemCols, "TMEM budget");
     static_assert(kDynBytes + 512 <= 232448, "shared memory budget");
 };
@@ -147,10 +147,19 @@ struct CfgW {
 //   warp 0: Q and K producer      warp 2: V producer (and TMEM owner)
 //   warps 1 / 4: S issuers of the even / odd KV tiles   S(T) = Q K(T)^T into buffer T % 2
 //   warp 3: PV issuer  O += P(T) V(T)
-//   warps 8-11: softmax (thread = query row = TMEM lane) and the unit's epilogue.
+//   warps 8-11: softmax (thread = query row = TMEM lane)
+//   warps 12-15: epilogue -- normalise O, write it and the LSE out
 // An S tile of head_dim 256 takes 16 products of N = BN; two issuers keep that chain ahead
-// of the softmax.  The first PV of a unit waits until the previous unit's epilogue has
-// read O out of TMEM.
+// of the softmax.  At the end of a unit the softmax hands its (max, sum) per row to the
+// epilogue warps through shared memory and goes on with the next unit's tiles; the next
+// unit's first PV waits until the epilogue has read O out of TMEM.  Register split per
+// warpgroup: roles kRegsRole, softmax kRegsSoftmax, epilogue the launch budget.
+constexpr int kRegsLaunch4 = 128;  // 512 threads
+constexpr int kRegsRole = 96;
+constexpr int kRegsSoftmax = 160;
+static_assert(256 * kRegsRole + 128 * kRegsSoftmax + 128 * kRegsLaunch4 <= 512 * kRegsLaunch4,
+              "register split");
+
 template <int D>
 __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -164,7 +173,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
-    __shared__ uint64_t o_done, o_free, mma_drain;
+    __shared__ uint64_t o_done, o_free, mma_drain, stats_full, stats_free;
+    __shared__ float2 stats[kBM];  // per row: the unit's running max and sum, for the epilogue
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -200,6 +210,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
         mbar_init(&o_done, 1);
         mbar_init(&o_free, 128);
         mbar_init(&mma_drain, 3);
+        mbar_init(&stats_full, 128);
+        mbar_init(&stats_free, 128);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -212,143 +224,147 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if ((warp == 0 || warp == 2) && lane == 0) {
-        // -------------------------------------------- Q + K producer / V producer
-        const bool is_k = warp == 0;
-        uint64_t* full = is_k ? k_full : v_full;
-        uint64_t* empty = is_k ? k_empty : v_empty;
-        const int ns = is_k ? NK : NV;
-        const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
-        uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
-        tma_prefetch_desc(tm);
-        if (is_k) tma_prefetch_desc(&tm_q);
-        int L = 0;   // tiles issued into this ring
-        int rq = 0;  // Q tiles issued
-        bool ok = true;
-        for (int r = 0; ok; ++r) {
-            const int w = zigzag_unit(cta, r, G);
-            if (w >= p.nunits) break;
-            int bh, kvz;
-            const TileRange t = unit_at(w, bh, kvz);
-            if (t.n == 0) continue;
-            if (is_k) {
-                // the Q tile is free once every S product of the previous unit is done
-                if (rq > 0 && !wait_or_abort(&q_empty, (rq - 1) & 1, &abort_flag)) break;
-                ++rq;
-                mbar_arrive_expect_tx(&q_full, C::kQBytes);
+    if (warp < 8) {
+        regs_dec<kRegsRole>();
+        if ((warp == 0 || warp == 2) && lane == 0) {
+            // -------------------------------------------- Q + K producer / V producer
+            const bool is_k = warp == 0;
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
+            const int ns = is_k ? NK : NV;
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
+            tma_prefetch_desc(tm);
+            if (is_k) tma_prefetch_desc(&tm_q);
+            int L = 0;   // tiles issued into this ring
+            int rq = 0;  // Q tiles issued
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int w = zigzag_unit(cta, r, G);
+                if (w >= p.nunits) break;
+                int bh, kvz;
+                const TileRange t = unit_at(w, bh, kvz);
+                if (t.n == 0) continue;
+                if (is_k) {
+                    // the Q tile is free once every S product of the previous unit is done
+                    if (rq > 0 && !wait_or_abort(&q_empty, (rq - 1) & 1, &abort_flag)) break;
+                    ++rq;
+                    mbar_arrive_expect_tx(&q_full, C::kQBytes);
 #pragma unroll
-                for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(sm + C::kQOff + dc * (kBM * 128), &tm_q, dc * 64, t.q0, bh, &q_full);
-            }
-            for (int i = 0; i < t.n; ++i, ++L) {
-                const int slot = L % ns;
-                if (L >= ns && !wait_or_abort(&empty[slot], ((L / ns) - 1) & 1, &abort_flag)) {
-                    ok = false;
-                    break;
+                    for (int dc = 0; dc < D / 64; ++dc)
+                        tma_load_3d(sm + C::kQOff + dc * (kBM * 128), &tm_q, dc * 64, t.q0, bh, &q_full);
                 }
-                mbar_arrive_expect_tx(&full[slot], C::kSlotBytes);
+                for (int i = 0; i < t.n; ++i, ++L) {
+                    const int slot = L % ns;
+                    if (L >= ns && !wait_or_abort(&empty[slot], ((L / ns) - 1) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[slot], C::kSlotBytes);
 #pragma unroll
-                for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(ring + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64,
-                                (t.kt0 + i) * BN, kvz, &full[slot]);
+                    for (int dc = 0; dc < D / 64; ++dc)
+                        tma_load_3d(ring + slot * C::kSlotBytes + dc * (BN * 128), tm, dc * 64,
+                                    (t.kt0 + i) * BN, kvz, &full[slot]);
+                }
             }
-        }
-        if (abort_flag) {  // let copies in flight land before the CTA exits
-            for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
-            if (rq > 0) wait_bounded(&q_full, (rq - 1) & 1);
-        }
-    } else if ((warp == 1 || warp == 4) && lane == 0) {
-        // --------------------------------------------- S issuers (even / odd tiles)
-        const int par = warp == 1 ? 0 : 1;
-        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
-        const uint64_t qd = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
-        const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
-        int T = 0;   // tiles of all units so far (= K ring index)
-        int uq = 0;  // units with tiles so far (phase of q_full)
-        bool ok = true;
-        for (int r = 0; ok; ++r) {
-            const int w = zigzag_unit(cta, r, G);
-            if (w >= p.nunits) break;
-            int bh, kvz;
-            const TileRange t = unit_at(w, bh, kvz);
-            if (t.n == 0) continue;
-            if (!wait_or_abort(&q_full, uq & 1, &abort_flag)) break;
-            ++uq;
-            tc_fence_after();
-            for (int i = 0; i < t.n; ++i, ++T) {
-                if ((T & 1) != par) continue;
-                const int b = T & 1, slot = T % NK;
-                // S buffer b is free once the softmax has read S(T-2) out of it
-                if (T >= 2 && !wait_or_abort(&s_free[b], ((T >> 1) - 1) & 1, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                if (!wait_or_abort(&k_full[slot], (T / NK) & 1, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
+            if (abort_flag) {  // let copies in flight land before the CTA exits
+                for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
+                if (rq > 0) wait_bounded(&q_full, (rq - 1) & 1);
+            }
+        } else if ((warp == 1 || warp == 4) && lane == 0) {
+            // --------------------------------------------- S issuers (even / odd tiles)
+            const int par = warp == 1 ? 0 : 1;
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
+            const uint64_t qd = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
+            const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
+            int T = 0;   // tiles of all units so far (= K ring index)
+            int uq = 0;  // units with tiles so far (phase of q_full)
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int w = zigzag_unit(cta, r, G);
+                if (w >= p.nunits) break;
+                int bh, kvz;
+                const TileRange t = unit_at(w, bh, kvz);
+                if (t.n == 0) continue;
+                if (!wait_or_abort(&q_full, uq & 1, &abort_flag)) break;
+                ++uq;
                 tc_fence_after();
-                const uint64_t kd = desc_add(kd0, (uint32_t)(slot * C::kSlotBytes));
+                for (int i = 0; i < t.n; ++i, ++T) {
+                    if ((T & 1) != par) continue;
+                    const int b = T & 1, slot = T % NK;
+                    // S buffer b is free once the softmax has read S(T-2) out of it
+                    if (T >= 2 && !wait_or_abort(&s_free[b], ((T >> 1) - 1) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!wait_or_abort(&k_full[slot], (T / NK) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t kd = desc_add(kd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                    const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-                    tc_mma_ss(tmem + b * BN, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s,
-                              kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                        const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+                        tc_mma_ss(tmem + b * BN, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s,
+                                  kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&s_full[b]);
+                    tc_commit(&k_empty[slot]);  // K(T) consumed once this product is done
                 }
-                tc_commit(&s_full[b]);
-                tc_commit(&k_empty[slot]);  // K(T) consumed once this product is done
+                if (ok) tc_commit(&q_empty);  // this issuer's products of the unit read Q no more
             }
-            if (ok) tc_commit(&q_empty);  // this issuer's products of the unit read Q no more
-        }
-        tc_commit(&mma_drain);
-        wait_bounded(&mma_drain, 0);
-    } else if (warp == 3 && lane == 0) {
-        // ----------------------------------------------------------- PV issuer
-        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-        const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
-        int T = 0;
-        int uo = 0;  // units with tiles so far (o_free completes once per such unit)
-        bool ok = true;
-        for (int r = 0; ok; ++r) {
-            const int w = zigzag_unit(cta, r, G);
-            if (w >= p.nunits) break;
-            int bh, kvz;
-            const TileRange t = unit_at(w, bh, kvz);
-            if (t.n == 0) continue;
-            // the previous unit's epilogue must have read O before it is overwritten
-            if (uo > 0 && !wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag)) break;
-            ++uo;
-            for (int i = 0; i < t.n; ++i, ++T) {
-                const int b = T & 1, slot = T % NV;
-                if (!wait_or_abort(&p_full[b], (T >> 1) & 1, &abort_flag) ||
-                    !wait_or_abort(&v_full[slot], (T / NV) & 1, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
+            tc_commit(&mma_drain);
+            wait_bounded(&mma_drain, 0);
+        } else if (warp == 3 && lane == 0) {
+            // ----------------------------------------------------------- PV issuer
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
+            const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
+            int T = 0;
+            int uo = 0;  // units with tiles so far (o_free completes once per such unit)
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int w = zigzag_unit(cta, r, G);
+                if (w >= p.nunits) break;
+                int bh, kvz;
+                const TileRange t = unit_at(w, bh, kvz);
+                if (t.n == 0) continue;
+                // the previous unit's epilogue must have read O before it is overwritten
+                if (uo > 0 && !wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag)) break;
+                ++uo;
+                for (int i = 0; i < t.n; ++i, ++T) {
+                    const int b = T & 1, slot = T % NV;
+                    if (!wait_or_abort(&p_full[b], (T >> 1) & 1, &abort_flag) ||
+                        !wait_or_abort(&v_full[slot], (T / NV) & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    tc_mma_ts(tmem + C::kColO, tmem + C::kColP + b * (BN / 2) + kk * 8,
-                              desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&p_free[b]);      // P buffer b may be rewritten; O holds PV(T)
-                tc_commit(&v_empty[slot]);  // V(T) consumed
-                if (i == t.n - 1) tc_commit(&o_done);
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc_mma_ts(tmem + C::kColO, tmem + C::kColP + b * (BN / 2) + kk * 8,
+                                  desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&p_free[b]);      // P buffer b may be rewritten; O holds PV(T)
+                    tc_commit(&v_empty[slot]);  // V(T) consumed
+                    if (i == t.n - 1) tc_commit(&o_done);
+                }
             }
+            tc_commit(&mma_drain);
+            wait_bounded(&mma_drain, 0);
         }
-        tc_commit(&mma_drain);
-        wait_bounded(&mma_drain, 0);
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------ softmax + epilogue
+    } else if (warp < 12) {
+        // ------------------------------------------------------------------ softmax
+        regs_inc<kRegsSoftmax>();
         const int row = (warp & 3) * 32 + lane;
         const uint32_t tm_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t tm_o = tm_row + C::kColO;
         const float c = p.c;
         const bool c_pos = c > 0.f;
         const float cm = c_pos ? c : 1.0f;  // exponent = x * cm - m
-        int T = 0;      // S tiles consumed so far (across units)
-        int ocnt = 0;   // units with tiles so far (phase of o_done)
+        int T = 0;   // S tiles consumed so far (across units)
+        int su = 0;  // units with tiles so far (phase of stats_full / stats_free)
         bool ok = true;
         // Waits end with a warp-uniform verdict, so that a wait given up on never leaves
         // part of a warp ahead of a warp-collective tcgen05 access.
@@ -360,7 +376,6 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             if (w >= p.nunits) break;
             int bh, kvz;
             const TileRange t = unit_at(w, bh, kvz);
-            const int q_row = t.q0 + row;
             const int qpos = t.qpos_lo + row;
             const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
             const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
@@ -484,12 +499,40 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 tc_fence_before();
                 mbar_arrive(&p_full[b]);
             }
-            // ------------------------------------------------------------ epilogue
-            bool have_o = false;
             if (t.n > 0) {
-                have_o = ok && wait_warp(&o_done, ocnt & 1);
-                ++ocnt;
+                // hand the unit's (max, sum) to the epilogue warps once they have taken the
+                // previous unit's
+                if (su > 0) ok = wait_warp(&stats_free, (su - 1) & 1) && ok;
+                stats[row] = make_float2(m_used, l_sum);
+                mbar_arrive(&stats_full);
+                ++su;
+            }
+        }
+    } else {
+        // ----------------------------------------------------------------- epilogue
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t tm_o = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kColO;
+        int ue = 0;  // units with tiles so far (phase of o_done and stats_full)
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_or_abort(bar, parity, &abort_flag));
+        };
+        for (int r = 0;; ++r) {
+            const int w = zigzag_unit(cta, r, G);
+            if (w >= p.nunits) break;
+            int bh, kvz;
+            const TileRange t = unit_at(w, bh, kvz);
+            const int q_row = t.q0 + row;
+            bool have_o = false;
+            float m_used = -INFINITY, l_sum = 0.f;
+            if (t.n > 0) {
+                have_o = wait_warp(&o_done, ue & 1);
                 tc_fence_after();
+                have_o = wait_warp(&stats_full, ue & 1) && have_o;
+                const float2 st = stats[row];
+                m_used = st.x;
+                l_sum = st.y;
+                mbar_arrive(&stats_free);
+                ++ue;
             }
             const bool row_valid = t.rows > 0 && row < t.rows;
             const bool live = have_o && l_sum > 0.f;
@@ -505,6 +548,10 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                }
+                if (c0 + 32 == D && t.n > 0) {
+                    tc_fence_before();
+                    mbar_arrive(&o_free);  // O has been read: the next unit may overwrite it
                 }
                 if (row_valid) {
                     if (p.o_f32) {
@@ -525,8 +572,6 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     }
                 }
             }
-            tc_fence_before();
-            if (t.n > 0) mbar_arrive(&o_free);  // O has been read: the next unit may overwrite it
         }
     }
     tc_fence_before();
@@ -1064,6 +1109,14 @@ attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, con
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
+        // setmaxnreg.inc waits until the launch's register pool can serve it; the split is
+        // sized for exactly kRegsLaunch4 registers per thread at launch.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, prefill_wide_kernel<D>) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        if (fa.numRegs != kRegsLaunch4) return ATTN_ERR_UNSUPPORTED;
         attr_set = true;
     }
     const long long units = (long long)p.nqt * a.b * a.hq;
