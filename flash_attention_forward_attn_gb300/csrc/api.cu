@@ -49,14 +49,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
-int resolve_chunk(int kv_chunk) { return kv_chunk == 0 ? attn::kDefaultKvChunk : kv_chunk; }
+int resolve_chunk(int kv_chunk, int b, int max_cache_len) {
+    return kv_chunk == 0 ? attn::default_kv_chunk(b, max_cache_len) : kv_chunk;
+}
 
 // Split-KV scratch: partial outputs [rows][max_splits][d] fp32, then (m, l) pairs.
 bool decode_scratch_sizes(int b, int hq, int s_active, int d, int max_cache_len, int kv_chunk,
                           size_t* o_bytes, size_t* ml_bytes, int* max_splits) {
     if (b <= 0 || hq <= 0 || s_active <= 0 || !head_dim_ok(d) || max_cache_len <= 0) return false;
     if (kv_chunk < 0 || (kv_chunk % 32) != 0) return false;
-    const int chunk = resolve_chunk(kv_chunk);
+    const int chunk = resolve_chunk(kv_chunk, b, max_cache_len);
     const long long splits = (max_cache_len + (long long)chunk - 1) / chunk;
     const long long rows = (long long)b * hq * s_active;
     *max_splits = (int)splits;
@@ -160,7 +162,7 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
     a.o = o;
     a.lse = lse;
     a.o_dtype = o_dtype;
-    a.kv_chunk = resolve_chunk(kv_chunk);
+    a.kv_chunk = resolve_chunk(kv_chunk, b, max_cache_len);
     a.part_o = static_cast<float*>(workspace);
     a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ob);
     a.max_splits = max_splits;

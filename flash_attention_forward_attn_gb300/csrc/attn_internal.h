@@ -47,8 +47,18 @@ struct DecodeArgs {
     int max_splits;
 };
 
-// Tokens per split when the caller passes kv_chunk = 0.
-constexpr int kDefaultKvChunk = 1024;
+// Tokens per split when the caller passes kv_chunk = 0: the largest power of two in
+// [kMinDefaultKvChunk, kMaxDefaultKvChunk] that is at most b * max_cache_len / 128, i.e.
+// about 128 splits across the batch for every kv head.  Long splits keep the per-split
+// merge and the partial-output traffic small; short batches still get enough CTAs.
+constexpr int kMinDefaultKvChunk = 256;
+constexpr int kMaxDefaultKvChunk = 4096;
+inline int default_kv_chunk(int b, int max_cache_len) {
+    const long long per = (long long)b * max_cache_len / 128;
+    int chunk = kMaxDefaultKvChunk;
+    while (chunk > kMinDefaultKvChunk && chunk > per) chunk >>= 1;
+    return chunk;
+}
 
 // cuTensorMapEncodeTiled, fetched once through the runtime (no link against libcuda).
 typedef CUresult (*TensorMapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -114,8 +114,10 @@ size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_c
  * Sizes: hq % hkv == 0; (hq / hkv) * s_active <= 16; d in {64, 128, 256};
  *   1 <= s_active; cache_len[b] in [s_active, max_cache_len];
  *   paged: page_size a power of two in [16, 256], max_cache_len <=
- *   max_pages_per_seq * page_size, num_pages >= 1; kv_chunk = 0 (default) or a positive
- *   multiple of 32 (and of page_size when page_size > 32).
+ *   max_pages_per_seq * page_size, num_pages >= 1; kv_chunk = 0 or a positive multiple of
+ *   32 (and of page_size when page_size > 32).  kv_chunk = 0 picks the largest power of two
+ *   in [256, 4096] not above b * max_cache_len / 128 (about 128 splits across the batch
+ *   per kv head); attn_decode_workspace_bytes applies the same rule.
  * Workspace: device scratch of at least attn_decode_workspace_bytes(...), 16-byte aligned,
  *   owned by the caller, not read before it is written; calls that share it must not
  *   overlap on the device.

@@ -91,11 +91,27 @@ def test_decode_rejects_before_launch(lib, kw, status):
     assert decode(lib, **kw) == status
 
 
-def test_workspace_bytes_formula(lib):
+def _ws(b, hq, s_active, d, max_len, chunk):
     # rows = b*hq*s_active; splits = ceil(max_len / chunk); O partials (256-byte padded) + (m, l)
-    rows, splits, d = 64 * 32 * 4, 32, 128
-    o = rows * splits * d * 4
-    assert A.attn_decode_workspace_bytes(64, 32, 4, 128, 32768) == o + rows * splits * 8
+    rows, splits = b * hq * s_active, -(-max_len // chunk)
+    return ((rows * splits * d * 4 + 255) // 256) * 256 + rows * splits * 8
+
+
+@pytest.mark.parametrize("b,max_len,chunk", [
+    (64, 32768, 4096),   # long batch: the largest default split
+    (16, 32768, 4096),   # b * max_len / 128 = 4096
+    (8, 16384, 1024),    # 1024
+    (1, 32768, 256),     # 256: one long sequence still gets 128 splits
+    (4, 4096, 256),      # 128 -> clamped to the smallest default split
+])
+def test_workspace_default_chunk(lib, b, max_len, chunk):
+    """kv_chunk = 0: the largest power of two in [256, 4096] not above b * max_len / 128."""
+    assert A.attn_decode_workspace_bytes(b, 32, 4, 128, max_len) == _ws(b, 32, 4, 128, max_len, chunk)
+    assert A.attn_decode_workspace_bytes(b, 32, 4, 128, max_len, chunk) == _ws(b, 32, 4, 128, max_len, chunk)
+
+
+def test_workspace_bytes_formula(lib):
+    assert A.attn_decode_workspace_bytes(64, 32, 4, 128, 32768, 1024) == _ws(64, 32, 4, 128, 32768, 1024)
     assert A.attn_decode_workspace_bytes(1, 1, 1, 64, 100, 64) == ((2 * 64 * 4 + 255) // 256) * 256 + 16
     assert A.attn_decode_workspace_bytes(1, 1, 1, 96, 100) == 0
     assert A.attn_decode_workspace_bytes(1, 1, 1, 64, 100, 33) == 0

@@ -43,13 +43,14 @@ def test_static_scratch_decode_matches_workspace_decode_twice(cuda_device):
 def test_static_scratch_rejects_calls_larger_than_the_array(cuda_device):
     import flash_attention_forward_attn_gb300 as A
 
-    # 64 sequences x 32 heads x 4 tokens x 32 splits x 128 dims of fp32 partials > 64 MiB
+    # 64 sequences x 32 heads x 4 tokens x 32 splits (1024-token chunks) x 128 dims of fp32
+    # partials > 64 MiB
     w = C.PAGED_DECODE_SPEC4
-    need = A.attn_decode_workspace_bytes(w.b, w.hq, w.s_active, w.d, 32768)
+    need = A.attn_decode_workspace_bytes(w.b, w.hq, w.s_active, w.d, 32768, 1024)
     assert need > 64 << 20
     q = torch.zeros((w.b, w.hq, w.s_active, w.d), dtype=torch.bfloat16, device=cuda_device)
     kc = torch.zeros((4, w.hkv, 32, w.d), dtype=torch.bfloat16, device=cuda_device)
     bt = torch.zeros((w.b, 1024), dtype=torch.int32, device=cuda_device)
     cl = torch.full((w.b,), 32, dtype=torch.int32, device=cuda_device)
     with pytest.raises(A.AttnError, match="ATTN_ERR_WORKSPACE"):
-        A.attn_fwd_decode_static_ws(q, kc, kc, bt, cl, max_cache_len=32768)
+        A.attn_fwd_decode_static_ws(q, kc, kc, bt, cl, max_cache_len=32768, kv_chunk=1024)
