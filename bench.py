@@ -159,8 +159,11 @@ def source_sha(*rel_paths) -> str:
 KERNEL_SOURCES = {
     "prefill": ("flash_attention_forward_attn_gb300/csrc/prefill_sm103.cu",
                 "flash_attention_forward_attn_gb300/csrc/attn_ptx.cuh"),
+    # the decode launch shape (split length) is chosen in the API layer
     "decode": ("flash_attention_forward_attn_gb300/csrc/decode_sm103.cu",
-               "flash_attention_forward_attn_gb300/csrc/attn_ptx.cuh"),
+               "flash_attention_forward_attn_gb300/csrc/attn_ptx.cuh",
+               "flash_attention_forward_attn_gb300/csrc/api.cu",
+               "flash_attention_forward_attn_gb300/csrc/attn_internal.h"),
 }
 
 
