@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
+    __shared__ uint64_t q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[2], p_full[2], o_done[2], o_free[2], mma_drain, stage_free;
     __shared__ uint64_t turn[2];  // MMA issue turns of tiles A and B
     __shared__ uint32_t tmem_base_sh;
@@ -668,8 +668,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(&q_full, 1);
-        mbar_init(&q_empty, 2);  // both MMA issuers
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);   // Q_A / Q_B landed
+            mbar_init(&q_empty[i], 1);  // tile A's / B's last S of the unit done
+        }
         for (int i = 0; i < NK; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 2);
@@ -716,22 +718,29 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
             tma_prefetch_desc(tm);
             if (!is_k) tma_prefetch_desc(&tm_q);
-            int L = 0;   // tiles issued so far into this ring
-            int rq = 0;  // Q loads issued
+            int L = 0;           // tiles issued so far into this ring
+            int nq[2] = {0, 0};  // Q_A / Q_B loads issued
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int w = zigzag_unit(cta, r, G);
                 if (w >= p.nunits) break;
                 const Unit u = unit_at(w);
                 if (!is_k) {
-                    if (r > 0 && !wait_or_abort(&q_empty, (r - 1) & 1, &abort_flag)) break;
-                    ++rq;
-                    mbar_arrive_expect_tx(&q_full, (u.has_b ? 2 : 1) * C::kQBytes);
-                    for (int x = 0; x < (u.has_b ? 2 : 1); ++x)
+                    // Q_X is reloaded as soon as tile X's last S of the previous unit is done
+                    // (tile A's KV range ends a tile before B's, so Q_A comes back first)
+                    for (int x = 0; ok && x < (u.has_b ? 2 : 1); ++x) {
+                        if (nq[x] > 0 && !wait_or_abort(&q_empty[x], (nq[x] - 1) & 1, &abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        ++nq[x];
+                        mbar_arrive_expect_tx(&q_full[x], C::kQBytes);
 #pragma unroll
                         for (int dc = 0; dc < D / 64; ++dc)
                             tma_load_3d(sm + (x ? C::kQBOff : C::kQAOff) + dc * (kBM * 128), &tm_q,
-                                        dc * 64, u.t[x].q0, u.bh, &q_full);
+                                        dc * 64, u.t[x].q0, u.bh, &q_full[x]);
+                    }
+                    if (!ok) break;
                 }
                 for (int j = u.u0; j < u.u1; ++j, ++L) {
                     const int slot = L % ns;
@@ -748,7 +757,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             }
             if (abort_flag) {  // let copies in flight land before the CTA exits
                 for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
-                if (rq > 0) wait_bounded(&q_full, (rq - 1) & 1);
+                for (int x = 0; x < 2; ++x)
+                    if (nq[x] > 0) wait_bounded(&q_full[x], (nq[x] - 1) & 1);
             }
         } else if ((warp == 1 || warp == 3) && lane == 0) {
             // ------------------------------------------------ MMA issuers, one per Q tile
@@ -772,17 +782,22 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             int Lbase = 0;  // ring index (K and V alike) of the unit's first tile
             int cnt = 0;    // S products of this tile issued so far (phase of s/p_full)
             int turns = 0;  // turns taken so far (phase of turn[x])
+            int nq = 0;     // units with a tile X so far (phase of q_full[x])
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int w = zigzag_unit(cta, r, G);
                 if (w >= p.nunits) break;
                 const Unit u = unit_at(w);
                 const TileRange t = x ? u.t[1] : u.t[0];
-                if (!wait_or_abort(&q_full, r & 1, &abort_flag)) break;
+                const bool has_x = x == 0 || u.has_b;  // tile X exists in this unit
+                if (has_x) {
+                    if (!wait_or_abort(&q_full[x], nq & 1, &abort_flag)) break;
+                    ++nq;
+                    if (t.n == 0) tc_commit(&q_empty[x]);  // no product will read Q_X
+                }
                 bool freed = r == 0;  // previous unit's O_X read out?
                 const int cbase = cnt;
                 const int nu = u.u1 - u.u0;
-                if (nu == 0) tc_commit(&q_empty);
                 for (int j = u.u0; ok && j <= u.u1 && nu > 0; ++j) {
                     const int Lk = Lbase + (j - u.u0), Lv = Lk - 1;  // K(j), V(j-1)
                     const bool have_k = j < u.u1, have_v = j > u.u0;
@@ -834,7 +849,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                         if (in_k) tc_commit(&k_empty[ks]);
                         else mbar_arrive(&k_empty[ks]);
                     }
-                    if (j == u.u1 - 1) tc_commit(&q_empty);  // every S of this tile issued
+                    if (in_k && j == t.kt0 + t.n - 1) tc_commit(&q_empty[x]);  // last S of tile X
                 }
                 // a tile with no product this unit still consumes the epilogue's o_free phase
                 if (ok && !freed && !wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag)) ok = false;
