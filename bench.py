@@ -242,42 +242,68 @@ def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False)
 
 
 def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
-    """Same metric through the public API with host buffers: pinned H2D of Q, K, V, the
-    call, and D2H of O and LSE, all inside the timed region."""
+    """Same metric through the public API with host buffers: every step copies Q, K, V from
+    pinned host memory, calls attn_fwd_prefill, and copies O and LSE back, all inside the
+    timed region.  Steps are pipelined the way a serving loop would run them: two sets of
+    device buffers, each input copied on its own stream (several copy engines), the call on
+    `stream`, the results copied back on another stream, so step i+1's uploads overlap step
+    i's call and download.  Events order each step's copies, call and download."""
     import torch
 
     import flash_attention_forward_attn_gb300 as A
 
     hq_, hk_, hv_ = (x.cpu().pin_memory() for x in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+    hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
+    dev_in = [(q, k, v)] + [tuple(torch.empty_like(x) for x in (q, k, v))]
+    dev_out = [(o, lse), (torch.empty_like(o), torch.empty_like(lse))]
+    up = [torch.cuda.Stream(device=dev) for _ in range(3)]
+    down = torch.cuda.Stream(device=dev)
+    ev_in = [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]
+    ev_call = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]  # a buffer set's download is done
+    used = [False, False]
 
-    def step():
-        with torch.cuda.stream(stream):
-            q.copy_(hq_, non_blocking=True)
-            k.copy_(hk_, non_blocking=True)
-            v.copy_(hv_, non_blocking=True)
-            A.attn_fwd_prefill(q, k, v, causal=w.causal, window=w.window, scale=w.scale, o=o,
-                               lse=lse, stream=stream)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+    def step(i):
+        bset = i & 1
+        din, (do_, dl) = dev_in[bset], dev_out[bset]
+        for j, (dst, src) in enumerate(zip(din, (hq_, hk_, hv_))):
+            if used[bset]:
+                up[j].wait_event(ev_free[bset])  # the set's previous step is fully done
+            with torch.cuda.stream(up[j]):
+                dst.copy_(src, non_blocking=True)
+            ev_in[bset][j].record(up[j])
+        for j in range(3):
+            stream.wait_event(ev_in[bset][j])
+        A.attn_fwd_prefill(din[0], din[1], din[2], causal=w.causal, window=w.window,
+                           scale=w.scale, o=do_, lse=dl, stream=stream)
+        ev_call[bset].record(stream)
+        down.wait_event(ev_call[bset])
+        with torch.cuda.stream(down):
+            ho[bset].copy_(do_, non_blocking=True)
+            hl[bset].copy_(dl, non_blocking=True)
+        ev_free[bset].record(down)
+        used[bset] = True
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
-        step()
-    e.record(stream)
+    s.record(up[0])
+    for j in (1, 2):
+        up[j].wait_event(s)
+    for i in range(steps):
+        step(warmup + i)
+    e.record(down)
     torch.cuda.synchronize()
     barrier(world)
     value, _ = aggregate_throughput(w.flops() * steps, s.elapsed_time(e) / 1e3, world, dev)
     return {"value": value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": s.elapsed_time(e) / steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": s.elapsed_time(e) / steps,
+            "pipelining": "2 buffer sets; per-input upload streams; download stream"}
 
 
 def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world):
