@@ -783,6 +783,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             int cnt = 0;    // S products of this tile issued so far (phase of s/p_full)
             int turns = 0;  // turns taken so far (phase of turn[x])
             int nq = 0;     // units with a tile X so far (phase of q_full[x])
+            int uo = 0;     // units in which tile X had products so far (phase of o_free[x])
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int w = zigzag_unit(cta, r, G);
@@ -795,7 +796,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     ++nq;
                     if (t.n == 0) tc_commit(&q_empty[x]);  // no product will read Q_X
                 }
-                bool freed = r == 0;  // previous unit's O_X read out?
+                // O_X may be overwritten once the epilogue has read out the previous unit
+                // in which tile X had products (o_free completes once per such unit, so it
+                // can never run two phases ahead of this wait)
+                bool freed = uo == 0;
                 const int cbase = cnt;
                 const int nu = u.u1 - u.u0;
                 for (int j = u.u0; ok && j <= u.u1 && nu > 0; ++j) {
@@ -806,7 +810,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     const int ks = Lk % NK, vs = (Lv + NV) % NV;
                     // everything this turn's products need, before taking the turn
                     if (have_v) ok = wait_or_abort(&v_full[vs], (Lv / NV) & 1, &abort_flag);
-                    if (ok && in_v && !freed) ok = freed = wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag);
+                    if (ok && in_v && !freed) ok = freed = wait_or_abort(&o_free[x], (uo - 1) & 1, &abort_flag);
                     const int i = (j - 1) - t.kt0;  // index of V(j-1) within this tile's range
                     if (ok && in_v) ok = wait_or_abort(pfull, (cbase + i) & 1, &abort_flag);
                     if (ok && have_k) ok = wait_or_abort(&k_full[ks], (Lk / NK) & 1, &abort_flag);
@@ -851,8 +855,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     }
                     if (in_k && j == t.kt0 + t.n - 1) tc_commit(&q_empty[x]);  // last S of tile X
                 }
-                // a tile with no product this unit still consumes the epilogue's o_free phase
-                if (ok && !freed && !wait_or_abort(&o_free[x], (r - 1) & 1, &abort_flag)) ok = false;
+                if (t.n > 0) ++uo;
                 Lbase += nu;
             }
             tc_commit(&mma_drain);
@@ -1040,7 +1043,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                                                    __uint_as_float(rr[2 * e + 1]) * inv);
                 }
                 tc_fence_before();
-                mbar_arrive(ofree);  // O_X has been read: the next unit may overwrite it
+                if (t.n > 0) mbar_arrive(ofree);  // O_X read out: the next unit may overwrite it
                 if (t.rows > 0) {
                     if (eidx > 0) ok = wait_or_abort(&stage_free, (eidx - 1) & 1, &abort_flag) && ok;
                     uint8_t* st = sm + C::kOStOff;
@@ -1082,7 +1085,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                                              __uint_as_float(rr[4 * e + 2]) * inv, __uint_as_float(rr[4 * e + 3]) * inv);
                 }
                 tc_fence_before();
-                mbar_arrive(ofree);  // O_X has been read: the next unit may overwrite it
+                if (t.n > 0) mbar_arrive(ofree);  // O_X read out: the next unit may overwrite it
             }
         }
         if (store_thread) bulk_wait0();  // every staged tile has reached global memory

@@ -40,10 +40,23 @@ SMALL = [
     ("one_query_d128", 2, 4, 4, 1, 77, 128, True, 0, torch.bfloat16),
     ("causal_window_d64_gqa8", 1, 8, 1, 257, 257, 64, True, 64, torch.bfloat16),
     ("noncausal_d256_tail", 1, 1, 1, 129, 65, 256, False, 0, torch.float32),
+    ("causal_more_q_than_k_d256", 1, 2, 1, 300, 100, 256, True, 0, torch.float32),
+]
+
+# More work units than SMs, so each persistent CTA runs several units: Q reloads between
+# units, the epilogue hand-over, odd query-tile counts (a last unit without tile B) and units
+# whose query rows precede every key (no KV tile at all).
+MULTI_UNIT = [
+    # name, b, hq, hkv, sq, skv, d, causal, window, out
+    ("multi_unit_causal_d128", 1, 40, 8, 1024, 1024, 128, True, 0, torch.bfloat16),
+    ("multi_unit_odd_tiles_d128", 1, 60, 10, 640, 640, 128, True, 0, torch.float32),
+    ("multi_unit_empty_units_d64", 1, 64, 16, 700, 300, 64, True, 0, torch.bfloat16),
+    ("multi_unit_window_d256", 1, 40, 8, 640, 640, 256, True, 200, torch.bfloat16),
+    ("multi_unit_empty_units_d256", 1, 48, 8, 520, 200, 256, True, 0, torch.float32),
 ]
 
 
-@pytest.mark.parametrize("case", SMALL, ids=lambda c: c[0])
+@pytest.mark.parametrize("case", SMALL + MULTI_UNIT, ids=lambda c: c[0])
 def test_prefill_small_all_rows(case, cuda_device):
     name, b, hq, hkv, sq, skv, d, causal, window, out = case
     w = C.PrefillWorkload(name, b, hq, hkv, sq, skv, d, causal, window, seed=0xC0FFEE + len(name))
