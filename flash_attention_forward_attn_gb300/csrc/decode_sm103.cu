@@ -30,6 +30,9 @@ constexpr int kBT = 32;          // tokens per pipeline slot
 constexpr int kConsumers = 4;    // consumer warps
 constexpr int kStages = 4;       // ring slots (one per consumer warp)
 constexpr int kThreads = (kConsumers + 1) * 32;
+// Consumer warp w takes tiles w, w + kConsumers, ... and waits on slot i % kStages at the
+// phase of tile i; that phase accounting holds only when every slot belongs to one warp.
+static_assert(kStages == kConsumers, "each consumer warp owns one ring slot");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
