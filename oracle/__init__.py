@@ -60,12 +60,19 @@ def _load():
             lib.oracle_allowed.restype = I
             lib.oracle_attention_rows.argtypes = [P, L, P, P, L, I, D, P, I, L, P, P, P]
             lib.oracle_attention_rows.restype = I
+            lib.oracle_attention_rows_sink.argtypes = [P, L, P, P, L, I, D, P, I, L, D, P, P, P]
+            lib.oracle_attention_rows_sink.restype = I
             lib.oracle_prefill.argtypes = [P, P, P, I, I, I, L, L, I, D, I, L, L, L, P, P]
             lib.oracle_prefill.restype = I
+            lib.oracle_prefill_sink.argtypes = [P, P, P, I, I, I, L, L, I, D, I, L, P, L, L, P, P]
+            lib.oracle_prefill_sink.restype = I
             lib.oracle_gather_paged.argtypes = [P, P, L, I, I, I, I, L, P]
             lib.oracle_gather_paged.restype = I
             lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, D, L, L, P, P]
             lib.oracle_decode.restype = I
+            lib.oracle_decode_sink.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, D, P, L, L,
+                                               P, P]
+            lib.oracle_decode_sink.restype = I
             lib.oracle_decode_mask.argtypes = [P, I, I, I, L, P]
             lib.oracle_decode_mask.restype = I
             _lib = lib
@@ -109,8 +116,18 @@ def bf16_to_f64(bits) -> np.ndarray:
     return np.array([lib.oracle_bf16_to_f64(int(x)) for x in flat]).reshape(np.shape(bits))
 
 
-def attention_rows(q_rows, k, v, qpos, scale, causal, window, want_p=False):
-    """Rows of one head.  q_rows [n, d], k/v [skv, d] (bf16 bits), qpos [n].
+def _sinks(sink, hq):
+    """Per-query-head sink logits as a float64 array [hq], or None for no sink."""
+    if sink is None:
+        return None
+    a = np.ascontiguousarray(sink, dtype=np.float64).reshape(-1)
+    assert a.shape == (hq,), "sink holds one logit per query head"
+    return a
+
+
+def attention_rows(q_rows, k, v, qpos, scale, causal, window, want_p=False, sink=None):
+    """Rows of one head.  q_rows [n, d], k/v [skv, d] (bf16 bits), qpos [n]; sink: the
+    head's sink logit (None = no sink).
 
     Returns (o [n, d] float64, lse [n] float64[, p [n, skv] float64])."""
     q_rows, k, v = _u16(q_rows), _u16(k), _u16(v)
@@ -121,25 +138,29 @@ def attention_rows(q_rows, k, v, qpos, scale, causal, window, want_p=False):
     o = np.empty((n, d), dtype=np.float64)
     lse = np.empty(n, dtype=np.float64)
     p = np.empty((n, skv), dtype=np.float64) if want_p else None
-    _check(_load().oracle_attention_rows(_ptr(q_rows), n, _ptr(k), _ptr(v), skv, d, float(scale),
-                                         _ptr(qp), int(causal), int(window), _ptr(o), _ptr(lse),
-                                         _ptr(p)))
+    sk = -np.inf if sink is None else float(sink)
+    _check(_load().oracle_attention_rows_sink(_ptr(q_rows), n, _ptr(k), _ptr(v), skv, d,
+                                              float(scale), _ptr(qp), int(causal), int(window),
+                                              sk, _ptr(o), _ptr(lse), _ptr(p)))
     return (o, lse, p) if want_p else (o, lse)
 
 
-def prefill(q, k, v, scale, causal, window, threads=None):
-    """Full prefill.  q [B,HQ,SQ,D], k/v [B,HKV,SKV,D] bf16 bits -> (o f64, lse f64)."""
+def prefill(q, k, v, scale, causal, window, threads=None, sink=None):
+    """Full prefill.  q [B,HQ,SQ,D], k/v [B,HKV,SKV,D] bf16 bits -> (o f64, lse f64).
+    sink: [HQ] per-query-head sink logits, or None."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     B, HQ, SQ, D = q.shape
     _, HKV, SKV, _ = k.shape
+    sk = _sinks(sink, HQ)
     o = np.empty((B, HQ, SQ, D), dtype=np.float64)
     lse = np.empty((B, HQ, SQ), dtype=np.float64)
     lib = _load()
     nbh = B * HQ
 
     def run(bh):
-        return lib.oracle_prefill(_ptr(q), _ptr(k), _ptr(v), B, HQ, HKV, SQ, SKV, D, float(scale),
-                                  int(causal), int(window), bh, bh + 1, _ptr(o), _ptr(lse))
+        return lib.oracle_prefill_sink(_ptr(q), _ptr(k), _ptr(v), B, HQ, HKV, SQ, SKV, D,
+                                       float(scale), int(causal), int(window), _ptr(sk), bh,
+                                       bh + 1, _ptr(o), _ptr(lse))
 
     with ThreadPoolExecutor(max_workers=min(threads or default_threads(), nbh)) as ex:
         for rc in ex.map(run, range(nbh)):
@@ -158,11 +179,13 @@ def gather_paged(cache, table_row, num_pages, g, length):
     return out
 
 
-def decode(q, k_cache, v_cache, table, cache_len, scale, threads=None):
+def decode(q, k_cache, v_cache, table, cache_len, scale, threads=None, sink=None):
     """Decode.  q [B,HQ,s_active,D]; paged caches [num_pages,HKV,page,D] with table
-    [B,max_pages] uint32, or flat caches [B,HKV,max_len,D] with table None."""
+    [B,max_pages] uint32, or flat caches [B,HKV,max_len,D] with table None.
+    sink: [HQ] per-query-head sink logits, or None."""
     q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
     B, HQ, SA, D = q.shape
+    sk = _sinks(sink, HQ)
     cl = np.ascontiguousarray(cache_len, dtype=np.int32)
     if table is not None:
         table = np.ascontiguousarray(table, dtype=np.uint32)
@@ -176,9 +199,10 @@ def decode(q, k_cache, v_cache, table, cache_len, scale, threads=None):
     lib = _load()
 
     def run(bh):
-        return lib.oracle_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(table), _ptr(cl), B,
-                                 HQ, HKV, D, SA, page, max_pages, num_pages, max_len, float(scale),
-                                 bh, bh + 1, _ptr(o), _ptr(lse))
+        return lib.oracle_decode_sink(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(table),
+                                      _ptr(cl), B, HQ, HKV, D, SA, page, max_pages, num_pages,
+                                      max_len, float(scale), _ptr(sk), bh, bh + 1, _ptr(o),
+                                      _ptr(lse))
 
     with ThreadPoolExecutor(max_workers=min(threads or default_threads(), B * HQ)) as ex:
         for rc in ex.map(run, range(B * HQ)):

@@ -83,27 +83,39 @@ void oracle_scores(const double *q, const double *k, long skv, int d, double sca
     }
 }
 
-/* Softmax over the allowed entries of one score row.
- *   M = max over allowed s_j;  P_j = exp(s_j - M) / sum_allowed exp(s_k - M);  P_j = 0
- *   where not allowed;  LSE = M + ln sum_allowed exp(s_j - M).
- * A row with nothing allowed has P = 0 and LSE = -inf (minfer 8n, "rows with l == 0
- * stay 0").  Returns LSE. */
-double oracle_softmax(const double *s, const unsigned char *allowed, long n, double *p)
+/* Softmax over the allowed entries of one score row, with an optional attention sink.
+ * The sink is one extra logit of the row that joins the maximum and the sum but has no
+ * value row (Flash-Attention: Context (CTE), "Algorithm - the per-section max update":
+ * the sink logit is appended as one more column of the max; "Algorithm - fused exp and
+ * the running sum": exp(sink - max) is appended to the row sum).  sink = -inf means no
+ * sink.
+ *   M = max(max over allowed s_j, sink);  l = sum_allowed exp(s_j - M) + exp(sink - M);
+ *   P_j = exp(s_j - M) / l, P_j = 0 where not allowed;  LSE = M + ln l.
+ * A row with nothing allowed and no sink has P = 0 and LSE = -inf (minfer 8n, "rows
+ * with l == 0 stay 0"); with a sink it has P = 0 and LSE = sink.  Returns LSE. */
+double oracle_softmax_sink(const double *s, const unsigned char *allowed, long n, double sink,
+                           double *p)
 {
-    double m = -INFINITY;
+    double m = sink;
     for (long j = 0; j < n; ++j)
         if (allowed[j] && s[j] > m) m = s[j];
     if (m == -INFINITY) {
         for (long j = 0; j < n; ++j) p[j] = 0.0;
         return -INFINITY;
     }
-    double l = 0.0;
+    double l = exp(sink - m); /* exactly 0 without a sink */
     for (long j = 0; j < n; ++j) {
         p[j] = allowed[j] ? exp(s[j] - m) : 0.0;
         l += p[j];
     }
     for (long j = 0; j < n; ++j) p[j] = p[j] / l;
     return m + log(l);
+}
+
+/* The softmax without a sink (see oracle_softmax_sink). */
+double oracle_softmax(const double *s, const unsigned char *allowed, long n, double *p)
+{
+    return oracle_softmax_sink(s, allowed, n, -INFINITY, p);
 }
 
 /* O = sum_j P_j * V_j.  v: [n][d] double. */
@@ -118,8 +130,8 @@ void oracle_pv(const double *p, const double *v, long n, int d, double *o)
 
 /* One query row end to end, on already widened K and V of its kv head. */
 static int row_f64(const double *q, const double *k, const double *v, long skv, int d,
-                   double scale, long q_pos, int causal, long window, double *o, double *lse,
-                   double *p_out)
+                   double scale, long q_pos, int causal, long window, double sink, double *o,
+                   double *lse, double *p_out)
 {
     double *s = (double *)malloc(sizeof(double) * (size_t)(skv > 0 ? skv : 1));
     double *p = p_out ? p_out : (double *)malloc(sizeof(double) * (size_t)(skv > 0 ? skv : 1));
@@ -130,18 +142,20 @@ static int row_f64(const double *q, const double *k, const double *v, long skv, 
     }
     oracle_scores(q, k, skv, d, scale, s);
     for (long j = 0; j < skv; ++j) al[j] = (unsigned char)oracle_allowed(j, skv, q_pos, causal, window);
-    *lse = oracle_softmax(s, al, skv, p);
+    *lse = oracle_softmax_sink(s, al, skv, sink, p);
     oracle_pv(p, v, skv, d, o);
     free(s); free(al);
     if (!p_out) free(p);
     return ORACLE_OK;
 }
 
-/* Rows of one head, given as bf16 bits: q_rows [n][d], k and v [skv][d], q_pos [n].
- * Writes o [n][d] and lse [n]; p_out (nullable) receives [n][skv] probabilities. */
-int oracle_attention_rows(const uint16_t *q_rows, long n, const uint16_t *k, const uint16_t *v,
-                          long skv, int d, double scale, const long *q_pos, int causal,
-                          long window, double *o, double *lse, double *p_out)
+/* Rows of one head, given as bf16 bits: q_rows [n][d], k and v [skv][d], q_pos [n],
+ * with the head's sink logit (-inf for none).  Writes o [n][d] and lse [n]; p_out
+ * (nullable) receives [n][skv] probabilities. */
+int oracle_attention_rows_sink(const uint16_t *q_rows, long n, const uint16_t *k,
+                               const uint16_t *v, long skv, int d, double scale,
+                               const long *q_pos, int causal, long window, double sink,
+                               double *o, double *lse, double *p_out)
 {
     if (n < 0 || skv < 0 || d <= 0) return ORACLE_ERR_ARG;
     double *kd = (double *)malloc(sizeof(double) * (size_t)(skv * d + 1));
@@ -153,18 +167,29 @@ int oracle_attention_rows(const uint16_t *q_rows, long n, const uint16_t *k, con
     int rc = ORACLE_OK;
     for (long r = 0; r < n && rc == ORACLE_OK; ++r) {
         widen(q_rows + r * d, d, qd);
-        rc = row_f64(qd, kd, vd, skv, d, scale, q_pos[r], causal, window, o + r * d, lse + r,
-                     p_out ? p_out + r * skv : NULL);
+        rc = row_f64(qd, kd, vd, skv, d, scale, q_pos[r], causal, window, sink, o + r * d,
+                     lse + r, p_out ? p_out + r * skv : NULL);
     }
     free(kd); free(vd); free(qd);
     return rc;
 }
 
+/* oracle_attention_rows_sink without a sink. */
+int oracle_attention_rows(const uint16_t *q_rows, long n, const uint16_t *k, const uint16_t *v,
+                          long skv, int d, double scale, const long *q_pos, int causal,
+                          long window, double *o, double *lse, double *p_out)
+{
+    return oracle_attention_rows_sink(q_rows, n, k, v, skv, d, scale, q_pos, causal, window,
+                                      -INFINITY, o, lse, p_out);
+}
+
 /* Prefill over flattened heads [bh_begin, bh_end) of q [B][HQ][SQ][D] against
- * k, v [B][HKV][SKV][D]; o [B][HQ][SQ][D], lse [B][HQ][SQ]. */
-int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int HQ, int HKV,
-                   long SQ, long SKV, int D, double scale, int causal, long window,
-                   long bh_begin, long bh_end, double *o, double *lse)
+ * k, v [B][HKV][SKV][D]; o [B][HQ][SQ][D], lse [B][HQ][SQ].  sink: [HQ] logits, one per
+ * query head (shared by every batch; CTE and TKG keep the sink per query head), or NULL
+ * for none. */
+int oracle_prefill_sink(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int HQ,
+                        int HKV, long SQ, long SKV, int D, double scale, int causal, long window,
+                        const double *sink, long bh_begin, long bh_end, double *o, double *lse)
 {
     if (HKV <= 0 || HQ % HKV != 0) return ORACLE_ERR_ARG;
     long *qp = (long *)malloc(sizeof(long) * (size_t)(SQ > 0 ? SQ : 1));
@@ -178,11 +203,21 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int 
         const uint16_t *qh = q + (size_t)bh * SQ * D;
         const uint16_t *kh = k + ((size_t)b * HKV + g) * SKV * D;
         const uint16_t *vh = v + ((size_t)b * HKV + g) * SKV * D;
-        rc = oracle_attention_rows(qh, SQ, kh, vh, SKV, D, scale, qp, causal, window,
-                                   o + (size_t)bh * SQ * D, lse + (size_t)bh * SQ, NULL);
+        rc = oracle_attention_rows_sink(qh, SQ, kh, vh, SKV, D, scale, qp, causal, window,
+                                        sink ? sink[h] : -INFINITY, o + (size_t)bh * SQ * D,
+                                        lse + (size_t)bh * SQ, NULL);
     }
     free(qp);
     return rc;
+}
+
+/* oracle_prefill_sink without a sink. */
+int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int HQ, int HKV,
+                   long SQ, long SKV, int D, double scale, int causal, long window,
+                   long bh_begin, long bh_end, double *o, double *lse)
+{
+    return oracle_prefill_sink(q, k, v, B, HQ, HKV, SQ, SKV, D, scale, causal, window, NULL,
+                               bh_begin, bh_end, o, lse);
 }
 
 /* Paged gather: logical token j of a sequence lives in physical page table_row[j / page],
@@ -207,11 +242,14 @@ int oracle_gather_paged(const uint16_t *cache, const uint32_t *table_row, long n
  * (TKG "The single-query decode attention").
  * q [B][HQ][s_active][D]; paged cache [num_pages][HKV][page][D] when table != NULL
  * (table [B][max_pages]), else flat cache [B][HKV][max_cache_len][D];
- * o [B][HQ][s_active][D], lse [B][HQ][s_active]. */
-int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                  const uint32_t *table, const int32_t *cache_len, int B, int HQ, int HKV, int D,
-                  int s_active, int page, long max_pages, long num_pages, long max_cache_len,
-                  double scale, long bh_begin, long bh_end, double *o, double *lse)
+ * o [B][HQ][s_active][D], lse [B][HQ][s_active].  sink: [HQ] logits or NULL, as for
+ * oracle_prefill_sink (TKG "GQA / MQA grouped-query broadcast": the sink is per query
+ * head, broadcast over the batch). */
+int oracle_decode_sink(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                       const uint32_t *table, const int32_t *cache_len, int B, int HQ, int HKV,
+                       int D, int s_active, int page, long max_pages, long num_pages,
+                       long max_cache_len, double scale, const double *sink, long bh_begin,
+                       long bh_end, double *o, double *lse)
 {
     if (HKV <= 0 || HQ % HKV != 0 || s_active <= 0) return ORACLE_ERR_ARG;
     int rc = ORACLE_OK;
@@ -240,12 +278,24 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
         }
         for (int t = 0; t < s_active; ++t) qp[t] = len - s_active + t;
         if (rc == ORACLE_OK)
-            rc = oracle_attention_rows(q + (size_t)bh * s_active * D, s_active, kf, vf, len, D,
-                                       scale, qp, 1, 0, o + (size_t)bh * s_active * D,
-                                       lse + (size_t)bh * s_active, NULL);
+            rc = oracle_attention_rows_sink(q + (size_t)bh * s_active * D, s_active, kf, vf, len,
+                                            D, scale, qp, 1, 0, sink ? sink[h] : -INFINITY,
+                                            o + (size_t)bh * s_active * D,
+                                            lse + (size_t)bh * s_active, NULL);
         free(kf); free(vf); free(qp);
     }
     return rc;
+}
+
+/* oracle_decode_sink without a sink. */
+int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                  const uint32_t *table, const int32_t *cache_len, int B, int HQ, int HKV, int D,
+                  int s_active, int page, long max_pages, long num_pages, long max_cache_len,
+                  double scale, long bh_begin, long bh_end, double *o, double *lse)
+{
+    return oracle_decode_sink(q, k_cache, v_cache, table, cache_len, B, HQ, HKV, D, s_active,
+                              page, max_pages, num_pages, max_cache_len, scale, NULL, bh_begin,
+                              bh_end, o, lse);
 }
 
 /* The decode 0/1 mask, [B][HQ][s_active][max_len] bytes (TKG "gen_mask_tkg"):

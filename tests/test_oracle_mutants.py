@@ -26,6 +26,9 @@ MUTANTS = {
     "tril_strict": ("(uint8_t)(u <= t)", "(uint8_t)(u < t)"),
     "decode_qpos_drops_t": ("qp[t] = len - s_active + t;", "qp[t] = len - s_active;"),
     "exp_sign_flipped": ("exp(s[j] - m)", "exp(m - s[j])"),
+    "sink_left_out_of_the_sum": ("double l = exp(sink - m);", "double l = 0.0;"),
+    "sink_left_out_of_the_max": ("double m = sink;", "double m = -INFINITY;"),
+    "sink_sign_flipped": ("double l = exp(sink - m);", "double l = exp(-sink - m);"),
 }
 
 

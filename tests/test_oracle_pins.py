@@ -315,3 +315,117 @@ def test_decode_mask_structure():
     # one new token: the mask is exactly the length cut (type A)
     m1 = oracle.decode_mask(lens, 1, 1, max_len)
     np.testing.assert_array_equal(m1[:, 0, 0], (np.arange(max_len)[None] < lens[:, None]))
+
+
+# ----------------------------------------------------------------------------- attention sink
+# The sink is one logit per query head that joins the row's maximum and sum and has no
+# value row (Flash-Attention: Context (CTE), "Algorithm - the per-section max update" and
+# "Algorithm - fused exp and the running sum"; TKG keeps it per query head).
+
+def test_sink_of_minus_inf_is_no_sink():
+    b, hq, hkv, sq, skv, d = 1, 4, 2, 12, 20, 8
+    q = rand_bits(50, (b, hq, sq, d), "q")
+    k, v = rand_bits(50, (b, hkv, skv, d), "k"), rand_bits(50, (b, hkv, skv, d), "v")
+    for causal, window in [(0, 0), (1, 0), (1, 5)]:
+        o1, l1 = oracle.prefill(q, k, v, 0.3, causal, window)
+        o2, l2 = oracle.prefill(q, k, v, 0.3, causal, window, sink=np.full(hq, -np.inf))
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+    fk, fv, _, _, _ = _flat_and_paged(51, 1, hkv, d, [17], 8, False)
+    qd = rand_bits(52, (1, hq, 2, d), "q")
+    cl = np.array([17], np.int32)
+    o1, l1 = oracle.decode(qd, fk, fv, None, cl, 0.3)
+    o2, l2 = oracle.decode(qd, fk, fv, None, cl, 0.3, sink=np.full(hq, -np.inf))
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("causal,window,sq,skv,counts", [
+    (1, 3, 6, 6, [1, 2, 3, 3, 3, 3]),
+    (1, 0, 3, 5, [3, 4, 5]),
+    (0, 0, 3, 5, [5, 5, 5]),
+])
+def test_zero_q_with_sink_closed_form(causal, window, sq, skv, counts):
+    """All allowed scores are 0, so with n allowed keys and sink s the row's weights are
+    1 / (n + e^s) per key: O = mean(allowed V) * n / (n + e^s), LSE = ln(n + e^s)."""
+    d = 4
+    sinks = np.array([0.5, -1.25, 30.0, 1000.0])
+    hq = len(sinks)
+    q = np.zeros((1, hq, sq, d), dtype=np.uint16)
+    k, v = rand_bits(53, (1, 1, skv, d), "k"), rand_bits(53, (1, 1, skv, d), "v")
+    o, lse = oracle.prefill(q, k, v, 1.0, causal, window, sink=sinks)
+    vf = f64(v[0, 0])
+    for h, s in enumerate(sinks):
+        for i, c in enumerate(counts):
+            last = i + skv - sq
+            hi = last if causal else skv - 1
+            mean = vf[hi - c + 1: hi + 1].mean(0)
+            if s < 700:
+                np.testing.assert_allclose(o[0, h, i], mean * c / (c + math.exp(s)), rtol=1e-12,
+                                           atol=1e-300)
+                assert abs(lse[0, h, i] - math.log(c + math.exp(s))) < 1e-12
+            else:  # e^s overflows a double: the row's mass is all on the sink
+                np.testing.assert_allclose(o[0, h, i], mean * c * math.exp(-s), rtol=1e-12,
+                                           atol=1e-300)
+                assert abs(lse[0, h, i] - (s + math.log1p(c * math.exp(-s)))) < 1e-9
+
+
+def test_row_with_only_the_sink():
+    """Queries before the first key (sq > skv, causal) allow no key: O = 0, LSE = sink."""
+    hq, sq, skv, d = 2, 6, 3, 4
+    q = rand_bits(54, (1, hq, sq, d), "q")
+    k, v = rand_bits(54, (1, 1, skv, d), "k"), rand_bits(54, (1, 1, skv, d), "v")
+    sinks = np.array([0.75, -2.5])
+    o, lse = oracle.prefill(q, k, v, 0.5, 1, 0, sink=sinks)
+    for i in range(sq - skv):  # q_pos = i + skv - sq < 0
+        np.testing.assert_array_equal(o[0, :, i], 0.0)
+        np.testing.assert_array_equal(lse[0, :, i], sinks)
+    o0, _ = oracle.prefill(q, k, v, 0.5, 1, 0)
+    np.testing.assert_array_equal(o0[0, :, : sq - skv], 0.0)
+
+
+def _sink_as_key(q, k, v, scale, sink_val):
+    """The sink written as an ordinary key at position 0 of an extended problem: one more
+    head dimension holding 1 in every query and sink/scale in the extra key (0 in the
+    real keys), a zero value row, and a zero extra value column.  Requires sink/scale
+    exact in bf16."""
+    b, hq, sq, d = q.shape
+    _, hkv, skv, _ = k.shape
+    one = bits(np.array([1.0], np.float32))[0]
+    ks = bits(np.array([sink_val / scale], np.float32))[0]
+    q2 = np.concatenate([q, np.full((b, hq, sq, 1), one, np.uint16)], axis=3)
+    k2 = np.zeros((b, hkv, skv + 1, d + 1), np.uint16)
+    k2[:, :, 1:, :d] = k
+    k2[:, :, 0, d] = ks
+    v2 = np.zeros((b, hkv, skv + 1, d + 1), np.uint16)
+    v2[:, :, 1:, :d] = v
+    return q2, k2, v2
+
+
+@pytest.mark.parametrize("causal", [0, 1])
+def test_sink_equals_an_extra_zero_value_key(causal):
+    """The pages append the sink as one more column of the max and of the sum; the same
+    row, built as an ordinary key (score = sink, value 0) through the no-sink oracle,
+    must give the same O and LSE.  The extra key sits at position 0, which every causal
+    row with q_pos >= -1 sees."""
+    b, hq, hkv, sq, skv, d, scale, s = 1, 2, 1, 9, 14, 8, 0.5, 1.5
+    q = rand_bits(55, (b, hq, sq, d), "q")
+    k, v = rand_bits(55, (b, hkv, skv, d), "k"), rand_bits(55, (b, hkv, skv, d), "v")
+    o1, l1 = oracle.prefill(q, k, v, scale, causal, 0, sink=np.full(hq, s))
+    q2, k2, v2 = _sink_as_key(q, k, v, scale, s)
+    o2, l2 = oracle.prefill(q2, k2, v2, scale, causal, 0)
+    np.testing.assert_array_equal(o2[..., d], 0.0)
+    np.testing.assert_allclose(o1, o2[..., :d], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def test_decode_sink_equals_an_extra_zero_value_key():
+    hq, hkv, d, n, sa, scale, s = 4, 2, 8, 21, 2, 0.25, -0.75
+    fk, fv, _, _, _ = _flat_and_paged(56, 1, hkv, d, [n], 8, False)
+    q = rand_bits(57, (1, hq, sa, d), "q")
+    sinks = np.full(hq, s)
+    o1, l1 = oracle.decode(q, fk, fv, None, np.array([n], np.int32), scale, sink=sinks)
+    q2, k2, v2 = _sink_as_key(q, fk[:, :, :n], fv[:, :, :n], scale, s)
+    o2, l2 = oracle.decode(q2, k2, v2, None, np.array([n + 1], np.int32), scale)
+    np.testing.assert_allclose(o1, o2[..., :d], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
