@@ -202,7 +202,9 @@ def time_steps(fn, steps, warmup, flush_buf, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False):
+def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False, sink=False):
+    """Time attn_fwd_prefill on workload w (with sink=True: attn_fwd_prefill_ex with the
+    per-head sink logits of workloads.configs.sink_logits)."""
     import torch
 
     import flash_attention_forward_attn_gb300 as A
@@ -212,10 +214,15 @@ def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False)
     o = torch.empty(q.shape, dtype=torch.bfloat16 if w.o_dtype == "bf16" else torch.float32,
                     device=dev)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    sk = torch.from_numpy(C.sink_logits(w.hq)).to(dev) if sink else None
 
     def step():
-        A.attn_fwd_prefill(q, k, v, causal=w.causal, window=w.window, scale=w.scale, o=o, lse=lse,
-                           stream=stream)
+        if sink:
+            A.attn_fwd_prefill_ex(q, k, v, causal=w.causal, window=w.window, scale=w.scale, o=o,
+                                  lse=lse, sink=sk, stream=stream)
+        else:
+            A.attn_fwd_prefill(q, k, v, causal=w.causal, window=w.window, scale=w.scale, o=o,
+                               lse=lse, stream=stream)
 
     ms = time_steps(step, steps, warmup, flush, stream)
     assert A.attn_get_device_error(stream) == 0
@@ -224,9 +231,9 @@ def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False)
     value, slowest_s = aggregate_throughput(flops * steps, sum(ms) / 1e3, world, dev)
     tflops = value / 1e12
     achieved = flops / (mean_ms / 1e3) / 1e12
-    traffic = recorded_traffic("prefill", w.name)
+    traffic = None if sink else recorded_traffic("prefill", w.name)
     ent = {
-        "workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": mean_ms,
+        "workload": w.name + ("+sink" if sink else ""), "value": tflops, "unit": "TFLOP/s", "ms_per_step": mean_ms,
         "ms_min": min(ms), "flops_per_step": flops, "steps": steps, "gpu_launches": steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
@@ -306,7 +313,9 @@ def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
             "pipelining": "2 buffer sets; per-input upload streams; download stream"}
 
 
-def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world):
+def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False):
+    """Time attn_fwd_decode on workload w (with sink=True: attn_fwd_decode_ex with the
+    per-head sink logits of workloads.configs.sink_logits)."""
     import torch
 
     import flash_attention_forward_attn_gb300 as A
@@ -317,11 +326,16 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world):
                      dtype=torch.uint8, device=dev)
     o = torch.empty(t["q"].shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(t["q"].shape[:3], dtype=torch.float32, device=dev)
+    sk = torch.from_numpy(C.sink_logits(w.hq)).to(dev) if sink else None
+    args = (t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["cache_len"])
 
     def step():
-        A.attn_fwd_decode(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["cache_len"],
-                          max_cache_len=t["max_cache_len"], scale=w.scale, o=o, lse=lse,
-                          workspace=ws, stream=stream)
+        if sink:
+            A.attn_fwd_decode_ex(*args, max_cache_len=t["max_cache_len"], scale=w.scale, o=o,
+                                 lse=lse, sink=sk, workspace=ws, stream=stream)
+        else:
+            A.attn_fwd_decode(*args, max_cache_len=t["max_cache_len"], scale=w.scale, o=o,
+                              lse=lse, workspace=ws, stream=stream)
 
     ms = time_steps(step, steps, warmup, flush, stream)
     assert A.attn_get_device_error(stream) == 0
@@ -330,12 +344,13 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world):
     value, slowest_s = aggregate_throughput(nbytes * steps, sum(ms) / 1e3, world, dev)
     achieved = nbytes / (mean_ms / 1e3) / 1e9
     ent = {
-        "workload": w.name, "value": value / 1e9, "unit": "GB/s", "ms_per_step": mean_ms,
+        "workload": w.name + ("+sink" if sink else ""), "value": value / 1e9, "unit": "GB/s",
+        "ms_per_step": mean_ms,
         "ms_min": min(ms), "bytes_per_step": nbytes, "mean_cache_len": float(t["lens"].mean()),
         "steps": steps, "gpu_launches": 2 * steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": recorded_traffic("decode", w.name),
+                     "traffic": None if sink else recorded_traffic("decode", w.name),
                      "timed": "whole call (split-KV kernel + combine kernel)",
                      "peak_source": f"{peaks['source']} HBM copy (MEASURED_PEAKS.json)"},
         "slowest_rank_s": slowest_s,
@@ -440,6 +455,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="time only this named workload (profiling runs); prints its entry")
+    ap.add_argument("--sink", action="store_true",
+                    help="with --workload: the _ex call with per-head attention-sink logits")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -464,9 +481,11 @@ def main():
     if args.workload is not None:
         wx = C.REGISTRY[args.workload]
         if isinstance(wx, C.PrefillWorkload):
-            ent = prefill_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world)
+            ent = prefill_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world,
+                                sink=args.sink)
         else:
-            ent = decode_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world)
+            ent = decode_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world,
+                               sink=args.sink)
         if rank == 0:
             print(json.dumps(ent), flush=True)
         return 0
@@ -487,6 +506,13 @@ def main():
             for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4):
                 extras[wx.name] = decode_entry(wx, dev, max(ext_steps, 50), args.warmup, flush,
                                                stream, peaks, world)
+            # the attention sink (attn_opts.sink) on the 2K prefill and the 1-token decode
+            ent = prefill_entry(w, dev, ext_steps, args.warmup, flush, stream, peaks, world,
+                                sink=True)
+            extras[ent["workload"]] = ent
+            ent = decode_entry(C.PAGED_DECODE, dev, max(ext_steps, 50), args.warmup, flush,
+                               stream, peaks, world, sink=True)
+            extras[ent["workload"]] = ent
     clocks = clk.summary()
 
     cpu = None

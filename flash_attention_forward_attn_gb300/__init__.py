@@ -42,6 +42,11 @@ def library_path() -> str:
     return _build.LIB
 
 
+class AttnOpts(ctypes.Structure):
+    """attn_opts of attn.h: optional features of the _ex calls."""
+    _fields_ = [("sink", ctypes.c_void_p)]
+
+
 def load_library(build_if_missing: bool = False):
     """Load libattn_gb300.so (building it first only if asked).  Raises if absent."""
     global _lib
@@ -58,13 +63,19 @@ def load_library(build_if_missing: bool = False):
                                "(the attention path has no CPU fallback)")
         lib = ctypes.CDLL(path)
         P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        O = ctypes.POINTER(AttnOpts)
         lib.attn_fwd_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P]
         lib.attn_fwd_prefill.restype = I
+        lib.attn_fwd_prefill_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, O, P]
+        lib.attn_fwd_prefill_ex.restype = I
         lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
         lib.attn_decode_workspace_bytes.restype = S
         lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, I, I, P,
                                         S, P]
         lib.attn_fwd_decode.restype = I
+        lib.attn_fwd_decode_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, I, I,
+                                           O, P, S, P]
+        lib.attn_fwd_decode_ex.restype = I
         lib.attn_fwd_decode_static_ws.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F,
                                                   P, P, I, I, P]
         lib.attn_fwd_decode_static_ws.restype = I
@@ -128,12 +139,9 @@ def attn_get_device_error(stream=None) -> int:
     return load_library().attn_get_device_error(_stream_ptr(stream))
 
 
-def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
-                     o=None, lse=None, o_dtype=None, stream=None):
-    """O, LSE of softmax(scale Q K^T + mask) V.  q [b,hq,sq,d], k/v [b,hkv,skv,d] bf16."""
+def _prefill_marshal(q, k, v, o, lse, o_dtype):
     import torch
 
-    lib = load_library()
     _req(q, "q", torch.bfloat16)
     _req(k, "k", torch.bfloat16, q.device)
     _req(v, "v", torch.bfloat16, q.device)
@@ -152,10 +160,44 @@ def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | N
         _req(lse, "lse", torch.float32, q.device)
         if tuple(lse.shape) != (b, hq, sq):
             raise ValueError("lse must be [b,hq,sq]")
+    return o, (b, hq, hkv, sq, skv, d)
+
+
+def _opts(sink, hq, device):
+    """attn_opts for the _ex calls: sink is an fp32 tensor [hq] on the device, or None."""
+    import torch
+
+    if sink is not None:
+        _req(sink, "sink", torch.float32, device)
+        if tuple(sink.shape) != (hq,):
+            raise ValueError("sink must hold one fp32 logit per query head: shape [hq]")
+    return AttnOpts(sink=None if sink is None else sink.data_ptr())
+
+
+def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
+                     o=None, lse=None, o_dtype=None, stream=None):
+    """O, LSE of softmax(scale Q K^T + mask) V.  q [b,hq,sq,d], k/v [b,hkv,skv,d] bf16."""
+    lib = load_library()
+    o, (b, hq, hkv, sq, skv, d) = _prefill_marshal(q, k, v, o, lse, o_dtype)
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     _check(lib.attn_fwd_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, hq, hkv, sq,
                                 skv, d, sc, int(bool(causal)), int(window), _dtype_code(o.dtype),
                                 _stream_ptr(stream)), "attn_fwd_prefill")
+    return o, lse
+
+
+def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
+                        o=None, lse=None, o_dtype=None, sink=None, stream=None):
+    """attn_fwd_prefill with the attn_opts options: sink, an fp32 [hq] tensor of
+    per-query-head sink logits (scaled-score units) on q's device, or None."""
+    lib = load_library()
+    o, (b, hq, hkv, sq, skv, d) = _prefill_marshal(q, k, v, o, lse, o_dtype)
+    opts = _opts(sink, hq, q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(lib.attn_fwd_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, hq, hkv, sq,
+                                   skv, d, sc, int(bool(causal)), int(window),
+                                   _dtype_code(o.dtype), ctypes.byref(opts), _stream_ptr(stream)),
+           "attn_fwd_prefill_ex")
     return o, lse
 
 
@@ -225,47 +267,45 @@ def attn_fwd_decode(q, k_cache, v_cache, block_table, cache_len, *, max_cache_le
     """Decode attention.  q [b,hq,s_active,d] bf16; paged caches [num_pages,hkv,page,d] with
     block_table int32/uint32-bits [b,max_pages], or flat caches [b,hkv,max_cache_len,d] with
     block_table None; cache_len int32 [b]."""
+    lib = load_library()
+    o, (b, hq, hkv, d, s_active, page, max_pages, num_pages, mcl) = _decode_marshal(
+        q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse, o_dtype)
+    workspace = _decode_workspace(workspace, b, hq, s_active, d, mcl, kv_chunk, q.device)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(lib.attn_fwd_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                               _ptr(cache_len), b, hq, hkv, d, s_active, page, max_pages,
+                               num_pages, mcl, sc, _ptr(o), _ptr(lse), _dtype_code(o.dtype),
+                               kv_chunk, _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+           "attn_fwd_decode")
+    return o, lse
+
+
+def _decode_workspace(workspace, b, hq, s_active, d, max_cache_len, kv_chunk, dev):
     import torch
 
-    lib = load_library()
-    _req(q, "q", torch.bfloat16)
-    dev = q.device
-    _req(k_cache, "k_cache", torch.bfloat16, dev)
-    _req(v_cache, "v_cache", torch.bfloat16, dev)
-    _req(cache_len, "cache_len", torch.int32, dev)
-    if v_cache.shape != k_cache.shape or q.dim() != 4 or k_cache.dim() != 4:
-        raise ValueError("bad q / cache shapes")
-    b, hq, s_active, d = q.shape
-    if block_table is not None:
-        _req(block_table, "block_table", block_table.dtype, dev)
-        if block_table.dtype not in (torch.int32, torch.uint32):
-            raise TypeError("block_table must hold 32-bit entries (uint32 bit patterns)")
-        if block_table.dim() != 2 or block_table.shape[0] != b:
-            raise ValueError("block_table must be [b, max_pages_per_seq]")
-        num_pages, hkv, page, dk = k_cache.shape
-        max_pages = block_table.shape[1]
-    else:
-        bb, hkv, ml, dk = k_cache.shape
-        if bb != b or ml != max_cache_len:
-            raise ValueError("a flat cache must be [b, hkv, max_cache_len, d]")
-        num_pages, page, max_pages = 0, 0, 0
-    if dk != d or cache_len.shape != (b,):
-        raise ValueError("head_dim or cache_len shape mismatch")
-    if o is None:
-        o = torch.empty((b, hq, s_active, d), dtype=o_dtype or torch.bfloat16, device=dev)
-    _req(o, "o", o.dtype, dev)
-    if lse is not None:
-        _req(lse, "lse", torch.float32, dev)
     need = attn_decode_workspace_bytes(b, hq, s_active, d, max_cache_len, kv_chunk)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     _req(workspace, "workspace", torch.uint8, dev)
+    return workspace
+
+
+def attn_fwd_decode_ex(q, k_cache, v_cache, block_table, cache_len, *, max_cache_len: int,
+                       scale: float | None = None, o=None, lse=None, o_dtype=None,
+                       kv_chunk: int = 0, sink=None, workspace=None, stream=None):
+    """attn_fwd_decode with the attn_opts options: sink, an fp32 [hq] tensor of
+    per-query-head sink logits (scaled-score units) on q's device, or None."""
+    lib = load_library()
+    o, (b, hq, hkv, d, s_active, page, max_pages, num_pages, mcl) = _decode_marshal(
+        q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse, o_dtype)
+    workspace = _decode_workspace(workspace, b, hq, s_active, d, mcl, kv_chunk, q.device)
+    opts = _opts(sink, hq, q.device)
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    _check(lib.attn_fwd_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                               _ptr(cache_len), b, hq, hkv, d, s_active, page, max_pages,
-                               num_pages, max_cache_len, sc, _ptr(o), _ptr(lse),
-                               _dtype_code(o.dtype), kv_chunk, _ptr(workspace),
-                               workspace.numel(), _stream_ptr(stream)), "attn_fwd_decode")
+    _check(lib.attn_fwd_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                  _ptr(cache_len), b, hq, hkv, d, s_active, page, max_pages,
+                                  num_pages, mcl, sc, _ptr(o), _ptr(lse), _dtype_code(o.dtype),
+                                  kv_chunk, ctypes.byref(opts), _ptr(workspace),
+                                  workspace.numel(), _stream_ptr(stream)), "attn_fwd_decode_ex")
     return o, lse
 
 

@@ -47,6 +47,14 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// The options of an _ex call (NULL = none set); returns false if a set option is invalid.
+bool read_opts(const attn_opts* opts, const float** sink) {
+    *sink = opts ? opts->sink : nullptr;
+    return *sink == nullptr || aligned4(*sink);
+}
+
 bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
 int resolve_chunk(int kv_chunk, int b, int max_cache_len) {
@@ -86,14 +94,17 @@ const char* attn_status_string(attn_status s) {
     return "ATTN_ERR_UNKNOWN";
 }
 
-attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
-                             int b, int hq, int hkv, int sq, int skv, int d, float scale,
-                             int causal, int window, attn_dtype o_dtype, void* stream) {
+attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int b, int hq, int hkv, int sq, int skv, int d, float scale,
+                                int causal, int window, attn_dtype o_dtype,
+                                const attn_opts* opts, void* stream) {
     if (b <= 0 || hq <= 0 || hkv <= 0 || sq < 0 || skv < 0 || window < 0) return ATTN_ERR_INVALID_ARG;
     if (hq % hkv != 0 || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
     if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
     if (window > 0 && !causal) return ATTN_ERR_UNSUPPORTED;  // the window is chained after causal
+    const float* sink;
+    if (!read_opts(opts, &sink)) return ATTN_ERR_INVALID_ARG;
     if (sq == 0) return ATTN_OK;
     if (!q || !o || (skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o) || (skv > 0 && (!aligned16(k) || !aligned16(v))))
@@ -101,8 +112,15 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* 
     if ((long long)b * hq > 0x7fffffffLL || (long long)b * hkv > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
     attn::PrefillArgs a{q, k, v, o, lse, b, hq, hkv, sq, skv, d, scale, causal ? 1 : 0, window,
-                        o_dtype};
+                        o_dtype, sink};
     return attn::prefill_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int b, int hq, int hkv, int sq, int skv, int d, float scale,
+                             int causal, int window, attn_dtype o_dtype, void* stream) {
+    return attn_fwd_prefill_ex(q, k, v, o, lse, b, hq, hkv, sq, skv, d, scale, causal, window,
+                               o_dtype, nullptr, stream);
 }
 
 size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_cache_len,
@@ -113,12 +131,13 @@ size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_c
     return ob + mlb;
 }
 
-attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
-                            const uint32_t* block_table, const int32_t* cache_len, int b, int hq,
-                            int hkv, int d, int s_active, int page_size, int max_pages_per_seq,
-                            int num_pages, int max_cache_len, float scale, void* o, float* lse,
-                            attn_dtype o_dtype, int kv_chunk, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                               const uint32_t* block_table, const int32_t* cache_len, int b,
+                               int hq, int hkv, int d, int s_active, int page_size,
+                               int max_pages_per_seq, int num_pages, int max_cache_len,
+                               float scale, void* o, float* lse, attn_dtype o_dtype, int kv_chunk,
+                               const attn_opts* opts, void* workspace, size_t workspace_bytes,
+                               void* stream) {
     if (b <= 0 || hq <= 0 || hkv <= 0 || s_active <= 0 || max_cache_len <= 0)
         return ATTN_ERR_INVALID_ARG;
     if (hq % hkv != 0 || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -129,6 +148,8 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
         return ATTN_ERR_INVALID_ARG;
     if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
     if ((hq / hkv) * (long long)s_active > 16) return ATTN_ERR_UNSUPPORTED;
+    const float* sink;
+    if (!read_opts(opts, &sink)) return ATTN_ERR_INVALID_ARG;
     if (block_table) {
         if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0)
             return ATTN_ERR_INVALID_ARG;
@@ -166,7 +187,19 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
     a.part_o = static_cast<float*>(workspace);
     a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ob);
     a.max_splits = max_splits;
+    a.sink = sink;
     return attn::decode_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const uint32_t* block_table, const int32_t* cache_len, int b, int hq,
+                            int hkv, int d, int s_active, int page_size, int max_pages_per_seq,
+                            int num_pages, int max_cache_len, float scale, void* o, float* lse,
+                            attn_dtype o_dtype, int kv_chunk, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    return attn_fwd_decode_ex(q, k_cache, v_cache, block_table, cache_len, b, hq, hkv, d, s_active,
+                              page_size, max_pages_per_seq, num_pages, max_cache_len, scale, o,
+                              lse, o_dtype, kv_chunk, nullptr, workspace, workspace_bytes, stream);
 }
 
 attn_status attn_gen_mask_decode(const int32_t* cache_len, int b, int hq, int s_active,

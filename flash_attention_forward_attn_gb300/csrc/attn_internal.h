@@ -28,6 +28,7 @@ struct PrefillArgs {
     float scale;
     int causal, window;
     attn_dtype o_dtype;
+    const float* sink;  // [hq] sink logits, or NULL
 };
 
 struct DecodeArgs {
@@ -45,6 +46,7 @@ struct DecodeArgs {
     float* part_o;        // [b*hq*s_active][max_splits][d]
     float* part_ml;       // [b*hq*s_active][max_splits][2]
     int max_splits;
+    const float* sink;    // [hq] sink logits, or NULL
 };
 
 // Tokens per split when the caller passes kv_chunk = 0: the largest power of two in

@@ -356,6 +356,31 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Normaliser and log-sum-exp of one finished row.  m is the row's reference max in log2
+// units of the scaled scores, l its running sum against m, live whether any key was
+// allowed; sink is the head's sink logit in scaled-score units (-inf: none).  The sink
+// joins the max and the sum as one more logit with no value row ("Flash-Attention:
+// Context (CTE)", "Algorithm - the per-section max update" and "Algorithm - fused exp
+// and the running sum"): with M = max(m, sink log2 e) and f = 2^(m - M),
+//   O = acc f / (l f + 2^(sink log2 e - M)),   LSE = (M + log2(l f + 2^(sink log2 e - M))) ln 2.
+// Writes inv (O = acc * inv) and lse (natural log).  Without a sink this is exactly
+// inv = 1 / l and lse = (m + log2 l) ln 2, or 0 and -inf for a row with nothing allowed.
+__device__ __forceinline__ void finish_row(bool live, float m, float l, float sink, float& inv,
+                                           float& lse) {
+    constexpr float kL2e = 1.4426950408889634f, kLn2f = 0.6931471805599453f;
+    if (sink == -INFINITY) {
+        inv = live ? 1.0f / l : 0.f;
+        lse = live ? (m + __log2f(l)) * kLn2f : -INFINITY;
+        return;
+    }
+    const float sl = sink * kL2e;
+    const float M = live ? fmaxf(m, sl) : sl;
+    const float f = live ? ex2(m - M) : 0.f;
+    const float lt = l * f + ex2(sl - M);
+    inv = f / lt;
+    lse = (M + __log2f(lt)) * kLn2f;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

@@ -337,11 +337,13 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
 
 // Merge the chunks of one (sequence, head, new token) row by log-sum-exp:
 //   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
-//   LSE = (M + log2 L) ln 2   (m_i are in log2 units of the scaled scores).
+//   LSE = (M + log2 L) ln 2   (m_i are in log2 units of the scaled scores);
+// with a sink, the merged row is finished by finish_row (the sink joins M and L).
 template <int D, typename OutT>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __restrict__ cache_len,
                                                            const float* __restrict__ part_o,
                                                            const float* __restrict__ part_ml,
+                                                           const float* __restrict__ sink,
                                                            OutT* __restrict__ o, float* lse,
                                                            int hq, int s_active, int chunk,
                                                            int max_splits, int max_cache_len) {
@@ -363,8 +365,17 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __rest
                 Lsum += wt * ml[2 * s + 1];
                 acc += wt * po[(size_t)s * D];
             }
-            out = acc / Lsum;
-            lse_v = (M + __log2f(Lsum)) * kLn2;
+            if (sink == nullptr) {
+                out = acc / Lsum;
+                lse_v = (M + __log2f(Lsum)) * kLn2;
+            } else {
+                float inv;
+                finish_row(true, M, Lsum, sink[(rowid / s_active) % hq], inv, lse_v);
+                out = acc * inv;
+            }
+        } else if (sink != nullptr) {  // nothing allowed: the sink alone (O = 0, LSE = sink)
+            float inv;
+            finish_row(false, 0.f, 0.f, sink[(rowid / s_active) % hq], inv, lse_v);
         }
     }
     if constexpr (sizeof(OutT) == 2)
@@ -444,11 +455,11 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     const unsigned nrows = (unsigned)((size_t)a.b * a.hq * a.s_active);
     if (a.o_dtype == ATTN_BF16)
         decode_combine_kernel<D, __nv_bfloat16><<<nrows, D, 0, stream>>>(
-            a.cache_len, a.part_o, a.part_ml, static_cast<__nv_bfloat16*>(a.o), a.lse, a.hq,
+            a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<__nv_bfloat16*>(a.o), a.lse, a.hq,
             a.s_active, a.kv_chunk, a.max_splits, a.max_cache_len);
     else
         decode_combine_kernel<D, float><<<nrows, D, 0, stream>>>(
-            a.cache_len, a.part_o, a.part_ml, static_cast<float*>(a.o), a.lse, a.hq, a.s_active,
+            a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<float*>(a.o), a.lse, a.hq, a.s_active,
             a.kv_chunk, a.max_splits, a.max_cache_len);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;

@@ -59,6 +59,7 @@ static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * kRegsLaunch3, "register 
 struct PrefillParams {
     void* o;
     float* lse;
+    const float* sink;  // [hq] sink logits of the query heads, or NULL
     int hq, hkv, sq, skv, group, nqt, window, causal, o_f32;
     int nbh;     // b * hq
     int nunits;  // work units of the persistent kernel
@@ -536,10 +537,10 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             }
             const bool row_valid = t.rows > 0 && row < t.rows;
             const bool live = have_o && l_sum > 0.f;
-            const float inv = live ? 1.0f / l_sum : 0.f;
+            float inv, lse_v;
+            finish_row(live, m_used, l_sum, p.sink ? p.sink[bh % p.hq] : -INFINITY, inv, lse_v);
             const size_t orow = (size_t)bh * p.sq + q_row;
-            if (row_valid && p.lse != nullptr)
-                p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+            if (row_valid && p.lse != nullptr) p.lse[orow] = lse_v;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t rr[32];
@@ -1019,10 +1020,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             }
             const bool row_valid = t.rows > 0 && row < t.rows;
             const bool live = have_o && l_sum > 0.f;
-            const float inv = live ? 1.0f / l_sum : 0.f;
+            float inv, lse_v;
+            finish_row(live, m_used, l_sum, p.sink ? p.sink[u.bh % p.hq] : -INFINITY, inv, lse_v);
             const size_t orow = (size_t)u.bh * p.sq + q_row;
-            if (row_valid && p.lse != nullptr)
-                p.lse[orow] = live ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+            if (row_valid && p.lse != nullptr) p.lse[orow] = lse_v;
             if (!p.o_f32) {
                 // bf16: O_X -> registers (then O_X is free), scale, stage in shared memory in
                 // the 128-byte-swizzled box layout, and one thread stores the boxes with TMA
@@ -1206,6 +1207,7 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     PrefillParams p;
     p.o = a.o;
     p.lse = a.lse;
+    p.sink = a.sink;
     p.hq = a.hq;
     p.hkv = a.hkv;
     p.sq = a.sq;

@@ -49,6 +49,28 @@ typedef enum {
 typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
 
 /*
+ * attn_opts -- optional features of attn_fwd_prefill_ex and attn_fwd_decode_ex.  Pass
+ * NULL, or a zero-initialised struct, for the behaviour of the plain calls.  The struct
+ * is read on the host during the call and may be reused or freed afterwards.
+ *
+ *   sink : attention sink ("Flash-Attention: Context (CTE)", "Algorithm - the
+ *          per-section max update" and "Algorithm - fused exp and the running sum";
+ *          "Flash-Attention: Decode (TKG)", one sink per query head broadcast over the
+ *          batch).  A DEVICE array of fp32 [hq], one logit per query head, in the units
+ *          of the scaled scores s_j = scale * q.k_j.  The sink joins every row's maximum
+ *          and sum as one more logit without a value row:
+ *            O   = sum_{allowed j} exp(s_j - M) V_j / (sum_{allowed j} exp(s_j - M) + exp(sink - M))
+ *            LSE = M + ln(sum_{allowed j} exp(s_j - M) + exp(sink - M)),
+ *            M   = max(max_{allowed j} s_j, sink);
+ *          a row with no allowed key gets O = 0 and LSE = sink.  A logit of -inf is no
+ *          sink for that head.  Values must be finite or -inf (+inf or NaN give
+ *          unspecified results).  NULL = no sink.  Must be 4-byte aligned.
+ */
+typedef struct {
+    const float* sink;
+} attn_opts;
+
+/*
  * attn_fwd_prefill -- fused attention forward for sq queries against skv keys.
  *
  * Defines ("Flash-Attention: Context (CTE)", Abstract and "The masking"; optimum-neuron
@@ -79,6 +101,16 @@ typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
 attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                              int b, int hq, int hkv, int sq, int skv, int d, float scale,
                              int causal, int window, attn_dtype o_dtype, void* stream);
+
+/*
+ * attn_fwd_prefill_ex -- attn_fwd_prefill with the options of attn_opts (NULL = none):
+ * same arguments, layouts, semantics and errors, plus ATTN_ERR_INVALID_ARG for an
+ * invalid option (a misaligned sink pointer).
+ */
+attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int b, int hq, int hkv, int sq, int skv, int d, float scale,
+                                int causal, int window, attn_dtype o_dtype,
+                                const attn_opts* opts, void* stream);
 
 /*
  * attn_decode_workspace_bytes -- bytes of caller-provided scratch that attn_fwd_decode
@@ -132,6 +164,21 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
                             int num_pages, int max_cache_len, float scale, void* o, float* lse,
                             attn_dtype o_dtype, int kv_chunk, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/*
+ * attn_fwd_decode_ex -- attn_fwd_decode with the options of attn_opts (NULL = none):
+ * same arguments (opts sits after kv_chunk), layouts, workspace, semantics and errors,
+ * plus ATTN_ERR_INVALID_ARG for an invalid option (a misaligned sink pointer).  The
+ * sink is applied where the split-KV chunks are merged, so the workspace size is the
+ * same as without it.
+ */
+attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                               const uint32_t* block_table, const int32_t* cache_len, int b,
+                               int hq, int hkv, int d, int s_active, int page_size,
+                               int max_pages_per_seq, int num_pages, int max_cache_len,
+                               float scale, void* o, float* lse, attn_dtype o_dtype, int kv_chunk,
+                               const attn_opts* opts, void* workspace, size_t workspace_bytes,
+                               void* stream);
 
 /*
  * attn_fwd_decode_static_ws -- attn_fwd_decode for callers that cannot allocate device

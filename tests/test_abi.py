@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     assert declared_symbols() == sorted([
         "attn_fwd_prefill", "attn_decode_workspace_bytes", "attn_fwd_decode",
         "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
-        "attn_fwd_decode_static_ws"])
+        "attn_fwd_decode_static_ws", "attn_fwd_prefill_ex", "attn_fwd_decode_ex"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -89,6 +89,20 @@ def decode(lib, **kw):
 ])
 def test_decode_rejects_before_launch(lib, kw, status):
     assert decode(lib, **kw) == status
+
+
+def test_ex_calls_check_their_options_before_launch(lib):
+    bad = A.AttnOpts(sink=(1 << 20) + 2)  # a sink pointer that is not 4-byte aligned
+    none = A.AttnOpts()
+    args = (FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 0, 16, 128, 0.1, 1, 0, 0)
+    assert lib.attn_fwd_prefill_ex(*args, ctypes.byref(bad), None) == 1
+    assert lib.attn_fwd_prefill_ex(*args, ctypes.byref(none), None) == 0  # sq = 0: no-op
+    assert lib.attn_fwd_prefill_ex(*args, None, None) == 0
+    dargs = (FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 4, 32, 4, 8, 128, 0.1, FAKE, None, 0, 0)
+    assert lib.attn_fwd_decode_ex(*dargs, ctypes.byref(bad), FAKE, 1 << 30, None) == 1
+    # an invalid size is still reported first, with or without options
+    dbad = dargs[:8] + (80,) + dargs[9:]  # d = 80
+    assert lib.attn_fwd_decode_ex(*dbad, ctypes.byref(none), FAKE, 1 << 30, None) == 2
 
 
 def _ws(b, hq, s_active, d, max_len, chunk):

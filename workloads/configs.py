@@ -313,6 +313,17 @@ def decode_inputs_torch(w: DecodeWorkload, device, permute: bool = True):
     return out
 
 
+# Attention-sink logits, one per query head (scaled-score units): a fixed cycle of a
+# neutral, moderate, dominant (e^9 and e^60 outweigh every key of an N(0,1) row),
+# negligible and absent (-inf) sink, so every regime of the sink is present in a run.
+SINK_CYCLE = (0.0, 2.5, -1.75, 9.0, -40.0, float("-inf"), 0.75, 60.0)
+
+
+def sink_logits(hq: int) -> np.ndarray:
+    """fp32 [hq] sink logits of the query heads."""
+    return np.array([SINK_CYCLE[h % len(SINK_CYCLE)] for h in range(hq)], dtype=np.float32)
+
+
 def decode_io_bytes(w: DecodeWorkload, lens: np.ndarray) -> int:
     """Algorithmic HBM bytes of one decode call: each needed K/V byte once, the page
     table entries in use, cache_len, Q and O (bf16) and LSE."""
