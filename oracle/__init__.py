@@ -73,6 +73,11 @@ def _load():
             lib.oracle_decode_sink.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, D, P, L, L,
                                                P, P]
             lib.oracle_decode_sink.restype = I
+            lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_f64.restype = D
+            lib.oracle_decode_e4m3.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, D, D, D,
+                                               P, L, L, P, P]
+            lib.oracle_decode_e4m3.restype = I
             lib.oracle_decode_mask.argtypes = [P, I, I, I, L, P]
             lib.oracle_decode_mask.restype = I
             _lib = lib
@@ -203,6 +208,48 @@ def decode(q, k_cache, v_cache, table, cache_len, scale, threads=None, sink=None
                                       _ptr(cl), B, HQ, HKV, D, SA, page, max_pages, num_pages,
                                       max_len, float(scale), _ptr(sk), bh, bh + 1, _ptr(o),
                                       _ptr(lse))
+
+    with ThreadPoolExecutor(max_workers=min(threads or default_threads(), B * HQ)) as ex:
+        for rc in ex.map(run, range(B * HQ)):
+            _check(rc)
+    return o, lse
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """e4m3 byte codes -> float64 values (NaN for the NaN codes)."""
+    lib = _load()
+    flat = np.asarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([lib.oracle_e4m3_to_f64(int(x)) for x in flat]).reshape(np.shape(codes))
+
+
+def decode_e4m3(q, k_cache, v_cache, table, cache_len, scale, k_scale, v_scale, threads=None,
+                sink=None):
+    """Decode over an e4m3 cache.  q [B,HQ,s_active,D] bf16 bits; caches of e4m3 bytes
+    (uint8), paged [num_pages,HKV,page,D] with table [B,max_pages], or flat
+    [B,HKV,max_len,D] with table None; a cache byte stands for e4m3(byte) * k_scale (K) or
+    * v_scale (V).  sink: [HQ] per-query-head sink logits, or None."""
+    q = _u16(q)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    B, HQ, SA, D = q.shape
+    sk = _sinks(sink, HQ)
+    cl = np.ascontiguousarray(cache_len, dtype=np.int32)
+    if table is not None:
+        table = np.ascontiguousarray(table, dtype=np.uint32)
+        num_pages, HKV, page, _ = k_cache.shape
+        max_pages, max_len = table.shape[1], 0
+    else:
+        _, HKV, max_len, _ = k_cache.shape
+        num_pages, page, max_pages = 0, 1, 0
+    o = np.empty((B, HQ, SA, D), dtype=np.float64)
+    lse = np.empty((B, HQ, SA), dtype=np.float64)
+    lib = _load()
+
+    def run(bh):
+        return lib.oracle_decode_e4m3(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(table),
+                                      _ptr(cl), B, HQ, HKV, D, SA, page, max_pages, num_pages,
+                                      max_len, float(scale), float(k_scale), float(v_scale),
+                                      _ptr(sk), bh, bh + 1, _ptr(o), _ptr(lse))
 
     with ThreadPoolExecutor(max_workers=min(threads or default_threads(), B * HQ)) as ex:
         for rc in ex.map(run, range(B * HQ)):

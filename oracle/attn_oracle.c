@@ -298,6 +298,69 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
                               bh_end, o, lse);
 }
 
+/* e4m3 -> double, from the format's definition (the 8-bit float with 1 sign, 4 exponent
+ * and 3 mantissa bits, exponent bias 7, no infinities, and NaN only at S.1111.111; the
+ * FP8-e4m3 KV cache of Flash-Attention: Decode (TKG), "Decode (TKG) vs context (CTE) -
+ * the diff").  Exponent field 0 holds the subnormals m/8 * 2^-6. */
+double oracle_e4m3_to_f64(uint8_t b)
+{
+    const int sgn = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Decode over an e4m3 KV cache: each cache byte stands for e4m3(byte) * k_scale (K) or
+ * e4m3(byte) * v_scale (V); otherwise exactly oracle_decode_sink, whose layouts it shares
+ * with one byte per cache element.  The dequantised K and V of a sequence are built in
+ * double and run through the same row computation. */
+int oracle_decode_e4m3(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                       const uint32_t *table, const int32_t *cache_len, int B, int HQ, int HKV,
+                       int D, int s_active, int page, long max_pages, long num_pages,
+                       long max_cache_len, double scale, double k_scale, double v_scale,
+                       const double *sink, long bh_begin, long bh_end, double *o, double *lse)
+{
+    if (HKV <= 0 || HQ % HKV != 0 || s_active <= 0) return ORACLE_ERR_ARG;
+    int rc = ORACLE_OK;
+    for (long bh = bh_begin; bh < bh_end && rc == ORACLE_OK; ++bh) {
+        long b = bh / HQ;
+        int h = (int)(bh % HQ);
+        int g = oracle_kv_head(h, HQ, HKV);
+        long len = cache_len[b];
+        if (len < s_active || (!table && len > max_cache_len) ||
+            (table && (len + page - 1) / page > max_pages))
+            return ORACLE_ERR_ARG;
+        double *kd = (double *)malloc(sizeof(double) * (size_t)(len * D + 1));
+        double *vd = (double *)malloc(sizeof(double) * (size_t)(len * D + 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!kd || !vd || !qd) { free(kd); free(vd); free(qd); return ORACLE_ERR_NOMEM; }
+        for (long j = 0; j < len && rc == ORACLE_OK; ++j) {
+            size_t row;
+            if (table) {
+                uint32_t pg = table[(size_t)b * max_pages + j / page];
+                if ((long)pg >= num_pages) { rc = ORACLE_ERR_PAGE; break; }
+                row = ((size_t)pg * HKV + g) * page + (size_t)(j % page);
+            } else {
+                row = ((size_t)b * HKV + g) * (size_t)max_cache_len + (size_t)j;
+            }
+            for (int x = 0; x < D; ++x) {
+                kd[j * D + x] = oracle_e4m3_to_f64(k_cache[row * D + x]) * k_scale;
+                vd[j * D + x] = oracle_e4m3_to_f64(v_cache[row * D + x]) * v_scale;
+            }
+        }
+        for (int t = 0; t < s_active && rc == ORACLE_OK; ++t) {
+            const size_t r = (size_t)bh * s_active + t;
+            widen(q + r * D, D, qd);
+            rc = row_f64(qd, kd, vd, len, D, scale, len - s_active + t, 1, 0,
+                         sink ? sink[h] : -INFINITY, o + r * D, lse + r, NULL);
+        }
+        free(kd); free(vd); free(qd);
+    }
+    return rc;
+}
+
 /* The decode 0/1 mask, [B][HQ][s_active][max_len] bytes (TKG "gen_mask_tkg"):
  *   type A: position j is attendable iff j < cache_len[b] (cache_len = next write position);
  *   type C: the last s_active slots are the new tokens, and among them query t sees

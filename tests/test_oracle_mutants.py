@@ -29,6 +29,12 @@ MUTANTS = {
     "sink_left_out_of_the_sum": ("double l = exp(sink - m);", "double l = 0.0;"),
     "sink_left_out_of_the_max": ("double m = sink;", "double m = -INFINITY;"),
     "sink_sign_flipped": ("double l = exp(sink - m);", "double l = exp(-sink - m);"),
+    "e4m3_bias_off_by_one": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+                             "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_subnormal_as_normal": ("if (e == 0) v = ldexp((double)m / 8.0, -6);",
+                                 "if (e == 0) v = ldexp(1.0 + (double)m / 8.0, -7);"),
+    "e4m3_v_scale_dropped": ("oracle_e4m3_to_f64(v_cache[row * D + x]) * v_scale;",
+                             "oracle_e4m3_to_f64(v_cache[row * D + x]);"),
 }
 
 

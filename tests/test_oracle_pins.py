@@ -429,3 +429,81 @@ def test_decode_sink_equals_an_extra_zero_value_key():
     o2, l2 = oracle.decode(q2, k2, v2, None, np.array([n + 1], np.int32), scale)
     np.testing.assert_allclose(o1, o2[..., :d], rtol=0, atol=1e-13)
     np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- e4m3 KV cache
+# An FP8-e4m3 KV cache (Flash-Attention: Decode (TKG), "Decode (TKG) vs context (CTE) - the
+# diff"): a cache byte stands for e4m3(byte) * k_scale (K) or * v_scale (V).
+
+def test_e4m3_decoding_matches_torch_float8():
+    """All 256 codes against PyTorch's own float8_e4m3fn -> float conversion."""
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().double().numpy()
+    assert np.array_equal(ours, ref, equal_nan=True)
+    assert np.isnan(ours[[0x7F, 0xFF]]).all() and np.isfinite(np.delete(ours, [0x7F, 0xFF])).all()
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def _e4m3_codes(seed, n):
+    """Seeded e4m3 codes without the NaN codes."""
+    c = (rng.u64_np(seed, 0, n) & 0xFF).astype(np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0
+    return c
+
+
+def _e4m3_caches(seed, b, hkv, d, lens, page):
+    """Paged e4m3 caches through a permuted table (padding slots hold the NaN code), and
+    the same values as bf16 bit patterns (e4m3 values are exact in bf16)."""
+    npg = [-(-n // page) for n in lens]
+    total = sum(npg)
+    phys = np.argsort(rng.u64_np(seed + 1, 0, total), kind="stable").astype(np.uint32)
+    table = np.full((b, -(-max(lens) // page)), 0xFFFFFFFF, dtype=np.uint32)
+    kc = np.full((total, hkv, page, d), 0x7F, dtype=np.uint8)
+    vc = kc.copy()
+    off = 0
+    for i, n in enumerate(lens):
+        table[i, : npg[i]] = phys[off: off + npg[i]]
+        off += npg[i]
+        kk = _e4m3_codes(seed + 10 + i, hkv * n * d).reshape(hkv, n, d)
+        vv = _e4m3_codes(seed + 20 + i, hkv * n * d).reshape(hkv, n, d)
+        for j in range(n):
+            kc[table[i, j // page], :, j % page] = kk[:, j]
+            vc[table[i, j // page], :, j % page] = vv[:, j]
+    as_bf16 = lambda c: bits(oracle.e4m3_to_f64(np.where((c & 0x7F) == 0x7F, 0, c)).astype(np.float32))
+    kb, vb = as_bf16(kc), as_bf16(vc)
+    kb[(kc & 0x7F) == 0x7F] = rng.BF16_NAN_BITS
+    vb[(vc & 0x7F) == 0x7F] = rng.BF16_NAN_BITS
+    return kc, vc, kb, vb, table
+
+
+def test_e4m3_decode_equals_bf16_decode_on_the_same_values():
+    b, hq, hkv, d, page, sa = 2, 4, 2, 16, 8, 2
+    lens = [13, 30]
+    kc, vc, kb, vb, table = _e4m3_caches(60, b, hkv, d, lens, page)
+    q = rand_bits(61, (b, hq, sa, d), "q")
+    cl = np.array(lens, np.int32)
+    o1, l1 = oracle.decode_e4m3(q, kc, vc, table, cl, 0.05, 1.0, 1.0)
+    o2, l2 = oracle.decode(q, kb, vb, table, cl, 0.05)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    assert np.isfinite(o1).all()  # the NaN codes of the padding slots never leak
+
+
+def test_e4m3_scales_are_exact_factors():
+    """k_scale = 2 at scale s equals k_scale = 1 at scale 2s; v_scale = 1/2 halves O and
+    leaves LSE alone (powers of two scale exactly)."""
+    b, hq, hkv, d, page, sa = 2, 4, 1, 16, 8, 3
+    lens = [9, 27]
+    kc, vc, _, _, table = _e4m3_caches(62, b, hkv, d, lens, page)
+    q = rand_bits(63, (b, hq, sa, d), "q")
+    cl = np.array(lens, np.int32)
+    o1, l1 = oracle.decode_e4m3(q, kc, vc, table, cl, 0.03, 2.0, 1.0)
+    o2, l2 = oracle.decode_e4m3(q, kc, vc, table, cl, 0.06, 1.0, 1.0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    o3, l3 = oracle.decode_e4m3(q, kc, vc, table, cl, 0.06, 1.0, 0.5)
+    np.testing.assert_array_equal(o3, o2 * 0.5)
+    np.testing.assert_array_equal(l3, l2)
