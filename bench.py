@@ -313,15 +313,16 @@ def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
             "pipelining": "2 buffer sets; per-input upload streams; download stream"}
 
 
-def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False):
+def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False, e4m3=False):
     """Time attn_fwd_decode on workload w (with sink=True: attn_fwd_decode_ex with the
-    per-head sink logits of workloads.configs.sink_logits)."""
+    per-head sink logits of workloads.configs.sink_logits; with e4m3=True: attn_fwd_decode_ex
+    over the same caches rounded to FP8-e4m3, k_scale = v_scale = 1)."""
     import torch
 
     import flash_attention_forward_attn_gb300 as A
     from workloads import configs as C
 
-    t = C.decode_inputs_torch(w, dev)
+    t = C.decode_inputs_e4m3_torch(w, dev) if e4m3 else C.decode_inputs_torch(w, dev)
     ws = torch.empty(A.attn_decode_workspace_bytes(w.b, w.hq, w.s_active, w.d, t["max_cache_len"]),
                      dtype=torch.uint8, device=dev)
     o = torch.empty(t["q"].shape, dtype=torch.bfloat16, device=dev)
@@ -330,7 +331,7 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False)
     args = (t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["cache_len"])
 
     def step():
-        if sink:
+        if sink or e4m3:
             A.attn_fwd_decode_ex(*args, max_cache_len=t["max_cache_len"], scale=w.scale, o=o,
                                  lse=lse, sink=sk, workspace=ws, stream=stream)
         else:
@@ -340,17 +341,17 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False)
     ms = time_steps(step, steps, warmup, flush, stream)
     assert A.attn_get_device_error(stream) == 0
     mean_ms = sum(ms) / len(ms)
-    nbytes = C.decode_io_bytes(w, t["lens"])
+    nbytes = C.decode_io_bytes(w, t["lens"], kv_bytes=1 if e4m3 else 2)
     value, slowest_s = aggregate_throughput(nbytes * steps, sum(ms) / 1e3, world, dev)
     achieved = nbytes / (mean_ms / 1e3) / 1e9
+    label = w.name + ("+sink" if sink else "") + ("+e4m3" if e4m3 else "")
     ent = {
-        "workload": w.name + ("+sink" if sink else ""), "value": value / 1e9, "unit": "GB/s",
-        "ms_per_step": mean_ms,
+        "workload": label, "value": value / 1e9, "unit": "GB/s", "ms_per_step": mean_ms,
         "ms_min": min(ms), "bytes_per_step": nbytes, "mean_cache_len": float(t["lens"].mean()),
         "steps": steps, "gpu_launches": 2 * steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": None if sink else recorded_traffic("decode", w.name),
+                     "traffic": recorded_traffic("decode", label),
                      "timed": "whole call (split-KV kernel + combine kernel)",
                      "peak_source": f"{peaks['source']} HBM copy (MEASURED_PEAKS.json)"},
         "slowest_rank_s": slowest_s,
@@ -457,6 +458,8 @@ def main():
                     help="time only this named workload (profiling runs); prints its entry")
     ap.add_argument("--sink", action="store_true",
                     help="with --workload: the _ex call with per-head attention-sink logits")
+    ap.add_argument("--e4m3", action="store_true",
+                    help="with a decode --workload: the caches rounded to FP8-e4m3")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -485,7 +488,7 @@ def main():
                                 sink=args.sink)
         else:
             ent = decode_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world,
-                               sink=args.sink)
+                               sink=args.sink, e4m3=args.e4m3)
         if rank == 0:
             print(json.dumps(ent), flush=True)
         return 0
@@ -513,6 +516,11 @@ def main():
             ent = decode_entry(C.PAGED_DECODE, dev, max(ext_steps, 50), args.warmup, flush,
                                stream, peaks, world, sink=True)
             extras[ent["workload"]] = ent
+            # the FP8-e4m3 KV cache (attn_opts.kv_dtype): half the cache bytes
+            for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4):
+                ent = decode_entry(wx, dev, max(ext_steps, 50), args.warmup, flush, stream,
+                                   peaks, world, e4m3=True)
+                extras[ent["workload"]] = ent
     clocks = clk.summary()
 
     cpu = None

@@ -42,9 +42,13 @@ def library_path() -> str:
     return _build.LIB
 
 
+ATTN_KV_BF16, ATTN_KV_E4M3 = 0, 1
+
+
 class AttnOpts(ctypes.Structure):
     """attn_opts of attn.h: optional features of the _ex calls."""
-    _fields_ = [("sink", ctypes.c_void_p)]
+    _fields_ = [("sink", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 def load_library(build_if_missing: bool = False):
@@ -163,7 +167,7 @@ def _prefill_marshal(q, k, v, o, lse, o_dtype):
     return o, (b, hq, hkv, sq, skv, d)
 
 
-def _opts(sink, hq, device):
+def _opts(sink, hq, device, kv_dtype=ATTN_KV_BF16, k_scale=1.0, v_scale=1.0):
     """attn_opts for the _ex calls: sink is an fp32 tensor [hq] on the device, or None."""
     import torch
 
@@ -171,7 +175,8 @@ def _opts(sink, hq, device):
         _req(sink, "sink", torch.float32, device)
         if tuple(sink.shape) != (hq,):
             raise ValueError("sink must hold one fp32 logit per query head: shape [hq]")
-    return AttnOpts(sink=None if sink is None else sink.data_ptr())
+    return AttnOpts(sink=None if sink is None else sink.data_ptr(), kv_dtype=kv_dtype,
+                    k_scale=float(k_scale), v_scale=float(v_scale))
 
 
 def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
@@ -202,13 +207,14 @@ def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float 
 
 
 def _decode_marshal(q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse,
-                    o_dtype):
+                    o_dtype, cache_dtype=None):
     import torch
 
     _req(q, "q", torch.bfloat16)
     dev = q.device
-    _req(k_cache, "k_cache", torch.bfloat16, dev)
-    _req(v_cache, "v_cache", torch.bfloat16, dev)
+    cache_dtype = cache_dtype or torch.bfloat16
+    _req(k_cache, "k_cache", cache_dtype, dev)
+    _req(v_cache, "v_cache", cache_dtype, dev)
     _req(cache_len, "cache_len", torch.int32, dev)
     if v_cache.shape != k_cache.shape or q.dim() != 4 or k_cache.dim() != 4:
         raise ValueError("bad q / cache shapes")
@@ -292,14 +298,21 @@ def _decode_workspace(workspace, b, hq, s_active, d, max_cache_len, kv_chunk, de
 
 def attn_fwd_decode_ex(q, k_cache, v_cache, block_table, cache_len, *, max_cache_len: int,
                        scale: float | None = None, o=None, lse=None, o_dtype=None,
-                       kv_chunk: int = 0, sink=None, workspace=None, stream=None):
+                       kv_chunk: int = 0, sink=None, k_scale: float = 1.0, v_scale: float = 1.0,
+                       workspace=None, stream=None):
     """attn_fwd_decode with the attn_opts options: sink, an fp32 [hq] tensor of
-    per-query-head sink logits (scaled-score units) on q's device, or None."""
+    per-query-head sink logits (scaled-score units) on q's device, or None; and an e4m3
+    cache: k_cache and v_cache of dtype torch.float8_e4m3fn (or their bytes as uint8),
+    where element x stands for e4m3(x) * k_scale (K) or e4m3(x) * v_scale (V)."""
+    import torch
+
     lib = load_library()
+    fp8 = k_cache.dtype in (torch.float8_e4m3fn, torch.uint8)
     o, (b, hq, hkv, d, s_active, page, max_pages, num_pages, mcl) = _decode_marshal(
-        q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse, o_dtype)
+        q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse, o_dtype,
+        cache_dtype=k_cache.dtype if fp8 else None)
     workspace = _decode_workspace(workspace, b, hq, s_active, d, mcl, kv_chunk, q.device)
-    opts = _opts(sink, hq, q.device)
+    opts = _opts(sink, hq, q.device, ATTN_KV_E4M3 if fp8 else ATTN_KV_BF16, k_scale, v_scale)
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     _check(lib.attn_fwd_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                   _ptr(cache_len), b, hq, hkv, d, s_active, page, max_pages,

@@ -25,8 +25,10 @@ TensorMapEncodeFn tensor_map_encoder() {
     return fn;
 }
 
-bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                   const uint64_t* strides_bytes, const uint32_t* box) {
+namespace {
+
+bool make_map(CUtensorMapDataType type, CUtensorMap* map, const void* base, int rank,
+              const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
     TensorMapEncodeFn enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t d[3], s[2];
@@ -36,9 +38,21 @@ bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t*
         bx[i] = box[i];
     }
     for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d,
-               s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return enc(map, type, (cuuint32_t)rank, const_cast<void*>(base), d, s, bx, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box) {
+    return make_map(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, rank, dims, strides_bytes, box);
+}
+
+bool make_u8_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box) {
+    return make_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, map, base, rank, dims, strides_bytes, box);
 }
 
 }  // namespace attn
@@ -50,9 +64,24 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // The options of an _ex call (NULL = none set); returns false if a set option is invalid.
-bool read_opts(const attn_opts* opts, const float** sink) {
-    *sink = opts ? opts->sink : nullptr;
-    return *sink == nullptr || aligned4(*sink);
+struct Opts {
+    const float* sink = nullptr;
+    bool e4m3 = false;
+    float k_scale = 1.f, v_scale = 1.f;
+};
+
+bool read_opts(const attn_opts* opts, Opts* o) {
+    if (!opts) return true;
+    o->sink = opts->sink;
+    if (o->sink && !aligned4(o->sink)) return false;
+    if (opts->kv_dtype != ATTN_KV_BF16 && opts->kv_dtype != ATTN_KV_E4M3) return false;
+    o->e4m3 = opts->kv_dtype == ATTN_KV_E4M3;
+    if (o->e4m3) {
+        if (!isfinite(opts->k_scale) || !isfinite(opts->v_scale)) return false;
+        o->k_scale = opts->k_scale;
+        o->v_scale = opts->v_scale;
+    }
+    return true;
 }
 
 bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
@@ -103,8 +132,9 @@ attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, voi
     if (o_dtype != ATTN_BF16 && o_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
     if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
     if (window > 0 && !causal) return ATTN_ERR_UNSUPPORTED;  // the window is chained after causal
-    const float* sink;
-    if (!read_opts(opts, &sink)) return ATTN_ERR_INVALID_ARG;
+    Opts op;
+    if (!read_opts(opts, &op)) return ATTN_ERR_INVALID_ARG;
+    if (op.e4m3) return ATTN_ERR_UNSUPPORTED;  // prefill reads bf16 K and V
     if (sq == 0) return ATTN_OK;
     if (!q || !o || (skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o) || (skv > 0 && (!aligned16(k) || !aligned16(v))))
@@ -112,7 +142,7 @@ attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, voi
     if ((long long)b * hq > 0x7fffffffLL || (long long)b * hkv > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
     attn::PrefillArgs a{q, k, v, o, lse, b, hq, hkv, sq, skv, d, scale, causal ? 1 : 0, window,
-                        o_dtype, sink};
+                        o_dtype, op.sink};
     return attn::prefill_launch(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -148,8 +178,9 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
         return ATTN_ERR_INVALID_ARG;
     if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
     if ((hq / hkv) * (long long)s_active > 16) return ATTN_ERR_UNSUPPORTED;
-    const float* sink;
-    if (!read_opts(opts, &sink)) return ATTN_ERR_INVALID_ARG;
+    Opts op;
+    if (!read_opts(opts, &op)) return ATTN_ERR_INVALID_ARG;
+    if (op.e4m3 && d == 64) return ATTN_ERR_UNSUPPORTED;  // half a 128-byte box per row
     if (block_table) {
         if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0)
             return ATTN_ERR_INVALID_ARG;
@@ -187,7 +218,10 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
     a.part_o = static_cast<float*>(workspace);
     a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ob);
     a.max_splits = max_splits;
-    a.sink = sink;
+    a.sink = op.sink;
+    a.kv_e4m3 = op.e4m3 ? 1 : 0;
+    a.k_scale = op.k_scale;
+    a.v_scale = op.v_scale;
     return attn::decode_launch(a, static_cast<cudaStream_t>(stream));
 }
 

@@ -47,6 +47,8 @@ struct DecodeArgs {
     float* part_ml;       // [b*hq*s_active][max_splits][2]
     int max_splits;
     const float* sink;    // [hq] sink logits, or NULL
+    int kv_e4m3;          // the caches hold e4m3 bytes
+    float k_scale, v_scale;  // their dequantisation scales (1 for bf16)
 };
 
 // Tokens per split when the caller passes kv_chunk = 0: the largest power of two in
@@ -72,6 +74,9 @@ TensorMapEncodeFn tensor_map_encoder();
 // bf16 tensor map of rank 2 or 3 (innermost dim first), 128-byte swizzle, zero OOB fill.
 bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                    const uint64_t* strides_bytes, const uint32_t* box);
+// The same for a tensor of bytes (e4m3 values): dims and box in bytes.
+bool make_u8_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box);
 
 attn_status prefill_launch(const PrefillArgs& a, cudaStream_t stream);
 attn_status decode_launch(const DecodeArgs& a, cudaStream_t stream);

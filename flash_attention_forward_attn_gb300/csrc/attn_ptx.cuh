@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace attn {
@@ -332,6 +333,16 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same product with f16 operands (fp32 accumulate).
+__device__ __forceinline__ void mma_f16_16816(float* c, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -381,9 +392,31 @@ __device__ __forceinline__ void finish_row(bool live, float m, float l, float si
     lse = (M + __log2f(lt)) * kLn2f;
 }
 
+// Two e4m3 values (low byte first) -> f16x2 (low half first), exactly: every e4m3 value,
+// subnormals included, is an f16 normal or zero.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t r;
+    const unsigned short v = static_cast<unsigned short>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two e4m3 values (low byte first) -> bf16x2 (low half first), exactly (e4m3 is a subset of
+// bf16), by way of f16 and fp32.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
+    const uint32_t h = e4m3x2_to_f16x2(two_bytes);
+    return pack_bf16(__half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xffffu))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16))));
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled

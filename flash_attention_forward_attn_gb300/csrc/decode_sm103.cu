@@ -28,11 +28,10 @@ __device__ unsigned g_decode_error;
 
 constexpr int kBT = 32;          // tokens per pipeline slot
 constexpr int kConsumers = 4;    // consumer warps
-constexpr int kStages = 4;       // ring slots (one per consumer warp)
 constexpr int kThreads = (kConsumers + 1) * 32;
 // Consumer warp w takes tiles w, w + kConsumers, ... and waits on slot i % kStages at the
 // phase of tile i; that phase accounting holds only when every slot belongs to one warp.
-static_assert(kStages == kConsumers, "each consumer warp owns one ring slot");
+// So kStages is a multiple of kConsumers: slot s then only ever holds tiles of warp s % kConsumers.
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -44,10 +43,21 @@ __device__ __forceinline__ bool decode_allowed(int j, int len, int s_active, int
     return j < len && j <= len - s_active + t;
 }
 
-template <int D>
+// A K (or V) tile of a slot is kBoxes column boxes of 32 rows x 128 bytes (64 bf16 or 128
+// e4m3 head dims per box), each written by TMA with the 128-byte swizzle.
+template <int D, bool kE4M3>
 struct DecodeLayout {
-    static constexpr int kBoxBytes = kBT * 128;         // 32 rows x 128 bytes (64 bf16)
-    static constexpr int kHalf = (D / 64) * kBoxBytes;  // K (or V) tile of one slot
+    // Ring slots.  A CTA keeps kStages tiles in flight; with two CTAs per SM (registers) the
+    // bf16 ring of 4 x 16 KB keeps HBM near its copy rate, and the e4m3 ring, with tiles half
+    // as large, takes 8 slots (two per consumer warp) to keep the same bytes in flight.
+    static constexpr int kStages = kE4M3 ? 8 : 4;
+    static_assert(kStages % kConsumers == 0, "each ring slot belongs to one consumer warp");
+    static constexpr int kElemBytes = kE4M3 ? 1 : 2;
+    static constexpr int kBoxBytes = kBT * 128;
+    static constexpr int kBoxElems = 128 / kElemBytes;
+    static constexpr int kBoxes = D * kElemBytes / 128;
+    static_assert(kBoxes >= 1 && D * kElemBytes == kBoxes * 128, "whole 128-byte box columns");
+    static constexpr int kHalf = kBoxes * kBoxBytes;    // K (or V) tile of one slot
     static constexpr int kSlot = 2 * kHalf;
     static constexpr int kPipe = kStages * kSlot;
     static constexpr int kMerge = kConsumers * 16 * D * 4;
@@ -63,7 +73,8 @@ struct DecodeParams {
     float* part_ml;
     int hq, hkv, s_active, page_size, max_pages, num_pages, max_cache_len;
     int group, rows, chunk, max_splits, paged, box_rows;
-    float c;  // scale * log2(e)
+    float c;        // scale * log2(e) (* k_scale for an e4m3 cache)
+    float v_scale;  // V dequantisation scale of an e4m3 cache (1 for bf16)
 };
 
 __device__ __forceinline__ bool mbar_wait_plain(uint64_t* bar, uint32_t parity,
@@ -74,11 +85,15 @@ __device__ __forceinline__ bool mbar_wait_plain(uint64_t* bar, uint32_t parity,
     return true;
 }
 
-template <int D>
+// kE4M3: the cache holds e4m3 bytes.  k_scale is folded into p.c and v_scale applied to the
+// chunk's output, so the products run on the exact e4m3 values: K converted to bf16 for
+// the bf16 Q.K^T product, V to f16 for the P.V product with P in f16.
+template <int D, bool kE4M3>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const DecodeParams p) {
-    using L = DecodeLayout<D>;
+    using L = DecodeLayout<D, kE4M3>;
+    constexpr int kStages = L::kStages;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* pipe = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -113,52 +128,73 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            const int nbox = kBT / p.box_rows;
-            const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;
-            int issued = 0;
-            for (int i = 0; i < nblocks; ++i) {
-                const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(&empty_bar[s], ((i / kStages) - 1) & 1, &abort_flag))
-                    break;
-                const int j0 = tok0 + i * kBT;
-                int rows[kBT / 16];
-                uint32_t bytes = 0;
-                for (int bx = 0; bx < nbox; ++bx) {
-                    const int jb = j0 + bx * p.box_rows;
-                    rows[bx] = -1;
-                    if (jb >= len) continue;  // a box wholly past the cache end is not read
-                    if (p.paged) {
-                        const uint32_t pg = __ldg(p.table + (size_t)b * p.max_pages + jb / p.page_size);
-                        if (pg >= (uint32_t)p.num_pages) {
-                            atomicOr(&g_decode_error, kDevErrPageOOB);
-                            continue;  // never dereference an out-of-range page
-                        }
-                        rows[bx] = (int)(((long long)pg * p.hkv + g) * p.page_size + jb % p.page_size);
-                    } else {
-                        rows[bx] = (int)(((long long)b * p.hkv + g) * p.max_cache_len + jb);
-                    }
-                    bytes += 2u * (uint32_t)(D / 64) * box_bytes;
-                }
-                uint8_t* kdst = pipe + s * L::kSlot;
-                uint8_t* vdst = kdst + L::kHalf;
-                mbar_arrive_expect_tx(&full_bar[s], bytes);
-                for (int bx = 0; bx < nbox; ++bx) {
-                    if (rows[bx] < 0) continue;
+        }
+        const int nbox = kBT / p.box_rows;
+        const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;
+        int issued = 0;
+        bool ok = true;
+        // The rows of 32 tiles are found at once, one tile per lane (a paged cache costs a
+        // dependent block-table load per tile, which one thread would pay tile after tile);
+        // lane 0 then issues the tiles in order.
+        for (int i0 = 0; ok && i0 < nblocks; i0 += 32) {
+            int rl[kBT / 16];  // lane's tile i0 + lane: cache row of each box, -1 = not read
 #pragma unroll
-                    for (int dc = 0; dc < D / 64; ++dc) {
-                        tma_load_2d(kdst + dc * L::kBoxBytes + bx * box_bytes, &tm_k, dc * 64,
-                                    rows[bx], &full_bar[s]);
-                        tma_load_2d(vdst + dc * L::kBoxBytes + bx * box_bytes, &tm_v, dc * 64,
-                                    rows[bx], &full_bar[s]);
+            for (int bx = 0; bx < kBT / 16; ++bx) {
+                rl[bx] = -1;
+                const int jb = tok0 + (i0 + lane) * kBT + bx * p.box_rows;
+                // a box wholly past the cache end is not read
+                if (bx >= nbox || i0 + lane >= nblocks || jb >= len) continue;
+                if (p.paged) {
+                    const uint32_t pg = __ldg(p.table + (size_t)b * p.max_pages + jb / p.page_size);
+                    if (pg >= (uint32_t)p.num_pages) {
+                        atomicOr(&g_decode_error, kDevErrPageOOB);
+                        continue;  // never dereference an out-of-range page
+                    }
+                    rl[bx] = (int)(((long long)pg * p.hkv + g) * p.page_size + jb % p.page_size);
+                } else {
+                    rl[bx] = (int)(((long long)b * p.hkv + g) * p.max_cache_len + jb);
+                }
+            }
+            const int n = min(32, nblocks - i0);
+            for (int t = 0; t < n; ++t) {
+                int rows[kBT / 16];
+#pragma unroll
+                for (int bx = 0; bx < kBT / 16; ++bx) rows[bx] = __shfl_sync(0xffffffffu, rl[bx], t);
+                if (lane == 0) {
+                    const int i = i0 + t;
+                    const int s = i % kStages;
+                    if (i >= kStages && !mbar_wait(&empty_bar[s], ((i / kStages) - 1) & 1, &abort_flag)) {
+                        ok = false;
+                    } else {
+                        uint32_t bytes = 0;
+#pragma unroll
+                        for (int bx = 0; bx < kBT / 16; ++bx)
+                            if (bx < nbox && rows[bx] >= 0) bytes += 2u * (uint32_t)L::kBoxes * box_bytes;
+                        uint8_t* kdst = pipe + s * L::kSlot;
+                        uint8_t* vdst = kdst + L::kHalf;
+                        mbar_arrive_expect_tx(&full_bar[s], bytes);
+#pragma unroll
+                        for (int bx = 0; bx < kBT / 16; ++bx) {
+                            if (bx >= nbox || rows[bx] < 0) continue;
+#pragma unroll
+                            for (int dc = 0; dc < L::kBoxes; ++dc) {
+                                tma_load_2d(kdst + dc * L::kBoxBytes + bx * box_bytes, &tm_k,
+                                            dc * L::kBoxElems, rows[bx], &full_bar[s]);
+                                tma_load_2d(vdst + dc * L::kBoxBytes + bx * box_bytes, &tm_v,
+                                            dc * L::kBoxElems, rows[bx], &full_bar[s]);
+                            }
+                        }
+                        issued = i + 1;
                     }
                 }
-                issued = i + 1;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
             }
-            if (abort_flag) {  // let copies already in flight land before the CTA exits
-                for (int i = max(0, issued - kStages); i < issued; ++i)
-                    mbar_wait_plain(&full_bar[i % kStages], (i / kStages) & 1, kWaitLimitCycles);
-                atomicOr(&g_decode_error, kDevErrTimeout);
-            }
+        }
+        if (lane == 0 && abort_flag) {  // let copies already in flight land before the CTA exits
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                mbar_wait_plain(&full_bar[i % kStages], (i / kStages) & 1, kWaitLimitCycles);
+            atomicOr(&g_decode_error, kDevErrTimeout);
         }
     } else {
         // -------------------------------------------------------------- consumers
@@ -171,13 +207,30 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
         if (v0) q0 = p.q + ((size_t)(b * p.hq + g * p.group + r0 / p.s_active) * p.s_active + t0) * D;
         if (v1) q1 = p.q + ((size_t)(b * p.hq + g * p.group + r1 / p.s_active) * p.s_active + t1) * D;
         uint32_t qf[D / 16][4];
+        if constexpr (kE4M3) {
+            // The k index of k-step ks maps 2qd, 2qd+1 to head dims 16 ks + 4 qd + {0, 1} and
+            // 2qd+8, 2qd+9 to 16 ks + 4 qd + {2, 3} (a dot product does not depend on the
+            // order of its terms): one 32-bit shared load then gives a lane the four K bytes
+            // of its k-step.
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const int c = ks * 16 + 2 * qd;
-            qf[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c)) : 0u;
-            qf[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c)) : 0u;
-            qf[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c + 8)) : 0u;
-            qf[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c + 8)) : 0u;
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int c = ks * 16 + 4 * qd;
+                const uint2 a = v0 ? __ldg(reinterpret_cast<const uint2*>(q0 + c)) : make_uint2(0u, 0u);
+                const uint2 e = v1 ? __ldg(reinterpret_cast<const uint2*>(q1 + c)) : make_uint2(0u, 0u);
+                qf[ks][0] = a.x;
+                qf[ks][2] = a.y;
+                qf[ks][1] = e.x;
+                qf[ks][3] = e.y;
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int c = ks * 16 + 2 * qd;
+                qf[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c)) : 0u;
+                qf[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c)) : 0u;
+                qf[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c + 8)) : 0u;
+                qf[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c + 8)) : 0u;
+            }
         }
         float o[D / 8][4];
 #pragma unroll
@@ -193,16 +246,32 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
             float sc[4][4];
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            if constexpr (kE4M3) {
+                // token nt*8 + gq, head dims 16 ks + 4 qd .. +3 (chunk ks of its 128-byte row)
+                const uint8_t* kt = pipe + s * L::kSlot;
 #pragma unroll
-            for (int kp = 0; kp < D / 32; ++kp) {
+                for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    const uint32_t tok = nt * 8 + (lane & 7);
-                    const uint32_t cg = 4 * kp + (lane >> 3);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[nt], qf[2 * kp], b0, b1);
-                    mma_bf16_16816(sc[nt], qf[2 * kp + 1], b2, b3);
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const int tok = nt * 8 + gq;
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                            kt + (ks >> 3) * L::kBoxBytes + sw128_off(tok, ks & 7) + 4 * qd);
+                        mma_bf16_16816(sc[nt], qf[ks], e4m3x2_to_bf16x2(w & 0xffffu),
+                                       e4m3x2_to_bf16x2(w >> 16));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kp = 0; kp < D / 32; ++kp) {
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const uint32_t tok = nt * 8 + (lane & 7);
+                        const uint32_t cg = 4 * kp + (lane >> 3);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
+                        mma_bf16_16816(sc[nt], qf[2 * kp], b0, b1);
+                        mma_bf16_16816(sc[nt], qf[2 * kp + 1], b2, b3);
+                    }
                 }
             }
             const int j0 = tok0 + i * kBT;
@@ -253,20 +322,65 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 l_run[0] += sc[nt][0] + sc[nt][1];
                 l_run[1] += sc[nt][2] + sc[nt][3];
             }
-            // O += P V (P from the score accumulators, V via transposed ldmatrix)
+            // O += P V (P from the score accumulators)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
-                uint32_t pa[4];
-                pa[0] = pack_bf16(sc[2 * ks][0], sc[2 * ks][1]);
-                pa[1] = pack_bf16(sc[2 * ks][2], sc[2 * ks][3]);
-                pa[2] = pack_bf16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-                pa[3] = pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
                 uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
                 if (edge) {  // zero V rows of slots past the cache end (they may hold NaN)
                     const int jl = j0 + ks * 16 + 2 * qd;
                     keep_lo = (jl < len ? 0x0000ffffu : 0u) | (jl + 1 < len ? 0xffff0000u : 0u);
                     keep_hi = (jl + 8 < len ? 0x0000ffffu : 0u) | (jl + 9 < len ? 0xffff0000u : 0u);
                 }
+                uint32_t pa[4];
+                if constexpr (kE4M3) {
+                    // P in f16, V converted to f16.  The n index of n-tile np maps n to head
+                    // dim (D/8) n + np, so a lane (n = gq) reads D/8 consecutive bytes of each
+                    // of its four tokens (k = 2qd, 2qd+1, 2qd+8, 2qd+9) and pairs them bytewise.
+                    pa[0] = pack_f16(sc[2 * ks][0], sc[2 * ks][1]);
+                    pa[1] = pack_f16(sc[2 * ks][2], sc[2 * ks][3]);
+                    pa[2] = pack_f16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+                    pa[3] = pack_f16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+                    constexpr int kW = D / 32;  // 32-bit words of a lane's bytes per token
+                    const uint8_t* vt = pipe + s * L::kSlot + L::kHalf;
+                    const int ta = ks * 16 + 2 * qd;
+                    uint32_t vw[4][kW];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int tok = ta + (r & 1) + (r >> 1) * 8;
+#pragma unroll
+                        for (int c = 0; c < kW / 4; ++c) {
+                            const int ch = (D / 128) * gq + c;  // 16-byte chunk along the row
+                            const uint4 x = *reinterpret_cast<const uint4*>(
+                                vt + (ch >> 3) * L::kBoxBytes + sw128_off(tok, ch & 7));
+                            vw[r][4 * c] = x.x;
+                            vw[r][4 * c + 1] = x.y;
+                            vw[r][4 * c + 2] = x.z;
+                            vw[r][4 * c + 3] = x.w;
+                        }
+                    }
+#pragma unroll
+                    for (int wd = 0; wd < kW; ++wd) {
+                        const uint32_t ab0 = __byte_perm(vw[0][wd], vw[1][wd], 0x5140);
+                        const uint32_t ab1 = __byte_perm(vw[0][wd], vw[1][wd], 0x7362);
+                        const uint32_t cd0 = __byte_perm(vw[2][wd], vw[3][wd], 0x5140);
+                        const uint32_t cd1 = __byte_perm(vw[2][wd], vw[3][wd], 0x7362);
+                        const int np = 4 * wd;
+                        mma_f16_16816(o[np], pa, e4m3x2_to_f16x2(ab0 & 0xffffu) & keep_lo,
+                                      e4m3x2_to_f16x2(cd0 & 0xffffu) & keep_hi);
+                        mma_f16_16816(o[np + 1], pa, e4m3x2_to_f16x2(ab0 >> 16) & keep_lo,
+                                      e4m3x2_to_f16x2(cd0 >> 16) & keep_hi);
+                        mma_f16_16816(o[np + 2], pa, e4m3x2_to_f16x2(ab1 & 0xffffu) & keep_lo,
+                                      e4m3x2_to_f16x2(cd1 & 0xffffu) & keep_hi);
+                        mma_f16_16816(o[np + 3], pa, e4m3x2_to_f16x2(ab1 >> 16) & keep_lo,
+                                      e4m3x2_to_f16x2(cd1 >> 16) & keep_hi);
+                    }
+                    continue;
+                }
+                // bf16: V through transposed ldmatrix
+                pa[0] = pack_bf16(sc[2 * ks][0], sc[2 * ks][1]);
+                pa[1] = pack_bf16(sc[2 * ks][2], sc[2 * ks][3]);
+                pa[2] = pack_bf16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+                pa[3] = pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
 #pragma unroll
                 for (int np = 0; np < D / 16; ++np) {
                     const uint32_t mi = lane >> 3;
@@ -295,11 +409,22 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
         // issued has landed (each was waited on), so the ring can hold the merge data.
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
         float* mo = reinterpret_cast<float*>(pipe);  // [kConsumers][16][D]
+        if constexpr (kE4M3) {
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            const int col = n * 8 + 2 * qd;
-            *reinterpret_cast<float2*>(mo + (warp * 16 + r0) * D + col) = make_float2(o[n][0], o[n][1]);
-            *reinterpret_cast<float2*>(mo + (warp * 16 + r1) * D + col) = make_float2(o[n][2], o[n][3]);
+            for (int n = 0; n < D / 8; ++n) {  // n-tile n holds head dims (D/8) * {2qd, 2qd+1} + n
+                const int d0 = (D / 8) * 2 * qd + n, d1 = d0 + D / 8;
+                mo[(warp * 16 + r0) * D + d0] = o[n][0];
+                mo[(warp * 16 + r0) * D + d1] = o[n][1];
+                mo[(warp * 16 + r1) * D + d0] = o[n][2];
+                mo[(warp * 16 + r1) * D + d1] = o[n][3];
+            }
+        } else {
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                const int col = n * 8 + 2 * qd;
+                *reinterpret_cast<float2*>(mo + (warp * 16 + r0) * D + col) = make_float2(o[n][0], o[n][1]);
+                *reinterpret_cast<float2*>(mo + (warp * 16 + r1) * D + col) = make_float2(o[n][2], o[n][3]);
+            }
         }
         if (qd == 0) {
             m_sh[warp][r0] = m_run[0];
@@ -326,7 +451,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
             const int h = g * p.group + r / p.s_active, t = r % p.s_active;
             const size_t rowid = ((size_t)b * p.hq + h) * p.s_active + t;
             const size_t slot = rowid * p.max_splits + split;
-            p.part_o[slot * D + x] = acc;
+            p.part_o[slot * D + x] = kE4M3 ? acc * p.v_scale : acc;
             if (x == 0) {
                 p.part_ml[slot * 2 + 0] = M;
                 p.part_ml[slot * 2 + 1] = lsum;
@@ -405,19 +530,19 @@ __global__ void gen_mask_kernel(const int32_t* __restrict__ cache_len, int hq, i
     }
 }
 
-template <int D>
+template <int D, bool kE4M3>
 attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
-    using L = DecodeLayout<D>;
+    using L = DecodeLayout<D, kE4M3>;
     const bool paged = a.block_table != nullptr;
     const int box_rows = paged ? (a.page_size < kBT ? a.page_size : kBT) : kBT;
     CUtensorMap tk, tv;
     uint64_t rows = paged ? (uint64_t)a.num_pages * a.hkv * a.page_size
                           : (uint64_t)a.b * a.hkv * a.max_cache_len;
     uint64_t dims[2] = {(uint64_t)D, rows};
-    uint64_t strides[1] = {(uint64_t)D * 2};
-    uint32_t box[2] = {64u, (uint32_t)box_rows};
-    if (!make_bf16_map(&tk, a.k_cache, 2, dims, strides, box) ||
-        !make_bf16_map(&tv, a.v_cache, 2, dims, strides, box))
+    uint64_t strides[1] = {(uint64_t)D * L::kElemBytes};
+    uint32_t box[2] = {(uint32_t)L::kBoxElems, (uint32_t)box_rows};
+    const auto make = kE4M3 ? make_u8_map : make_bf16_map;
+    if (!make(&tk, a.k_cache, 2, dims, strides, box) || !make(&tv, a.v_cache, 2, dims, strides, box))
         return ATTN_ERR_CUDA;
     DecodeParams p;
     p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -438,19 +563,20 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     p.max_splits = a.max_splits;
     p.paged = paged ? 1 : 0;
     p.box_rows = box_rows;
-    p.c = a.scale * kLog2e;
+    p.c = kE4M3 ? a.scale * a.k_scale * kLog2e : a.scale * kLog2e;
+    p.v_scale = kE4M3 ? a.v_scale : 1.0f;
 
     static bool attr_set = false;  // benign race: every thread sets the same value
     if (!attr_set) {
-        if (cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::kDynBytes) != cudaSuccess) {
+        if (cudaFuncSetAttribute(decode_split_kernel<D, kE4M3>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
         attr_set = true;
     }
     dim3 grid(a.max_splits, a.hkv, a.b);
-    decode_split_kernel<D><<<grid, kThreads, L::kDynBytes, stream>>>(tk, tv, p);
+    decode_split_kernel<D, kE4M3><<<grid, kThreads, L::kDynBytes, stream>>>(tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const unsigned nrows = (unsigned)((size_t)a.b * a.hq * a.s_active);
     if (a.o_dtype == ATTN_BF16)
@@ -468,10 +594,17 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
 }  // namespace
 
 attn_status decode_launch(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.kv_e4m3) {
+        switch (a.d) {  // a 64-dim e4m3 row is half a 128-byte box: not supported
+            case 128: return decode_launch_d<128, true>(a, stream);
+            case 256: return decode_launch_d<256, true>(a, stream);
+            default: return ATTN_ERR_UNSUPPORTED;
+        }
+    }
     switch (a.d) {
-        case 64: return decode_launch_d<64>(a, stream);
-        case 128: return decode_launch_d<128>(a, stream);
-        case 256: return decode_launch_d<256>(a, stream);
+        case 64: return decode_launch_d<64, false>(a, stream);
+        case 128: return decode_launch_d<128, false>(a, stream);
+        case 256: return decode_launch_d<256, false>(a, stream);
         default: return ATTN_ERR_UNSUPPORTED;
     }
 }

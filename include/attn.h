@@ -48,6 +48,9 @@ typedef enum {
 
 typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
 
+/* Element type of a decode KV cache (attn_opts.kv_dtype). */
+typedef enum { ATTN_KV_BF16 = 0, ATTN_KV_E4M3 = 1 } attn_kv_dtype;
+
 /*
  * attn_opts -- optional features of attn_fwd_prefill_ex and attn_fwd_decode_ex.  Pass
  * NULL, or a zero-initialised struct, for the behaviour of the plain calls.  The struct
@@ -65,9 +68,22 @@ typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
  *          a row with no allowed key gets O = 0 and LSE = sink.  A logit of -inf is no
  *          sink for that head.  Values must be finite or -inf (+inf or NaN give
  *          unspecified results).  NULL = no sink.  Must be 4-byte aligned.
+ *
+ *   kv_dtype, k_scale, v_scale : decode only (attn_fwd_prefill_ex rejects a kv_dtype other
+ *          than ATTN_KV_BF16 with ATTN_ERR_UNSUPPORTED).  ATTN_KV_E4M3 declares k_cache
+ *          and v_cache as FP8-e4m3 caches ("Flash-Attention: Decode (TKG)", "Decode (TKG)
+ *          vs context (CTE) - the diff"): one byte per element (1 sign, 4 exponent bits
+ *          with bias 7, 3 mantissa bits; no infinities, NaN at S.1111.111), same layouts
+ *          as the bf16 caches with the byte as the element.  Element x of K stands for
+ *          e4m3(x) * k_scale and of V for e4m3(x) * v_scale; both scales must be finite.
+ *          With an e4m3 cache d must be 128 or 256.  Slots past cache_len may hold any
+ *          byte, NaN codes included; they contribute exactly zero.
  */
 typedef struct {
     const float* sink;
+    int kv_dtype;
+    float k_scale;
+    float v_scale;
 } attn_opts;
 
 /*
@@ -105,7 +121,8 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* 
 /*
  * attn_fwd_prefill_ex -- attn_fwd_prefill with the options of attn_opts (NULL = none):
  * same arguments, layouts, semantics and errors, plus ATTN_ERR_INVALID_ARG for an
- * invalid option (a misaligned sink pointer).
+ * invalid option (a misaligned sink pointer) and ATTN_ERR_UNSUPPORTED for an e4m3
+ * kv_dtype (prefill reads bf16 K and V).
  */
 attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int b, int hq, int hkv, int sq, int skv, int d, float scale,
@@ -168,9 +185,11 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
 /*
  * attn_fwd_decode_ex -- attn_fwd_decode with the options of attn_opts (NULL = none):
  * same arguments (opts sits after kv_chunk), layouts, workspace, semantics and errors,
- * plus ATTN_ERR_INVALID_ARG for an invalid option (a misaligned sink pointer).  The
- * sink is applied where the split-KV chunks are merged, so the workspace size is the
- * same as without it.
+ * plus ATTN_ERR_INVALID_ARG for an invalid option (a misaligned sink pointer, an unknown
+ * kv_dtype, a non-finite scale of an e4m3 cache) and ATTN_ERR_UNSUPPORTED for an e4m3
+ * cache with d = 64.  The sink is applied where the split-KV chunks are merged and the
+ * scales are folded into the chunk pass, so the workspace size is the same for every
+ * option.
  */
 attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v_cache,
                                const uint32_t* block_table, const int32_t* cache_len, int b,

@@ -100,6 +100,16 @@ def test_ex_calls_check_their_options_before_launch(lib):
     assert lib.attn_fwd_prefill_ex(*args, None, None) == 0
     dargs = (FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 4, 32, 4, 8, 128, 0.1, FAKE, None, 0, 0)
     assert lib.attn_fwd_decode_ex(*dargs, ctypes.byref(bad), FAKE, 1 << 30, None) == 1
+    e4 = lambda **kw: A.AttnOpts(**dict(dict(kv_dtype=1, k_scale=1.0, v_scale=1.0), **kw))
+    assert lib.attn_fwd_decode_ex(*dargs, ctypes.byref(A.AttnOpts(kv_dtype=5)), FAKE, 1 << 30,
+                                  None) == 1  # unknown cache type
+    assert lib.attn_fwd_decode_ex(*dargs, ctypes.byref(e4(k_scale=float("nan"))), FAKE, 1 << 30,
+                                  None) == 1
+    assert lib.attn_fwd_decode_ex(*dargs, ctypes.byref(e4(v_scale=float("inf"))), FAKE, 1 << 30,
+                                  None) == 1
+    d64 = dargs[:8] + (64,) + dargs[9:]
+    assert lib.attn_fwd_decode_ex(*d64, ctypes.byref(e4()), FAKE, 1 << 30, None) == 2
+    assert lib.attn_fwd_prefill_ex(*args, ctypes.byref(e4()), None) == 2  # prefill reads bf16
     # an invalid size is still reported first, with or without options
     dbad = dargs[:8] + (80,) + dargs[9:]  # d = 80
     assert lib.attn_fwd_decode_ex(*dbad, ctypes.byref(none), FAKE, 1 << 30, None) == 2

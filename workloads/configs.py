@@ -324,10 +324,23 @@ def sink_logits(hq: int) -> np.ndarray:
     return np.array([SINK_CYCLE[h % len(SINK_CYCLE)] for h in range(hq)], dtype=np.float32)
 
 
-def decode_io_bytes(w: DecodeWorkload, lens: np.ndarray) -> int:
-    """Algorithmic HBM bytes of one decode call: each needed K/V byte once, the page
-    table entries in use, cache_len, Q and O (bf16) and LSE."""
-    kv = int(lens.astype(np.int64).sum()) * w.hkv * w.d * 2 * 2
+def decode_inputs_e4m3_torch(w: DecodeWorkload, device, permute: bool = True):
+    """decode_inputs_torch with the caches rounded to e4m3 (torch.float8_e4m3fn, round to
+    nearest even): the FP8-e4m3 cache of the same synthetic values.  The NaN padding
+    slots stay NaN codes; N(0,1) samples never come near e4m3's largest value, 448."""
+    import torch
+
+    t = decode_inputs_torch(w, device, permute)
+    for which in ("k_cache", "v_cache"):
+        t[which] = t[which].to(torch.float8_e4m3fn)
+    return t
+
+
+def decode_io_bytes(w: DecodeWorkload, lens: np.ndarray, kv_bytes: int = 2) -> int:
+    """Algorithmic HBM bytes of one decode call: each needed K/V byte once (kv_bytes per
+    element: 2 for bf16, 1 for e4m3), the page table entries in use, cache_len, Q and O
+    (bf16) and LSE."""
+    kv = int(lens.astype(np.int64).sum()) * w.hkv * w.d * kv_bytes * 2
     pages = int((-(-lens.astype(np.int64) // w.page_size)).sum()) * 4 if w.paged else 0
     qo = 2 * w.b * w.hq * w.s_active * w.d * 2
     lse = w.b * w.hq * w.s_active * 4
