@@ -86,8 +86,11 @@ __device__ __forceinline__ bool mbar_wait_plain(uint64_t* bar, uint32_t parity,
 }
 
 // kE4M3: the cache holds e4m3 bytes.  k_scale is folded into p.c and v_scale applied to the
-// chunk's output, so the products run on the exact e4m3 values: K converted to bf16 for
-// the bf16 Q.K^T product, V to f16 for the P.V product with P in f16.
+// chunk's output, so the products run on the exact e4m3 values, converted to f16 (one
+// instruction per pair): Q.K^T with Q in f16 and P.V with P in f16.  Each Q row is scaled by
+// a power of two that puts its largest |element| in [2^13, 2^14) before it is rounded to
+// f16 (the factor comes back out of the row's softmax scale), so the f16 row holds every
+// bf16 element exactly unless it is below 2^-27 of the row's largest.
 template <int D, bool kE4M3>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -207,20 +210,54 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
         if (v0) q0 = p.q + ((size_t)(b * p.hq + g * p.group + r0 / p.s_active) * p.s_active + t0) * D;
         if (v1) q1 = p.q + ((size_t)(b * p.hq + g * p.group + r1 / p.s_active) * p.s_active + t1) * D;
         uint32_t qf[D / 16][4];
+        float c_row0 = p.c, c_row1 = p.c;  // softmax scale of rows r0, r1 (log2 units)
         if constexpr (kE4M3) {
             // The k index of k-step ks maps 2qd, 2qd+1 to head dims 16 ks + 4 qd + {0, 1} and
             // 2qd+8, 2qd+9 to 16 ks + 4 qd + {2, 3} (a dot product does not depend on the
             // order of its terms): one 32-bit shared load then gives a lane the four K bytes
             // of its k-step.
+            uint2 qa[D / 16], qb[D / 16];
+            float mx_a = 0.f, mx_b = 0.f;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 const int c = ks * 16 + 4 * qd;
-                const uint2 a = v0 ? __ldg(reinterpret_cast<const uint2*>(q0 + c)) : make_uint2(0u, 0u);
-                const uint2 e = v1 ? __ldg(reinterpret_cast<const uint2*>(q1 + c)) : make_uint2(0u, 0u);
-                qf[ks][0] = a.x;
-                qf[ks][2] = a.y;
-                qf[ks][1] = e.x;
-                qf[ks][3] = e.y;
+                qa[ks] = v0 ? __ldg(reinterpret_cast<const uint2*>(q0 + c)) : make_uint2(0u, 0u);
+                qb[ks] = v1 ? __ldg(reinterpret_cast<const uint2*>(q1 + c)) : make_uint2(0u, 0u);
+                const uint32_t wa[2] = {qa[ks].x, qa[ks].y}, wb[2] = {qb[ks].x, qb[ks].y};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t ba = (h & 1) ? (wa[h >> 1] & 0xffff0000u) : (wa[h >> 1] << 16);
+                    const uint32_t bb = (h & 1) ? (wb[h >> 1] & 0xffff0000u) : (wb[h >> 1] << 16);
+                    mx_a = fmaxf(mx_a, fabsf(__uint_as_float(ba)));
+                    mx_b = fmaxf(mx_b, fabsf(__uint_as_float(bb)));
+                }
+            }
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+            // power-of-two row factors 2^sa, 2^sb: the largest |q| lands in [2^13, 2^14)
+            int ea = 0, eb = 0;
+            if (mx_a > 0.f) frexpf(mx_a, &ea);  // mx in [2^(ea-1), 2^ea)
+            if (mx_b > 0.f) frexpf(mx_b, &eb);
+            const int sa = mx_a > 0.f ? 14 - ea : 0, sb = mx_b > 0.f ? 14 - eb : 0;
+            c_row0 = ldexpf(p.c, -sa);
+            c_row1 = ldexpf(p.c, -sb);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t wa[2] = {qa[ks].x, qa[ks].y}, wb[2] = {qb[ks].x, qb[ks].y};
+                uint32_t fa[2], fb[2];
+#pragma unroll
+                for (int w2 = 0; w2 < 2; ++w2) {
+                    fa[w2] = pack_f16(ldexpf(__uint_as_float(wa[w2] << 16), sa),
+                                      ldexpf(__uint_as_float(wa[w2] & 0xffff0000u), sa));
+                    fb[w2] = pack_f16(ldexpf(__uint_as_float(wb[w2] << 16), sb),
+                                      ldexpf(__uint_as_float(wb[w2] & 0xffff0000u), sb));
+                }
+                qf[ks][0] = fa[0];
+                qf[ks][2] = fa[1];
+                qf[ks][1] = fb[0];
+                qf[ks][3] = fb[1];
             }
         } else {
 #pragma unroll
@@ -256,8 +293,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                         const int tok = nt * 8 + gq;
                         const uint32_t w = *reinterpret_cast<const uint32_t*>(
                             kt + (ks >> 3) * L::kBoxBytes + sw128_off(tok, ks & 7) + 4 * qd);
-                        mma_bf16_16816(sc[nt], qf[ks], e4m3x2_to_bf16x2(w & 0xffffu),
-                                       e4m3x2_to_bf16x2(w >> 16));
+                        mma_f16_16816(sc[nt], qf[ks], e4m3x2_to_f16x2(w & 0xffffu),
+                                      e4m3x2_to_f16x2(w >> 16));
                     }
                 }
             } else {
@@ -281,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
             for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    float x0 = sc[nt][e] * p.c, x1 = sc[nt][2 + e] * p.c;
+                    float x0 = sc[nt][e] * c_row0, x1 = sc[nt][2 + e] * c_row1;
                     if (edge) {
                         const int j = j0 + nt * 8 + 2 * qd + e;
                         if (!(v0 && decode_allowed(j, len, p.s_active, t0))) x0 = -INFINITY;
