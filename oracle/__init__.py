@@ -78,6 +78,11 @@ def _load():
             lib.oracle_decode_e4m3.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, D, D, D,
                                                P, L, L, P, P]
             lib.oracle_decode_e4m3.restype = I
+            lib.oracle_rope_row.argtypes = [P, I, D, P]
+            lib.oracle_rope_row.restype = None
+            lib.oracle_decode_ext.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, D, L,
+                                              I, P, P, L, L, P, P]
+            lib.oracle_decode_ext.restype = I
             lib.oracle_decode_mask.argtypes = [P, I, I, I, L, P]
             lib.oracle_decode_mask.restype = I
             _lib = lib
@@ -250,6 +255,50 @@ def decode_e4m3(q, k_cache, v_cache, table, cache_len, scale, k_scale, v_scale, 
                                       _ptr(cl), B, HQ, HKV, D, SA, page, max_pages, num_pages,
                                       max_len, float(scale), float(k_scale), float(v_scale),
                                       _ptr(sk), bh, bh + 1, _ptr(o), _ptr(lse))
+
+    with ThreadPoolExecutor(max_workers=min(threads or default_threads(), B * HQ)) as ex:
+        for rc in ex.map(run, range(B * HQ)):
+            _check(rc)
+    return o, lse
+
+
+def rope_row(x, pos, inv_freq):
+    """Half-split RoPE of one row (float64 [d]) at position pos; returns a new array."""
+    x = np.array(x, dtype=np.float64)
+    f = np.ascontiguousarray(inv_freq, dtype=np.float64)
+    assert f.shape == (x.shape[0] // 2,)
+    _load().oracle_rope_row(_ptr(x), x.shape[0], float(pos), _ptr(f))
+    return x
+
+
+def decode_ext(q, k_cache, v_cache, table, cache_len, scale, window=0, circular=False,
+               k_new=None, v_new=None, inv_freq=None, sink=None, threads=None):
+    """Decode with a window (and a circular flat cache), new tokens' K/V given apart from
+    the cache, RoPE and a sink (see oracle_decode_ext).  q [B,HQ,s_active,D] and the caches
+    are bf16 bits; k_new / v_new [B,HKV,s_active,D] bf16 bits or None; inv_freq [D/2]."""
+    q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
+    B, HQ, SA, D = q.shape
+    sk = _sinks(sink, HQ)
+    kn = None if k_new is None else _u16(k_new)
+    vn = None if v_new is None else _u16(v_new)
+    f = None if inv_freq is None else np.ascontiguousarray(inv_freq, dtype=np.float64)
+    cl = np.ascontiguousarray(cache_len, dtype=np.int32)
+    if table is not None:
+        table = np.ascontiguousarray(table, dtype=np.uint32)
+        num_pages, HKV, page, _ = k_cache.shape
+        max_pages, max_len = table.shape[1], 0
+    else:
+        _, HKV, max_len, _ = k_cache.shape
+        num_pages, page, max_pages = 0, 1, 0
+    o = np.empty((B, HQ, SA, D), dtype=np.float64)
+    lse = np.empty((B, HQ, SA), dtype=np.float64)
+    lib = _load()
+
+    def run(bh):
+        return lib.oracle_decode_ext(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kn), _ptr(vn),
+                                     _ptr(table), _ptr(cl), B, HQ, HKV, D, SA, page, max_pages,
+                                     num_pages, max_len, float(scale), int(window), int(circular),
+                                     _ptr(f), _ptr(sk), bh, bh + 1, _ptr(o), _ptr(lse))
 
     with ThreadPoolExecutor(max_workers=min(threads or default_threads(), B * HQ)) as ex:
         for rc in ex.map(run, range(B * HQ)):

@@ -361,6 +361,102 @@ int oracle_decode_e4m3(const uint16_t *q, const uint8_t *k_cache, const uint8_t 
     return rc;
 }
 
+/* Rotary position embedding of one row x [d] at position pos, half-split form: for
+ * i < d/2, with theta = pos * inv_freq[i],
+ *   x'[i]       = x[i] cos theta - x[i + d/2] sin theta
+ *   x'[i + d/2] = x[i + d/2] cos theta + x[i] sin theta
+ * (Flash-Attention: Decode (TKG), "Algorithm", step 0: RoPE of Q from inverse
+ * frequencies and position ids, fused ahead of the Q.K^T product). */
+void oracle_rope_row(double *x, int d, double pos, const double *inv_freq)
+{
+    const int h = d / 2;
+    for (int i = 0; i < h; ++i) {
+        const double th = pos * inv_freq[i];
+        const double c = cos(th), sn = sin(th);
+        const double a = x[i], b = x[i + h];
+        x[i] = a * c - b * sn;
+        x[i + h] = b * c + a * sn;
+    }
+}
+
+/* Decode with the options of the pages' decode kernel, on a bf16 cache:
+ *   window > 0: new token t (q_pos = len - s_active + t) attends j iff
+ *     q_pos - window + 1 <= j <= q_pos (the prefill window band, AGENTS "Sliding
+ *     window"; TKG "gen_mask_tkg" type B is this band at the end of the cache);
+ *   circular (flat cache only, window > 0): logical position j lives at row
+ *     j mod max_cache_len, so cache_len may exceed max_cache_len (type B's wrapped
+ *     case); positions before the window are never read;
+ *   k_new, v_new ([B][HKV][s_active][D] bf16, or NULL): the new tokens' K and V,
+ *     which stand at positions len - s_active .. len - 1 instead of the cache's rows
+ *     (TKG "New-token K/V append": the product sees [cached prior | active]);
+ *   inv_freq ([D/2], or NULL): RoPE of each query row at its q_pos and of each k_new
+ *     row at its position (TKG "Algorithm", step 0; "GQA / MQA grouped-query broadcast":
+ *     one rotation for the shared K head);
+ *   sink ([HQ] or NULL): as oracle_decode_sink.
+ * Other arguments and layouts as oracle_decode_sink. */
+int oracle_decode_ext(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                      const uint16_t *k_new, const uint16_t *v_new, const uint32_t *table,
+                      const int32_t *cache_len, int B, int HQ, int HKV, int D, int s_active,
+                      int page, long max_pages, long num_pages, long max_cache_len, double scale,
+                      long window, int circular, const double *inv_freq, const double *sink,
+                      long bh_begin, long bh_end, double *o, double *lse)
+{
+    if (HKV <= 0 || HQ % HKV != 0 || s_active <= 0 || window < 0) return ORACLE_ERR_ARG;
+    if (circular && (table || window == 0 || window + s_active - 1 > max_cache_len))
+        return ORACLE_ERR_ARG;
+    int rc = ORACLE_OK;
+    for (long bh = bh_begin; bh < bh_end && rc == ORACLE_OK; ++bh) {
+        long b = bh / HQ;
+        int h = (int)(bh % HQ);
+        int g = oracle_kv_head(h, HQ, HKV);
+        long len = cache_len[b];
+        if (len < s_active || (!table && !circular && len > max_cache_len) ||
+            (table && (len + page - 1) / page > max_pages))
+            return ORACLE_ERR_ARG;
+        /* the oldest position any new token may attend */
+        const long lo = window > 0 ? (len - s_active) - window + 1 : 0;
+        double *kd = (double *)malloc(sizeof(double) * (size_t)(len * D + 1));
+        double *vd = (double *)malloc(sizeof(double) * (size_t)(len * D + 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!kd || !vd || !qd) { free(kd); free(vd); free(qd); return ORACLE_ERR_NOMEM; }
+        for (long j = 0; j < len && rc == ORACLE_OK; ++j) {
+            const long t = j - (len - s_active); /* >= 0: a new token */
+            if (k_new && t >= 0) {
+                const size_t r = (((size_t)b * HKV + g) * s_active + (size_t)t) * D;
+                widen(k_new + r, D, kd + j * D);
+                widen(v_new + r, D, vd + j * D);
+                if (inv_freq) oracle_rope_row(kd + j * D, D, (double)j, inv_freq);
+                continue;
+            }
+            if (j < lo) { /* outside every window: never attended, never read */
+                for (int x = 0; x < D; ++x) kd[j * D + x] = vd[j * D + x] = NAN;
+                continue;
+            }
+            size_t row;
+            if (table) {
+                uint32_t pg = table[(size_t)b * max_pages + j / page];
+                if ((long)pg >= num_pages) { rc = ORACLE_ERR_PAGE; break; }
+                row = ((size_t)pg * HKV + g) * page + (size_t)(j % page);
+            } else {
+                row = ((size_t)b * HKV + g) * (size_t)max_cache_len +
+                      (size_t)(circular ? j % max_cache_len : j);
+            }
+            widen(k_cache + row * D, D, kd + j * D);
+            widen(v_cache + row * D, D, vd + j * D);
+        }
+        for (int t = 0; t < s_active && rc == ORACLE_OK; ++t) {
+            const size_t r = (size_t)bh * s_active + t;
+            const long qp = len - s_active + t;
+            widen(q + r * D, D, qd);
+            if (inv_freq) oracle_rope_row(qd, D, (double)qp, inv_freq);
+            rc = row_f64(qd, kd, vd, len, D, scale, qp, 1, window, sink ? sink[h] : -INFINITY,
+                         o + r * D, lse + r, NULL);
+        }
+        free(kd); free(vd); free(qd);
+    }
+    return rc;
+}
+
 /* The decode 0/1 mask, [B][HQ][s_active][max_len] bytes (TKG "gen_mask_tkg"):
  *   type A: position j is attendable iff j < cache_len[b] (cache_len = next write position);
  *   type C: the last s_active slots are the new tokens, and among them query t sees

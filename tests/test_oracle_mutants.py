@@ -35,6 +35,15 @@ MUTANTS = {
                                  "if (e == 0) v = ldexp(1.0 + (double)m / 8.0, -7);"),
     "e4m3_v_scale_dropped": ("oracle_e4m3_to_f64(v_cache[row * D + x]) * v_scale;",
                              "oracle_e4m3_to_f64(v_cache[row * D + x]);"),
+    "rope_sign_flipped": ("x[i] = a * c - b * sn;", "x[i] = a * c + b * sn;"),
+    "rope_interleaved_pairs": ("const double a = x[i], b = x[i + h];",
+                               "const double a = x[i], b = x[i ^ 1];"),
+    "circular_row_not_wrapped": ("(size_t)(circular ? j % max_cache_len : j);",
+                                 "(size_t)(circular ? j : j);"),
+    "new_token_position_off_by_one": ("const long t = j - (len - s_active); /* >= 0: a new token */",
+                                      "const long t = j - (len - s_active) - 1;"),
+    "rope_q_at_cache_len": ("if (inv_freq) oracle_rope_row(qd, D, (double)qp, inv_freq);",
+                            "if (inv_freq) oracle_rope_row(qd, D, (double)len, inv_freq);"),
 }
 
 

@@ -507,3 +507,132 @@ def test_e4m3_scales_are_exact_factors():
     o3, l3 = oracle.decode_e4m3(q, kc, vc, table, cl, 0.06, 1.0, 0.5)
     np.testing.assert_array_equal(o3, o2 * 0.5)
     np.testing.assert_array_equal(l3, l2)
+
+
+# ----------------------------------------------------------------------------- decode extras
+# Window and circular flat cache (TKG "gen_mask_tkg" type B), new tokens' K/V given apart
+# from the cache (TKG "New-token K/V append"), fused RoPE (TKG "Algorithm", step 0).
+
+def test_decode_ext_without_options_is_decode():
+    b, hq, hkv, d, page, sa = 3, 4, 2, 8, 4, 2
+    lens = [9, 16, 5]
+    q = rand_bits(70, (b, hq, sa, d), "q")
+    cl = np.array(lens, np.int32)
+    fk, fv, kc, vc, table = _flat_and_paged(71, b, hkv, d, lens, page, True)
+    for kk, vv, tt in ((kc, vc, table), (fk, fv, None)):
+        o1, l1 = oracle.decode(q, kk, vv, tt, cl, 0.3)
+        o2, l2 = oracle.decode_ext(q, kk, vv, tt, cl, 0.3)
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("window", [1, 3, 10, 100])
+def test_decode_window_equals_last_rows_of_windowed_prefill(window):
+    hq, hkv, d, n, sa = 4, 2, 16, 45, 3
+    fk, fv, _, _, _ = _flat_and_paged(72, 1, hkv, d, [n], 8, False)
+    q = rand_bits(73, (1, hq, sa, d), "q")
+    o_dec, l_dec = oracle.decode_ext(q, fk, fv, None, np.array([n], np.int32), 0.2, window=window)
+    o_pre, l_pre = oracle.prefill(q, fk[:, :, :n], fv[:, :, :n], 0.2, 1, window)
+    np.testing.assert_array_equal(o_dec, o_pre)
+    np.testing.assert_array_equal(l_dec, l_pre)
+
+
+@pytest.mark.parametrize("n", [40, 64, 101, 300])
+def test_circular_cache_equals_the_full_cache(n):
+    """Logical position j at row j mod cap of a cap-row cache gives the same result as the
+    full cache, whenever the window (plus the new tokens) fits in cap."""
+    hq, hkv, d, sa, cap, window = 4, 2, 8, 3, 32, 28
+    fk, fv, _, _, _ = _flat_and_paged(74, 1, hkv, d, [n], 8, False)
+    ck = np.full((1, hkv, cap, d), rng.BF16_NAN_BITS, dtype=np.uint16)
+    cv = ck.copy()
+    for j in range(max(0, n - cap), n):
+        ck[:, :, j % cap] = fk[:, :, j]
+        cv[:, :, j % cap] = fv[:, :, j]
+    q = rand_bits(75, (1, hq, sa, d), "q")
+    cl = np.array([n], np.int32)
+    o1, l1 = oracle.decode_ext(q, ck, cv, None, cl, 0.25, window=window, circular=True)
+    o2, l2 = oracle.decode_ext(q, fk, fv, None, cl, 0.25, window=window)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    assert np.isfinite(o1).all()
+
+
+def test_new_tokens_given_apart_equal_tokens_in_the_cache():
+    b, hq, hkv, d, page, sa = 2, 4, 2, 8, 4, 3
+    lens = [7, 18]
+    q = rand_bits(76, (b, hq, sa, d), "q")
+    cl = np.array(lens, np.int32)
+    fk, fv, kc, vc, table = _flat_and_paged(77, b, hkv, d, lens, page, True)
+    kn = np.stack([fk[i, :, n - sa:n] for i, n in enumerate(lens)])
+    vn = np.stack([fv[i, :, n - sa:n] for i, n in enumerate(lens)])
+    kc2, vc2 = kc.copy(), vc.copy()
+    for i, n in enumerate(lens):  # the tail slots hold garbage: the new rows come from k_new
+        for j in range(n - sa, n):
+            kc2[table[i, j // page], :, j % page] = rng.BF16_NAN_BITS
+            vc2[table[i, j // page], :, j % page] = rng.BF16_NAN_BITS
+    o1, l1 = oracle.decode(q, kc, vc, table, cl, 0.3)
+    o2, l2 = oracle.decode_ext(q, kc2, vc2, table, cl, 0.3, k_new=kn, v_new=vn)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_rope_quarter_turn_and_identity_by_hand():
+    # d = 2, theta = pi/2: (a, b) -> (-b, a)
+    np.testing.assert_allclose(oracle.rope_row([1.0, 0.0], 1.0, [math.pi / 2]), [0.0, 1.0], atol=1e-15)
+    np.testing.assert_allclose(oracle.rope_row([3.0, 5.0], 1.0, [math.pi / 2]), [-5.0, 3.0], atol=1e-14)
+    # half-split pairing: element i rotates with element i + d/2
+    np.testing.assert_allclose(oracle.rope_row([1.0, 2.0, 3.0, 4.0], 2.0, [math.pi / 2, 0.0]),
+                               [-1.0, 2.0, -3.0, 4.0], atol=1e-14)
+    x = np.arange(1.0, 9.0)
+    np.testing.assert_array_equal(oracle.rope_row(x, 0.0, np.linspace(0.1, 1, 4)), x)
+    np.testing.assert_array_equal(oracle.rope_row(x, 37.0, np.zeros(4)), x)
+
+
+def test_rope_matches_complex_rotation_and_keeps_relative_positions():
+    d = 16
+    f = 10000.0 ** (-np.arange(d // 2) / (d // 2))
+    x = f64(rand_bits(78, (d,), "x"))
+    y = f64(rand_bits(78, (d,), "y"))
+    for pos in (0.0, 1.0, 17.0, 4093.0):
+        z = (x[: d // 2] + 1j * x[d // 2:]) * np.exp(1j * pos * f)  # numpy's own complex product
+        np.testing.assert_allclose(oracle.rope_row(x, pos, f), np.concatenate([z.real, z.imag]),
+                                   rtol=0, atol=1e-12)
+    # q(m).k(n) depends on m - n only
+    a = oracle.rope_row(x, 30.0, f) @ oracle.rope_row(y, 11.0, f)
+    b = oracle.rope_row(x, 519.0, f) @ oracle.rope_row(y, 500.0, f)
+    assert abs(a - b) < 1e-10
+
+
+def _quarter(bits_arr, pos):
+    """Exact RoPE with theta = pos * pi/2 on bf16 bits [..., d]: quarter turns of each
+    (i, i + d/2) pair, i.e. swaps and sign flips."""
+    x = bits_arr.copy()
+    h = x.shape[-1] // 2
+    a, b = x[..., :h].copy(), x[..., h:].copy()
+    for _ in range(int(pos) % 4):
+        a, b = b ^ np.uint16(0x8000), a  # (a, b) -> (-b, a)
+    x[..., :h], x[..., h:] = a, b
+    return x
+
+
+def test_decode_rope_equals_pre_rotated_inputs():
+    """With every inverse frequency pi/2 the rotations are exact quarter turns; decode with
+    RoPE (queries at q_pos, new keys at their positions) then equals plain decode on Q and
+    new K rotated by hand."""
+    b, hq, hkv, d, sa = 2, 4, 2, 8, 3
+    lens = [9, 14]
+    q = rand_bits(79, (b, hq, sa, d), "q")
+    cl = np.array(lens, np.int32)
+    fk, fv, _, _, _ = _flat_and_paged(80, b, hkv, d, lens, 8, False)
+    kn = np.stack([fk[i, :, n - sa:n] for i, n in enumerate(lens)])
+    vn = np.stack([fv[i, :, n - sa:n] for i, n in enumerate(lens)])
+    inv = np.full(d // 2, math.pi / 2)
+    o1, l1 = oracle.decode_ext(q, fk, fv, None, cl, 0.3, k_new=kn, v_new=vn, inv_freq=inv)
+    q2, fk2 = q.copy(), fk.copy()
+    for i, n in enumerate(lens):
+        for t in range(sa):
+            q2[i, :, t] = _quarter(q[i, :, t], n - sa + t)
+            fk2[i, :, n - sa + t] = _quarter(kn[i, :, t], n - sa + t)
+    o2, l2 = oracle.decode(q2, fk2, fv, None, cl, 0.3)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
