@@ -379,6 +379,20 @@ void oracle_rope_row(double *x, int d, double pos, const double *inv_freq)
     }
 }
 
+/* Round to the nearest bf16, ties to even (by way of binary32, whose rounding is the
+ * C conversion's round-to-nearest).  The rotated rows are bf16 operands of the product. */
+static double round_bf16(double v)
+{
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u) return (double)f; /* inf or NaN */
+    u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
 /* Decode with the options of the pages' decode kernel, on a bf16 cache:
  *   window > 0: new token t (q_pos = len - s_active + t) attends j iff
  *     q_pos - window + 1 <= j <= q_pos (the prefill window band, AGENTS "Sliding
@@ -391,7 +405,9 @@ void oracle_rope_row(double *x, int d, double pos, const double *inv_freq)
  *     (TKG "New-token K/V append": the product sees [cached prior | active]);
  *   inv_freq ([D/2], or NULL): RoPE of each query row at its q_pos and of each k_new
  *     row at its position (TKG "Algorithm", step 0; "GQA / MQA grouped-query broadcast":
- *     one rotation for the shared K head);
+ *     one rotation for the shared K head), each rotated row rounded to bf16: the rows
+ *     are the bf16 operands of the product, and the rotated K is what the cache stores
+ *     ("New-token K/V append": the persistent store of the RoPE'd K);
  *   sink ([HQ] or NULL): as oracle_decode_sink.
  * Other arguments and layouts as oracle_decode_sink. */
 int oracle_decode_ext(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -425,7 +441,10 @@ int oracle_decode_ext(const uint16_t *q, const uint16_t *k_cache, const uint16_t
                 const size_t r = (((size_t)b * HKV + g) * s_active + (size_t)t) * D;
                 widen(k_new + r, D, kd + j * D);
                 widen(v_new + r, D, vd + j * D);
-                if (inv_freq) oracle_rope_row(kd + j * D, D, (double)j, inv_freq);
+                if (inv_freq) {
+                    oracle_rope_row(kd + j * D, D, (double)j, inv_freq);
+                    for (int x = 0; x < D; ++x) kd[j * D + x] = round_bf16(kd[j * D + x]);
+                }
                 continue;
             }
             if (j < lo) { /* outside every window: never attended, never read */
@@ -448,7 +467,10 @@ int oracle_decode_ext(const uint16_t *q, const uint16_t *k_cache, const uint16_t
             const size_t r = (size_t)bh * s_active + t;
             const long qp = len - s_active + t;
             widen(q + r * D, D, qd);
-            if (inv_freq) oracle_rope_row(qd, D, (double)qp, inv_freq);
+            if (inv_freq) {
+                oracle_rope_row(qd, D, (double)qp, inv_freq);
+                for (int x = 0; x < D; ++x) qd[x] = round_bf16(qd[x]);
+            }
             rc = row_f64(qd, kd, vd, len, D, scale, qp, 1, window, sink ? sink[h] : -INFINITY,
                          o + r * D, lse + r, NULL);
         }

@@ -42,8 +42,10 @@ MUTANTS = {
                                  "(size_t)(circular ? j : j);"),
     "new_token_position_off_by_one": ("const long t = j - (len - s_active); /* >= 0: a new token */",
                                       "const long t = j - (len - s_active) - 1;"),
-    "rope_q_at_cache_len": ("if (inv_freq) oracle_rope_row(qd, D, (double)qp, inv_freq);",
-                            "if (inv_freq) oracle_rope_row(qd, D, (double)len, inv_freq);"),
+    "rope_q_at_cache_len": ("oracle_rope_row(qd, D, (double)qp, inv_freq);",
+                            "oracle_rope_row(qd, D, (double)len, inv_freq);"),
+    "rotated_rows_not_rounded": ("for (int x = 0; x < D; ++x) qd[x] = round_bf16(qd[x]);",
+                                 "for (int x = 0; x < D; ++x) qd[x] = qd[x];"),
 }
 
 

@@ -636,3 +636,31 @@ def test_decode_rope_equals_pre_rotated_inputs():
     o2, l2 = oracle.decode(q2, fk2, fv, None, cl, 0.3)
     np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+def test_decode_rope_rounds_the_rotated_rows_to_bf16():
+    """With a general frequency the rotated query and new-key rows are bf16 operands:
+    decode with RoPE equals plain decode on rows rotated (numpy's complex product) and
+    rounded to bf16 by the input module's own RNE rounding."""
+    b, hq, hkv, d, sa = 1, 2, 1, 16, 2
+    n = 11
+    q = rand_bits(81, (b, hq, sa, d), "q")
+    fk, fv, _, _, _ = _flat_and_paged(82, b, hkv, d, [n], 8, False)
+    kn, vn = fk[:, :, n - sa:n].copy(), fv[:, :, n - sa:n].copy()
+    f = 10000.0 ** (-np.arange(d // 2) / (d // 2))
+
+    def rot(bits_row, pos):
+        x = f64(bits_row)
+        z = (x[: d // 2] + 1j * x[d // 2:]) * np.exp(1j * pos * f)
+        return rng.f32_to_bf16_bits_np(np.concatenate([z.real, z.imag]).astype(np.float32))
+
+    o1, l1 = oracle.decode_ext(q, fk, fv, None, np.array([n], np.int32), 0.25, k_new=kn,
+                               v_new=vn, inv_freq=f)
+    q2, fk2 = q.copy(), fk.copy()
+    for t in range(sa):
+        for h in range(hq):
+            q2[0, h, t] = rot(q[0, h, t], n - sa + t)
+        fk2[0, 0, n - sa + t] = rot(kn[0, 0, t], n - sa + t)
+    o2, l2 = oracle.decode(q2, fk2, fv, None, np.array([n], np.int32), 0.25)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
