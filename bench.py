@@ -313,10 +313,13 @@ def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
             "pipelining": "2 buffer sets; per-input upload streams; download stream"}
 
 
-def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False, e4m3=False):
+def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False, e4m3=False,
+                 window=0, rope=False):
     """Time attn_fwd_decode on workload w (with sink=True: attn_fwd_decode_ex with the
     per-head sink logits of workloads.configs.sink_logits; with e4m3=True: attn_fwd_decode_ex
-    over the same caches rounded to FP8-e4m3, k_scale = v_scale = 1)."""
+    over the same caches rounded to FP8-e4m3, k_scale = v_scale = 1; window > 0 and rope:
+    attn_fwd_decode_ex with that window and RoPE of the queries, inverse frequencies
+    10000^(-2i/d))."""
     import torch
 
     import flash_attention_forward_attn_gb300 as A
@@ -329,11 +332,14 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False,
     lse = torch.empty(t["q"].shape[:3], dtype=torch.float32, device=dev)
     sk = torch.from_numpy(C.sink_logits(w.hq)).to(dev) if sink else None
     args = (t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["cache_len"])
+    inv = (torch.tensor([10000.0 ** (-2.0 * i / w.d) for i in range(w.d // 2)], dtype=torch.float32,
+                        device=dev) if rope else None)
 
     def step():
-        if sink or e4m3:
+        if sink or e4m3 or window or rope:
             A.attn_fwd_decode_ex(*args, max_cache_len=t["max_cache_len"], scale=w.scale, o=o,
-                                 lse=lse, sink=sk, workspace=ws, stream=stream)
+                                 lse=lse, sink=sk, window=window, rope_inv_freq=inv,
+                                 workspace=ws, stream=stream)
         else:
             A.attn_fwd_decode(*args, max_cache_len=t["max_cache_len"], scale=w.scale, o=o,
                               lse=lse, workspace=ws, stream=stream)
@@ -341,10 +347,12 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False,
     ms = time_steps(step, steps, warmup, flush, stream)
     assert A.attn_get_device_error(stream) == 0
     mean_ms = sum(ms) / len(ms)
-    nbytes = C.decode_io_bytes(w, t["lens"], kv_bytes=1 if e4m3 else 2)
+    nbytes = C.decode_io_bytes(w, t["lens"], kv_bytes=1 if e4m3 else 2, window=window) + (
+        w.d // 2 * 4 if rope else 0)
     value, slowest_s = aggregate_throughput(nbytes * steps, sum(ms) / 1e3, world, dev)
     achieved = nbytes / (mean_ms / 1e3) / 1e9
-    label = w.name + ("+sink" if sink else "") + ("+e4m3" if e4m3 else "")
+    label = (w.name + ("+sink" if sink else "") + ("+e4m3" if e4m3 else "") +
+             (f"+w{window}" if window else "") + ("+rope" if rope else ""))
     ent = {
         "workload": label, "value": value / 1e9, "unit": "GB/s", "ms_per_step": mean_ms,
         "ms_min": min(ms), "bytes_per_step": nbytes, "mean_cache_len": float(t["lens"].mean()),
@@ -460,6 +468,8 @@ def main():
                     help="with --workload: the _ex call with per-head attention-sink logits")
     ap.add_argument("--e4m3", action="store_true",
                     help="with a decode --workload: the caches rounded to FP8-e4m3")
+    ap.add_argument("--window", type=int, default=0, help="with a decode --workload: a window")
+    ap.add_argument("--rope", action="store_true", help="with a decode --workload: RoPE of Q")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -488,7 +498,7 @@ def main():
                                 sink=args.sink)
         else:
             ent = decode_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world,
-                               sink=args.sink, e4m3=args.e4m3)
+                               sink=args.sink, e4m3=args.e4m3, window=args.window, rope=args.rope)
         if rank == 0:
             print(json.dumps(ent), flush=True)
         return 0
@@ -521,6 +531,10 @@ def main():
                 ent = decode_entry(wx, dev, max(ext_steps, 50), args.warmup, flush, stream,
                                    peaks, world, e4m3=True)
                 extras[ent["workload"]] = ent
+            # a 4096-token window with RoPE of the queries (the pages' decode options)
+            ent = decode_entry(C.PAGED_DECODE_SPEC4, dev, max(ext_steps, 50), args.warmup, flush,
+                               stream, peaks, world, window=4096, rope=True)
+            extras[ent["workload"]] = ent
     clocks = clk.summary()
 
     cpu = None

@@ -48,7 +48,9 @@ ATTN_KV_BF16, ATTN_KV_E4M3 = 0, 1
 class AttnOpts(ctypes.Structure):
     """attn_opts of attn.h: optional features of the _ex calls."""
     _fields_ = [("sink", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
-                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("window", ctypes.c_int), ("circular", ctypes.c_int),
+                ("rope_inv_freq", ctypes.c_void_p)]
 
 
 def load_library(build_if_missing: bool = False):
@@ -80,6 +82,8 @@ def load_library(build_if_missing: bool = False):
         lib.attn_fwd_decode_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, I, I,
                                            O, P, S, P]
         lib.attn_fwd_decode_ex.restype = I
+        lib.attn_append_kv.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, O, P]
+        lib.attn_append_kv.restype = I
         lib.attn_fwd_decode_static_ws.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F,
                                                   P, P, I, I, P]
         lib.attn_fwd_decode_static_ws.restype = I
@@ -167,16 +171,24 @@ def _prefill_marshal(q, k, v, o, lse, o_dtype):
     return o, (b, hq, hkv, sq, skv, d)
 
 
-def _opts(sink, hq, device, kv_dtype=ATTN_KV_BF16, k_scale=1.0, v_scale=1.0):
-    """attn_opts for the _ex calls: sink is an fp32 tensor [hq] on the device, or None."""
+def _opts(sink, hq, device, kv_dtype=ATTN_KV_BF16, k_scale=1.0, v_scale=1.0, window=0,
+          circular=False, rope_inv_freq=None, d=None):
+    """attn_opts for the _ex calls: sink is an fp32 tensor [hq] on the device, or None;
+    rope_inv_freq an fp32 tensor [d/2] on the device, or None."""
     import torch
 
     if sink is not None:
         _req(sink, "sink", torch.float32, device)
         if tuple(sink.shape) != (hq,):
             raise ValueError("sink must hold one fp32 logit per query head: shape [hq]")
+    if rope_inv_freq is not None:
+        _req(rope_inv_freq, "rope_inv_freq", torch.float32, device)
+        if tuple(rope_inv_freq.shape) != (d // 2,):
+            raise ValueError("rope_inv_freq must be fp32 [d/2]")
     return AttnOpts(sink=None if sink is None else sink.data_ptr(), kv_dtype=kv_dtype,
-                    k_scale=float(k_scale), v_scale=float(v_scale))
+                    k_scale=float(k_scale), v_scale=float(v_scale), window=int(window),
+                    circular=int(bool(circular)),
+                    rope_inv_freq=None if rope_inv_freq is None else rope_inv_freq.data_ptr())
 
 
 def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
@@ -299,11 +311,14 @@ def _decode_workspace(workspace, b, hq, s_active, d, max_cache_len, kv_chunk, de
 def attn_fwd_decode_ex(q, k_cache, v_cache, block_table, cache_len, *, max_cache_len: int,
                        scale: float | None = None, o=None, lse=None, o_dtype=None,
                        kv_chunk: int = 0, sink=None, k_scale: float = 1.0, v_scale: float = 1.0,
+                       window: int = 0, circular: bool = False, rope_inv_freq=None,
                        workspace=None, stream=None):
     """attn_fwd_decode with the attn_opts options: sink, an fp32 [hq] tensor of
     per-query-head sink logits (scaled-score units) on q's device, or None; and an e4m3
     cache: k_cache and v_cache of dtype torch.float8_e4m3fn (or their bytes as uint8),
-    where element x stands for e4m3(x) * k_scale (K) or e4m3(x) * v_scale (V)."""
+    where element x stands for e4m3(x) * k_scale (K) or e4m3(x) * v_scale (V); a window;
+    a circular flat cache (max_cache_len rows, cache_len may exceed it); and RoPE of the
+    queries (rope_inv_freq fp32 [d/2])."""
     import torch
 
     lib = load_library()
@@ -312,7 +327,8 @@ def attn_fwd_decode_ex(q, k_cache, v_cache, block_table, cache_len, *, max_cache
         q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse, o_dtype,
         cache_dtype=k_cache.dtype if fp8 else None)
     workspace = _decode_workspace(workspace, b, hq, s_active, d, mcl, kv_chunk, q.device)
-    opts = _opts(sink, hq, q.device, ATTN_KV_E4M3 if fp8 else ATTN_KV_BF16, k_scale, v_scale)
+    opts = _opts(sink, hq, q.device, ATTN_KV_E4M3 if fp8 else ATTN_KV_BF16, k_scale, v_scale,
+                 window, circular, rope_inv_freq, d)
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     _check(lib.attn_fwd_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                   _ptr(cache_len), b, hq, hkv, d, s_active, page, max_pages,
@@ -320,6 +336,32 @@ def attn_fwd_decode_ex(q, k_cache, v_cache, block_table, cache_len, *, max_cache
                                   kv_chunk, ctypes.byref(opts), _ptr(workspace),
                                   workspace.numel(), _stream_ptr(stream)), "attn_fwd_decode_ex")
     return o, lse
+
+
+def attn_append_kv(k_new, v_new, k_cache, v_cache, block_table, cache_len, *,
+                   max_cache_len: int, circular: bool = False, rope_inv_freq=None, stream=None):
+    """Write the new tokens' K (RoPE'd with rope_inv_freq, if given) and V into a bf16 cache:
+    k_new, v_new bf16 [b, hkv, s_active, d]; token t at logical position
+    cache_len[b] - s_active + t.  Caches and block_table as for attn_fwd_decode."""
+    import torch
+
+    lib = load_library()
+    _req(k_new, "k_new", torch.bfloat16)
+    dev = k_new.device
+    _req(v_new, "v_new", torch.bfloat16, dev)
+    if k_new.dim() != 4 or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [b, hkv, s_active, d] with equal shapes")
+    b, hkv, s_active, d = k_new.shape
+    q_like = torch.empty((b, hkv, s_active, d), dtype=torch.bfloat16, device=dev)
+    _, (_, _, hkv2, _, _, page, max_pages, num_pages, mcl) = _decode_marshal(
+        q_like, k_cache, v_cache, block_table, cache_len, max_cache_len, None, None, None)
+    if hkv2 != hkv:
+        raise ValueError("k_new and the cache disagree on kv heads")
+    opts = _opts(None, hkv, dev, circular=circular, rope_inv_freq=rope_inv_freq, d=d)
+    _check(lib.attn_append_kv(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(block_table), _ptr(cache_len), b, hkv, d, s_active, page,
+                              max_pages, num_pages, mcl, ctypes.byref(opts), _stream_ptr(stream)),
+           "attn_append_kv")
 
 
 def attn_gen_mask_decode(cache_len, hq: int, s_active: int, max_len: int, mask=None,

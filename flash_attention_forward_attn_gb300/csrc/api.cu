@@ -68,6 +68,9 @@ struct Opts {
     const float* sink = nullptr;
     bool e4m3 = false;
     float k_scale = 1.f, v_scale = 1.f;
+    int window = 0;
+    bool circular = false;
+    const float* rope = nullptr;
 };
 
 bool read_opts(const attn_opts* opts, Opts* o) {
@@ -81,7 +84,18 @@ bool read_opts(const attn_opts* opts, Opts* o) {
         o->k_scale = opts->k_scale;
         o->v_scale = opts->v_scale;
     }
-    return true;
+    if (opts->window < 0 || (opts->circular != 0 && opts->circular != 1)) return false;
+    o->window = opts->window;
+    o->circular = opts->circular == 1;
+    o->rope = opts->rope_inv_freq;
+    return o->rope == nullptr || aligned4(o->rope);
+}
+
+// Paged-cache arguments shared by decode and append.
+bool paged_args_ok(int page_size, int num_pages, int max_pages_per_seq, int max_cache_len) {
+    if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return false;
+    if (num_pages <= 0 || max_pages_per_seq <= 0) return false;
+    return (long long)max_pages_per_seq * page_size >= max_cache_len;
 }
 
 bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
@@ -134,7 +148,9 @@ attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, voi
     if (window > 0 && !causal) return ATTN_ERR_UNSUPPORTED;  // the window is chained after causal
     Opts op;
     if (!read_opts(opts, &op)) return ATTN_ERR_INVALID_ARG;
-    if (op.e4m3) return ATTN_ERR_UNSUPPORTED;  // prefill reads bf16 K and V
+    // prefill reads bf16 K and V and takes its window as an argument; RoPE and a circular
+    // cache are decode options
+    if (op.e4m3 || op.window != 0 || op.circular || op.rope) return ATTN_ERR_UNSUPPORTED;
     if (sq == 0) return ATTN_OK;
     if (!q || !o || (skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o) || (skv > 0 && (!aligned16(k) || !aligned16(v))))
@@ -181,11 +197,13 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
     Opts op;
     if (!read_opts(opts, &op)) return ATTN_ERR_INVALID_ARG;
     if (op.e4m3 && d == 64) return ATTN_ERR_UNSUPPORTED;  // half a 128-byte box per row
+    // a circular cache is a flat ring that holds every new token's window
+    if (op.circular && (block_table || op.window == 0 ||
+                        (long long)op.window + s_active - 1 > max_cache_len || max_cache_len % 32 != 0))
+        return ATTN_ERR_INVALID_ARG;
     if (block_table) {
-        if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0)
+        if (!paged_args_ok(page_size, num_pages, max_pages_per_seq, max_cache_len))
             return ATTN_ERR_INVALID_ARG;
-        if (num_pages <= 0 || max_pages_per_seq <= 0) return ATTN_ERR_INVALID_ARG;
-        if ((long long)max_pages_per_seq * page_size < max_cache_len) return ATTN_ERR_INVALID_ARG;
         if ((long long)num_pages * hkv * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     } else if ((long long)b * hkv * max_cache_len > 0x7fffffffLL) {
         return ATTN_ERR_UNSUPPORTED;
@@ -222,6 +240,9 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
     a.kv_e4m3 = op.e4m3 ? 1 : 0;
     a.k_scale = op.k_scale;
     a.v_scale = op.v_scale;
+    a.window = op.window;
+    a.circular = op.circular ? 1 : 0;
+    a.rope_inv_freq = op.rope;
     return attn::decode_launch(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -234,6 +255,31 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
     return attn_fwd_decode_ex(q, k_cache, v_cache, block_table, cache_len, b, hq, hkv, d, s_active,
                               page_size, max_pages_per_seq, num_pages, max_cache_len, scale, o,
                               lse, o_dtype, kv_chunk, nullptr, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           const uint32_t* block_table, const int32_t* cache_len, int b, int hkv,
+                           int d, int s_active, int page_size, int max_pages_per_seq,
+                           int num_pages, int max_cache_len, const attn_opts* opts, void* stream) {
+    if (b <= 0 || hkv <= 0 || s_active <= 0 || max_cache_len <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!k_new || !v_new || !k_cache || !v_cache || !cache_len) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
+    Opts op;
+    if (!read_opts(opts, &op)) return ATTN_ERR_INVALID_ARG;
+    if (op.e4m3) return ATTN_ERR_UNSUPPORTED;  // the append writes bf16 caches
+    if (block_table) {
+        if (op.circular || !paged_args_ok(page_size, num_pages, max_pages_per_seq, max_cache_len))
+            return ATTN_ERR_INVALID_ARG;
+        if ((long long)num_pages * hkv * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    } else if ((long long)b * hkv * max_cache_len > 0x7fffffffLL) {
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    attn::AppendArgs a{k_new, v_new, k_cache, v_cache, block_table, cache_len, b, hkv, d,
+                       s_active, block_table ? page_size : 1, max_pages_per_seq, num_pages,
+                       max_cache_len, op.circular ? 1 : 0, op.rope};
+    return attn::append_launch(a, static_cast<cudaStream_t>(stream));
 }
 
 attn_status attn_gen_mask_decode(const int32_t* cache_len, int b, int hq, int s_active,

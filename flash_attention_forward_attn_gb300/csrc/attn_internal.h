@@ -49,6 +49,21 @@ struct DecodeArgs {
     const float* sink;    // [hq] sink logits, or NULL
     int kv_e4m3;          // the caches hold e4m3 bytes
     float k_scale, v_scale;  // their dequantisation scales (1 for bf16)
+    int window;           // decode window (0 = none)
+    int circular;         // flat cache used as a ring of max_cache_len rows
+    const float* rope_inv_freq;  // [d/2] RoPE inverse frequencies of Q, or NULL
+};
+
+// The new tokens' K/V written into a bf16 cache (attn_append_kv).
+struct AppendArgs {
+    const void* k_new;
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
+    const uint32_t* block_table;  // NULL for a flat cache
+    const int32_t* cache_len;
+    int b, hkv, d, s_active, page_size, max_pages_per_seq, num_pages, max_cache_len, circular;
+    const float* rope_inv_freq;  // [d/2], or NULL
 };
 
 // Tokens per split when the caller passes kv_chunk = 0: the largest power of two in
@@ -80,6 +95,7 @@ bool make_u8_map(CUtensorMap* map, const void* base, int rank, const uint64_t* d
 
 attn_status prefill_launch(const PrefillArgs& a, cudaStream_t stream);
 attn_status decode_launch(const DecodeArgs& a, cudaStream_t stream);
+attn_status append_launch(const AppendArgs& a, cudaStream_t stream);
 attn_status gen_mask_launch(const int32_t* cache_len, int b, int hq, int s_active, int max_len,
                             uint8_t* mask, cudaStream_t stream);
 

@@ -43,6 +43,52 @@ __device__ __forceinline__ bool decode_allowed(int j, int len, int s_active, int
     return j < len && j <= len - s_active + t;
 }
 
+// With a window W > 0 new token t also needs j >= q_pos - W + 1 (the prefill window band,
+// AGENTS "Sliding window"; TKG "gen_mask_tkg" type B is that band at the cache end).
+__device__ __forceinline__ bool decode_allowed_w(int j, int len, int s_active, int t, int window) {
+    return decode_allowed(j, len, s_active, t) && (window == 0 || j >= len - s_active + t - window + 1);
+}
+
+// Cache slots of a sequence and the first one any new token may read.  A flat or paged
+// cache keeps logical position j in slot j.  A circular flat cache of max_cache_len rows
+// keeps it in row j mod max_cache_len, so only min(len, max_cache_len) slots were ever
+// written and every one is read (the window covers nearly all of them).  Otherwise tiles
+// before the earliest window start are skipped (the start is rounded down to a 32-token tile).
+__device__ __forceinline__ int decode_nslots(int len, int circular, int max_cache_len) {
+    return circular ? min(len, max_cache_len) : len;
+}
+__device__ __forceinline__ int decode_first_slot(int len, int s_active, int window, int circular) {
+    return (window > 0 && !circular) ? (max(0, len - s_active - window + 1) & ~31) : 0;
+}
+
+// Logical position held by slot r of a circular cache of cap rows whose newest position
+// is len - 1 (r < min(len, cap)).
+__device__ __forceinline__ int circular_pos(int r, int len, int cap) {
+    return r + cap * ((len - 1 - r) / cap);
+}
+
+// RoPE of the element pairs (i, i + d/2) and (i + 1, i + 1 + d/2) held as bf16 pairs
+// lo = (x_i, x_i+1) and hi = (x_i+d/2, x_i+1+d/2), at position pos, half-split form
+// ("Flash-Attention: Decode (TKG)", "Algorithm", step 0): theta = pos * inv_freq[i],
+//   x_i' = x_i cos theta - x_{i+d/2} sin theta,  x_{i+d/2}' = x_{i+d/2} cos theta + x_i sin theta.
+// theta is formed and reduced modulo 2 pi in double, so large positions keep their accuracy.
+__device__ __forceinline__ void rope_sincos(int pos, float f, float& sn, float& cs) {
+    constexpr double kTwoPi = 6.283185307179586;
+    double th = (double)pos * (double)f;
+    th -= kTwoPi * rint(th / kTwoPi);
+    sincosf((float)th, &sn, &cs);
+}
+__device__ __forceinline__ void rope_bf16x2(uint32_t& lo, uint32_t& hi, int i, int pos,
+                                            const float* inv_freq) {
+    const float a0 = __uint_as_float(lo << 16), a1 = __uint_as_float(lo & 0xffff0000u);
+    const float b0 = __uint_as_float(hi << 16), b1 = __uint_as_float(hi & 0xffff0000u);
+    float s0, c0, s1, c1;
+    rope_sincos(pos, __ldg(inv_freq + i), s0, c0);
+    rope_sincos(pos, __ldg(inv_freq + i + 1), s1, c1);
+    lo = pack_bf16(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
+    hi = pack_bf16(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+}
+
 // A K (or V) tile of a slot is kBoxes column boxes of 32 rows x 128 bytes (64 bf16 or 128
 // e4m3 head dims per box), each written by TMA with the 128-byte swizzle.
 template <int D, bool kE4M3>
@@ -73,6 +119,8 @@ struct DecodeParams {
     float* part_ml;
     int hq, hkv, s_active, page_size, max_pages, num_pages, max_cache_len;
     int group, rows, chunk, max_splits, paged, box_rows;
+    int window, circular;    // decode window (0 = none); circular flat cache
+    const float* rope_inv_freq;  // [d/2] RoPE inverse frequencies of Q, or NULL
     float c;        // scale * log2(e) (* k_scale for an e4m3 cache)
     float v_scale;  // V dequantisation scale of an e4m3 cache (1 for bf16)
 };
@@ -107,13 +155,16 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = p.cache_len[b];
-    if (len < p.s_active || len > p.max_cache_len) {
+    if (len < p.s_active || (!p.circular && len > p.max_cache_len)) {
         if (threadIdx.x == 0 && split == 0 && g == 0) atomicOr(&g_decode_error, kDevErrCacheLen);
         return;
     }
-    const int tok0 = split * p.chunk;
-    if (tok0 >= len) return;  // this sequence is shorter than the split
-    const int tok1 = min(len, tok0 + p.chunk);
+    // this split covers cache slots [tok0, tok1); the combine skips the splits that return here
+    const int nslots = decode_nslots(len, p.circular, p.max_cache_len);
+    const int first = decode_first_slot(len, p.s_active, p.window, p.circular);
+    const int tok1 = min(nslots, (split + 1) * p.chunk);
+    const int tok0 = max(split * p.chunk, first);
+    if (tok0 >= tok1) return;  // the sequence is shorter than the split, or it precedes the window
     const int nblocks = (tok1 - tok0 + kBT - 1) / kBT;
 
     if (threadIdx.x == 0) {
@@ -146,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 rl[bx] = -1;
                 const int jb = tok0 + (i0 + lane) * kBT + bx * p.box_rows;
                 // a box wholly past the cache end is not read
-                if (bx >= nbox || i0 + lane >= nblocks || jb >= len) continue;
+                if (bx >= nbox || i0 + lane >= nblocks || jb >= nslots) continue;
                 if (p.paged) {
                     const uint32_t pg = __ldg(p.table + (size_t)b * p.max_pages + jb / p.page_size);
                     if (pg >= (uint32_t)p.num_pages) {
@@ -205,6 +256,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
         const int r0 = gq, r1 = gq + 8;
         const bool v0 = r0 < p.rows, v1 = r1 < p.rows;
         const int t0 = r0 % p.s_active, t1 = r1 % p.s_active;
+        const int qpos0 = len - p.s_active + t0, qpos1 = len - p.s_active + t1;  // RoPE positions
         const __nv_bfloat16* q0 = nullptr;
         const __nv_bfloat16* q1 = nullptr;
         if (v0) q0 = p.q + ((size_t)(b * p.hq + g * p.group + r0 / p.s_active) * p.s_active + t0) * D;
@@ -223,6 +275,19 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 const int c = ks * 16 + 4 * qd;
                 qa[ks] = v0 ? __ldg(reinterpret_cast<const uint2*>(q0 + c)) : make_uint2(0u, 0u);
                 qb[ks] = v1 ? __ldg(reinterpret_cast<const uint2*>(q1 + c)) : make_uint2(0u, 0u);
+            }
+            if (p.rope_inv_freq != nullptr) {  // element i of k-step ks pairs with k-step ks + D/32
+#pragma unroll
+                for (int ks = 0; ks < D / 32; ++ks) {
+                    const int c = ks * 16 + 4 * qd;
+                    rope_bf16x2(qa[ks].x, qa[ks + D / 32].x, c, qpos0, p.rope_inv_freq);
+                    rope_bf16x2(qa[ks].y, qa[ks + D / 32].y, c + 2, qpos0, p.rope_inv_freq);
+                    rope_bf16x2(qb[ks].x, qb[ks + D / 32].x, c, qpos1, p.rope_inv_freq);
+                    rope_bf16x2(qb[ks].y, qb[ks + D / 32].y, c + 2, qpos1, p.rope_inv_freq);
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
                 const uint32_t wa[2] = {qa[ks].x, qa[ks].y}, wb[2] = {qb[ks].x, qb[ks].y};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
@@ -268,6 +333,16 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 qf[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c + 8)) : 0u;
                 qf[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c + 8)) : 0u;
             }
+            if (p.rope_inv_freq != nullptr) {  // element i of k-step ks pairs with k-step ks + D/32
+#pragma unroll
+                for (int ks = 0; ks < D / 32; ++ks) {
+                    const int c = ks * 16 + 2 * qd;
+                    rope_bf16x2(qf[ks][0], qf[ks + D / 32][0], c, qpos0, p.rope_inv_freq);
+                    rope_bf16x2(qf[ks][2], qf[ks + D / 32][2], c + 8, qpos0, p.rope_inv_freq);
+                    rope_bf16x2(qf[ks][1], qf[ks + D / 32][1], c, qpos1, p.rope_inv_freq);
+                    rope_bf16x2(qf[ks][3], qf[ks + D / 32][3], c + 8, qpos1, p.rope_inv_freq);
+                }
+            }
         }
         float o[D / 8][4];
 #pragma unroll
@@ -311,8 +386,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                     }
                 }
             }
-            const int j0 = tok0 + i * kBT;
-            const bool edge = j0 + kBT > len - p.s_active;  // touches the new tokens or the end
+            const int j0 = tok0 + i * kBT;  // first slot of the tile
+            // tiles that touch the new tokens, the cache end or a window start are masked;
+            // every tile of a circular cache is (its slots hold positions of two laps)
+            const bool edge = p.circular || j0 + kBT > len - p.s_active ||
+                              (p.window > 0 && j0 < len - p.window);
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
@@ -320,9 +398,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 for (int e = 0; e < 2; ++e) {
                     float x0 = sc[nt][e] * c_row0, x1 = sc[nt][2 + e] * c_row1;
                     if (edge) {
-                        const int j = j0 + nt * 8 + 2 * qd + e;
-                        if (!(v0 && decode_allowed(j, len, p.s_active, t0))) x0 = -INFINITY;
-                        if (!(v1 && decode_allowed(j, len, p.s_active, t1))) x1 = -INFINITY;
+                        const int r = j0 + nt * 8 + 2 * qd + e;  // slot
+                        const int j = p.circular ? circular_pos(r, len, p.max_cache_len) : r;
+                        const bool in = r < nslots;
+                        if (!(v0 && in && decode_allowed_w(j, len, p.s_active, t0, p.window))) x0 = -INFINITY;
+                        if (!(v1 && in && decode_allowed_w(j, len, p.s_active, t1, p.window))) x1 = -INFINITY;
                     }
                     sc[nt][e] = x0;
                     sc[nt][2 + e] = x1;
@@ -365,8 +445,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
                 if (edge) {  // zero V rows of slots past the cache end (they may hold NaN)
                     const int jl = j0 + ks * 16 + 2 * qd;
-                    keep_lo = (jl < len ? 0x0000ffffu : 0u) | (jl + 1 < len ? 0xffff0000u : 0u);
-                    keep_hi = (jl + 8 < len ? 0x0000ffffu : 0u) | (jl + 9 < len ? 0xffff0000u : 0u);
+                    keep_lo = (jl < nslots ? 0x0000ffffu : 0u) | (jl + 1 < nslots ? 0xffff0000u : 0u);
+                    keep_hi = (jl + 8 < nslots ? 0x0000ffffu : 0u) | (jl + 9 < nslots ? 0xffff0000u : 0u);
                 }
                 uint32_t pa[4];
                 if constexpr (kE4M3) {
@@ -508,21 +588,24 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __rest
                                                            const float* __restrict__ sink,
                                                            OutT* __restrict__ o, float* lse,
                                                            int hq, int s_active, int chunk,
-                                                           int max_splits, int max_cache_len) {
+                                                           int max_splits, int max_cache_len,
+                                                           int window, int circular) {
     const size_t rowid = blockIdx.x;
     const int b = (int)(rowid / ((size_t)hq * s_active));
     const int x = threadIdx.x;
     const int len = cache_len[b];
     float out = 0.f, lse_v = -INFINITY;
-    if (len >= s_active && len <= max_cache_len) {
-        const int ns = (len + chunk - 1) / chunk;
+    if (len >= s_active && (circular || len <= max_cache_len)) {
+        // the splits that ran: those with a slot in [first, nslots) (as decode_split_kernel)
+        const int s0 = decode_first_slot(len, s_active, window, circular) / chunk;
+        const int ns = (decode_nslots(len, circular, max_cache_len) + chunk - 1) / chunk;
         const float* ml = part_ml + rowid * max_splits * 2;
         float M = -INFINITY;
-        for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
+        for (int s = s0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
         if (M != -INFINITY) {
             float Lsum = 0.f, acc = 0.f;
             const float* po = part_o + rowid * max_splits * D + x;
-            for (int s = 0; s < ns; ++s) {
+            for (int s = s0; s < ns; ++s) {
                 const float wt = ex2(ml[2 * s] - M);
                 Lsum += wt * ml[2 * s + 1];
                 acc += wt * po[(size_t)s * D];
@@ -545,6 +628,50 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __rest
     else
         o[rowid * D + x] = out;
     if (lse != nullptr && x == 0) lse[rowid] = lse_v;
+}
+
+// The new tokens' K and V written into a bf16 cache ("Flash-Attention: Decode (TKG)",
+// "New-token K/V append": the persistent store of the RoPE'd K).  One CTA per (new token,
+// kv head, sequence), thread i handles head dims i and i + d/2: new token t sits at logical
+// position len - s_active + t, which is its RoPE position (inv_freq != NULL) and its cache
+// slot (through the block table, or row j mod max_cache_len of a circular flat cache).
+__global__ void append_kv_kernel(const __nv_bfloat16* __restrict__ k_new,
+                                 const __nv_bfloat16* __restrict__ v_new,
+                                 __nv_bfloat16* __restrict__ k_cache,
+                                 __nv_bfloat16* __restrict__ v_cache, AppendArgs a) {
+    const int t = blockIdx.x, g = blockIdx.y, b = blockIdx.z, i = threadIdx.x;
+    const int h = a.d / 2;
+    const int len = a.cache_len[b];
+    if (len < a.s_active || (!a.circular && len > a.max_cache_len)) {
+        if (i == 0 && t == 0 && g == 0) atomicOr(&g_decode_error, kDevErrCacheLen);
+        return;
+    }
+    const int j = len - a.s_active + t;
+    size_t row;
+    if (a.block_table != nullptr) {
+        const uint32_t pg = __ldg(a.block_table + (size_t)b * a.max_pages_per_seq + j / a.page_size);
+        if (pg >= (uint32_t)a.num_pages) {
+            if (i == 0) atomicOr(&g_decode_error, kDevErrPageOOB);
+            return;  // never write an out-of-range page
+        }
+        row = ((size_t)pg * a.hkv + g) * a.page_size + (size_t)(j % a.page_size);
+    } else {
+        row = ((size_t)b * a.hkv + g) * (size_t)a.max_cache_len +
+              (size_t)(a.circular ? j % a.max_cache_len : j);
+    }
+    const size_t src = (((size_t)b * a.hkv + g) * a.s_active + t) * a.d;
+    float k0 = __bfloat162float(k_new[src + i]), k1 = __bfloat162float(k_new[src + i + h]);
+    if (a.rope_inv_freq != nullptr) {
+        float sn, cs;
+        rope_sincos(j, __ldg(a.rope_inv_freq + i), sn, cs);
+        const float r0 = k0 * cs - k1 * sn, r1 = k1 * cs + k0 * sn;
+        k0 = r0;
+        k1 = r1;
+    }
+    k_cache[row * a.d + i] = __float2bfloat16_rn(k0);
+    k_cache[row * a.d + i + h] = __float2bfloat16_rn(k1);
+    v_cache[row * a.d + i] = v_new[src + i];
+    v_cache[row * a.d + i + h] = v_new[src + i + h];
 }
 
 // The 0/1 decode mask, one byte per (sequence, head, new token, cache position).
@@ -602,6 +729,9 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     p.box_rows = box_rows;
     p.c = kE4M3 ? a.scale * a.k_scale * kLog2e : a.scale * kLog2e;
     p.v_scale = kE4M3 ? a.v_scale : 1.0f;
+    p.window = a.window;
+    p.circular = a.circular;
+    p.rope_inv_freq = a.rope_inv_freq;
 
     static bool attr_set = false;  // benign race: every thread sets the same value
     if (!attr_set) {
@@ -619,11 +749,11 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     if (a.o_dtype == ATTN_BF16)
         decode_combine_kernel<D, __nv_bfloat16><<<nrows, D, 0, stream>>>(
             a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<__nv_bfloat16*>(a.o), a.lse, a.hq,
-            a.s_active, a.kv_chunk, a.max_splits, a.max_cache_len);
+            a.s_active, a.kv_chunk, a.max_splits, a.max_cache_len, a.window, a.circular);
     else
         decode_combine_kernel<D, float><<<nrows, D, 0, stream>>>(
             a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<float*>(a.o), a.lse, a.hq, a.s_active,
-            a.kv_chunk, a.max_splits, a.max_cache_len);
+            a.kv_chunk, a.max_splits, a.max_cache_len, a.window, a.circular);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
@@ -644,6 +774,15 @@ attn_status decode_launch(const DecodeArgs& a, cudaStream_t stream) {
         case 256: return decode_launch_d<256, false>(a, stream);
         default: return ATTN_ERR_UNSUPPORTED;
     }
+}
+
+attn_status append_launch(const AppendArgs& a, cudaStream_t stream) {
+    dim3 grid(a.s_active, a.hkv, a.b);
+    append_kv_kernel<<<grid, a.d / 2, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.k_new), static_cast<const __nv_bfloat16*>(a.v_new),
+        static_cast<__nv_bfloat16*>(a.k_cache), static_cast<__nv_bfloat16*>(a.v_cache), a);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 attn_status gen_mask_launch(const int32_t* cache_len, int b, int hq, int s_active, int max_len,

@@ -78,12 +78,37 @@ typedef enum { ATTN_KV_BF16 = 0, ATTN_KV_E4M3 = 1 } attn_kv_dtype;
  *          e4m3(x) * k_scale and of V for e4m3(x) * v_scale; both scales must be finite.
  *          With an e4m3 cache d must be 128 or 256.  Slots past cache_len may hold any
  *          byte, NaN codes included; they contribute exactly zero.
+ *
+ *   window : decode only (prefill has its own window argument).  window > 0 gives new
+ *          token t (q_pos = cache_len - s_active + t) the keys j with
+ *          q_pos - window + 1 <= j <= q_pos: the prefill window band (AGENTS.md "Sliding
+ *          window"; "Flash-Attention: Decode (TKG)", "gen_mask_tkg" type B is that band
+ *          at the cache end).  Tiles wholly before every new token's window are not read,
+ *          so block-table entries for them may hold anything.  0 = no window.
+ *   circular : decode and attn_append_kv, flat caches only.  The flat cache is a ring of
+ *          max_cache_len rows: logical position j lives in row j mod max_cache_len, so
+ *          cache_len may exceed max_cache_len (type B's wrapped case).  Decode then needs
+ *          window > 0, window + s_active - 1 <= max_cache_len (the band fits in the
+ *          ring) and max_cache_len a multiple of 32.
+ *   rope_inv_freq : a DEVICE fp32 array [d/2] or NULL.  Decode rotates each query row by
+ *          rotary position embedding at its q_pos before the product, and attn_append_kv
+ *          rotates each new K row at its position ("Flash-Attention: Decode (TKG)",
+ *          "Algorithm", step 0; "New-token K/V append"), in half-split form: for i < d/2,
+ *          theta = pos * rope_inv_freq[i],
+ *            x'[i] = x[i] cos theta - x[i + d/2] sin theta,
+ *            x'[i + d/2] = x[i + d/2] cos theta + x[i] sin theta.
+ *          Keys already in the cache are used as stored (rotated when they were
+ *          appended).  The rotated query is rounded to bf16 before the product.  Must be
+ *          4-byte aligned.
  */
 typedef struct {
     const float* sink;
     int kv_dtype;
     float k_scale;
     float v_scale;
+    int window;
+    int circular;
+    const float* rope_inv_freq;
 } attn_opts;
 
 /*
@@ -185,9 +210,11 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
 /*
  * attn_fwd_decode_ex -- attn_fwd_decode with the options of attn_opts (NULL = none):
  * same arguments (opts sits after kv_chunk), layouts, workspace, semantics and errors,
- * plus ATTN_ERR_INVALID_ARG for an invalid option (a misaligned sink pointer, an unknown
- * kv_dtype, a non-finite scale of an e4m3 cache) and ATTN_ERR_UNSUPPORTED for an e4m3
- * cache with d = 64.  The sink is applied where the split-KV chunks are merged and the
+ * plus ATTN_ERR_INVALID_ARG for an invalid option (a misaligned sink or rope_inv_freq
+ * pointer, an unknown kv_dtype, a non-finite scale of an e4m3 cache, a negative window, a
+ * circular paged cache or a circular cache whose window does not fit) and
+ * ATTN_ERR_UNSUPPORTED for an e4m3 cache with d = 64.  With circular, cache_len[b] may
+ * exceed max_cache_len.  The sink is applied where the split-KV chunks are merged and the
  * scales are folded into the chunk pass, so the workspace size is the same for every
  * option.
  */
@@ -198,6 +225,27 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
                                float scale, void* o, float* lse, attn_dtype o_dtype, int kv_chunk,
                                const attn_opts* opts, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/*
+ * attn_append_kv -- write the new tokens' K and V into a bf16 cache ("Flash-Attention:
+ * Decode (TKG)", "New-token K/V append": the kernel's persistent store of the new K).
+ * New token t of sequence b goes to logical position cache_len[b] - s_active + t (cache_len
+ * already counts the new tokens, as for attn_fwd_decode), through the block table or, for
+ * a flat cache, at row j (row j mod max_cache_len with opts->circular).  With
+ * opts->rope_inv_freq its K row is rotated at position j first (see attn_opts) and rounded
+ * to bf16; V is copied as is.  Other options are ignored.
+ *
+ * Layouts: k_new, v_new bf16 [b, hkv, s_active, d]; caches and block_table as for
+ *   attn_fwd_decode (bf16 only).  Only the new tokens' cache rows are written.
+ * Sizes: as attn_fwd_decode, d in {64, 128, 256}; circular only with a flat cache.
+ * Errors: INVALID_ARG / UNSUPPORTED before launch; CUDA on launch failure; a block-table
+ *   entry >= num_pages (that row is not written) or a cache_len outside its range is
+ *   reported by attn_get_device_error().
+ */
+attn_status attn_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           const uint32_t* block_table, const int32_t* cache_len, int b, int hkv,
+                           int d, int s_active, int page_size, int max_pages_per_seq,
+                           int num_pages, int max_cache_len, const attn_opts* opts, void* stream);
 
 /*
  * attn_fwd_decode_static_ws -- attn_fwd_decode for callers that cannot allocate device

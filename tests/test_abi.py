@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     assert declared_symbols() == sorted([
         "attn_fwd_prefill", "attn_decode_workspace_bytes", "attn_fwd_decode",
         "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
-        "attn_fwd_decode_static_ws", "attn_fwd_prefill_ex", "attn_fwd_decode_ex"])
+        "attn_fwd_decode_static_ws", "attn_fwd_prefill_ex", "attn_fwd_decode_ex",
+        "attn_append_kv"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -110,6 +111,17 @@ def test_ex_calls_check_their_options_before_launch(lib):
     d64 = dargs[:8] + (64,) + dargs[9:]
     assert lib.attn_fwd_decode_ex(*d64, ctypes.byref(e4()), FAKE, 1 << 30, None) == 2
     assert lib.attn_fwd_prefill_ex(*args, ctypes.byref(e4()), None) == 2  # prefill reads bf16
+    op = lambda **kw: ctypes.byref(A.AttnOpts(**kw))
+    call = lambda a, o: lib.attn_fwd_decode_ex(*a, o, FAKE, 1 << 30, None)
+    flat = dargs[:3] + (None,) + dargs[4:]  # no block table
+    assert call(dargs, op(window=-1)) == 1
+    assert call(dargs, op(window=8, circular=1)) == 1  # a paged cache cannot be circular
+    assert call(flat, op(circular=1)) == 1  # circular needs a window
+    assert call(flat, op(window=126, circular=1)) == 1  # 126 + 4 - 1 > 128 rows
+    assert call(flat, op(window=8, circular=2)) == 1
+    assert call(dargs, op(rope_inv_freq=(1 << 20) + 2)) == 1  # misaligned
+    for kw in (dict(window=4), dict(circular=1), dict(rope_inv_freq=1 << 20)):
+        assert lib.attn_fwd_prefill_ex(*args, op(**kw), None) == 2  # decode options
     # an invalid size is still reported first, with or without options
     dbad = dargs[:8] + (80,) + dargs[9:]  # d = 80
     assert lib.attn_fwd_decode_ex(*dbad, ctypes.byref(none), FAKE, 1 << 30, None) == 2
@@ -156,3 +168,22 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
         A.load_library()
     monkeypatch.setattr(A, "_lib", None)
     importlib.reload(_build)
+
+
+def test_append_rejects_before_launch(lib):
+    def app(**kw):
+        a = dict(kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, table=FAKE, cl=FAKE, b=2, hkv=2, d=128, sa=4,
+                 page=32, maxp=4, npages=8, maxlen=128, opts=None)
+        a.update(kw)
+        return lib.attn_append_kv(a["kn"], a["vn"], a["k"], a["v"], a["table"], a["cl"], a["b"],
+                                  a["hkv"], a["d"], a["sa"], a["page"], a["maxp"], a["npages"],
+                                  a["maxlen"], a["opts"], None)
+    assert app(b=0) == 1
+    assert app(kn=None) == 1
+    assert app(cl=None) == 1
+    assert app(d=96) == 2
+    assert app(page=24) == 1
+    assert app(maxp=3) == 1
+    assert app(opts=ctypes.byref(A.AttnOpts(circular=1))) == 1  # a paged cache cannot be circular
+    assert app(opts=ctypes.byref(A.AttnOpts(kv_dtype=1, k_scale=1.0, v_scale=1.0))) == 2
+    assert app(v=ctypes.c_void_p((1 << 20) + 8)) == 1

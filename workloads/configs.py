@@ -336,12 +336,15 @@ def decode_inputs_e4m3_torch(w: DecodeWorkload, device, permute: bool = True):
     return t
 
 
-def decode_io_bytes(w: DecodeWorkload, lens: np.ndarray, kv_bytes: int = 2) -> int:
+def decode_io_bytes(w: DecodeWorkload, lens: np.ndarray, kv_bytes: int = 2, window: int = 0) -> int:
     """Algorithmic HBM bytes of one decode call: each needed K/V byte once (kv_bytes per
-    element: 2 for bf16, 1 for e4m3), the page table entries in use, cache_len, Q and O
-    (bf16) and LSE."""
-    kv = int(lens.astype(np.int64).sum()) * w.hkv * w.d * kv_bytes * 2
-    pages = int((-(-lens.astype(np.int64) // w.page_size)).sum()) * 4 if w.paged else 0
+    element: 2 for bf16, 1 for e4m3; with a window only the window + s_active - 1 newest
+    positions are needed), the page table entries in use, cache_len, Q and O (bf16) and LSE."""
+    lens = lens.astype(np.int64)
+    need = np.minimum(lens, window + w.s_active - 1) if window > 0 else lens
+    kv = int(need.sum()) * w.hkv * w.d * kv_bytes * 2
+    first = lens - need  # the oldest needed position
+    pages = int((-(-lens // w.page_size) - first // w.page_size).sum()) * 4 if w.paged else 0
     qo = 2 * w.b * w.hq * w.s_active * w.d * 2
     lse = w.b * w.hq * w.s_active * 4
     return kv + pages + w.b * 4 + qo + lse
