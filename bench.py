@@ -314,7 +314,7 @@ def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
 
 
 def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False, e4m3=False,
-                 window=0, rope=False):
+                 window=0, rope=False, kv_chunk=0):
     """Time attn_fwd_decode on workload w (with sink=True: attn_fwd_decode_ex with the
     per-head sink logits of workloads.configs.sink_logits; with e4m3=True: attn_fwd_decode_ex
     over the same caches rounded to FP8-e4m3, k_scale = v_scale = 1; window > 0 and rope:
@@ -326,8 +326,8 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False,
     from workloads import configs as C
 
     t = C.decode_inputs_e4m3_torch(w, dev) if e4m3 else C.decode_inputs_torch(w, dev)
-    ws = torch.empty(A.attn_decode_workspace_bytes(w.b, w.hq, w.s_active, w.d, t["max_cache_len"]),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.empty(A.attn_decode_workspace_bytes(w.b, w.hq, w.s_active, w.d, t["max_cache_len"],
+                                                   kv_chunk), dtype=torch.uint8, device=dev)
     o = torch.empty(t["q"].shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(t["q"].shape[:3], dtype=torch.float32, device=dev)
     sk = torch.from_numpy(C.sink_logits(w.hq)).to(dev) if sink else None
@@ -339,10 +339,10 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False,
         if sink or e4m3 or window or rope:
             A.attn_fwd_decode_ex(*args, max_cache_len=t["max_cache_len"], scale=w.scale, o=o,
                                  lse=lse, sink=sk, window=window, rope_inv_freq=inv,
-                                 workspace=ws, stream=stream)
+                                 kv_chunk=kv_chunk, workspace=ws, stream=stream)
         else:
             A.attn_fwd_decode(*args, max_cache_len=t["max_cache_len"], scale=w.scale, o=o,
-                              lse=lse, workspace=ws, stream=stream)
+                              lse=lse, kv_chunk=kv_chunk, workspace=ws, stream=stream)
 
     ms = time_steps(step, steps, warmup, flush, stream)
     assert A.attn_get_device_error(stream) == 0
@@ -470,6 +470,7 @@ def main():
                     help="with a decode --workload: the caches rounded to FP8-e4m3")
     ap.add_argument("--window", type=int, default=0, help="with a decode --workload: a window")
     ap.add_argument("--rope", action="store_true", help="with a decode --workload: RoPE of Q")
+    ap.add_argument("--kv-chunk", type=int, default=0, help="with a decode --workload: split length")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -498,7 +499,8 @@ def main():
                                 sink=args.sink)
         else:
             ent = decode_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world,
-                               sink=args.sink, e4m3=args.e4m3, window=args.window, rope=args.rope)
+                               sink=args.sink, e4m3=args.e4m3, window=args.window, rope=args.rope,
+                               kv_chunk=args.kv_chunk)
         if rank == 0:
             print(json.dumps(ent), flush=True)
         return 0

@@ -71,22 +71,53 @@ __device__ __forceinline__ int circular_pos(int r, int len, int cap) {
 // lo = (x_i, x_i+1) and hi = (x_i+d/2, x_i+1+d/2), at position pos, half-split form
 // ("Flash-Attention: Decode (TKG)", "Algorithm", step 0): theta = pos * inv_freq[i],
 //   x_i' = x_i cos theta - x_{i+d/2} sin theta,  x_{i+d/2}' = x_{i+d/2} cos theta + x_i sin theta.
-// theta is formed and reduced modulo 2 pi in double, so large positions keep their accuracy.
+// theta is reduced modulo 2 pi in fp32 by Cody and Waite's additive reduction: pos * f
+// is held exactly as hi + lo (an FMA gives the product's rounding error; pos < 2^24 is
+// exact in fp32), and 2 pi is taken off k times in two pieces, the first with 8
+// significant bits so that k * piece is exact while |k| < 2^16.  The error stays near
+// 1e-5 rad.  Larger angles (beyond 2^18 rad, rare) are reduced in double.
 __device__ __forceinline__ void rope_sincos(int pos, float f, float& sn, float& cs) {
+    const float x = (float)pos;
+    const float hi = x * f;
+    if (fabsf(hi) < 262144.f && pos < (1 << 24)) {
+        const float lo = fmaf(x, f, -hi);
+        constexpr float kInvTwoPi = 0.15915494309189535f;
+        constexpr float kC1 = 6.28125f;               // 201 / 32
+        constexpr float kC2 = 1.9353071795864769e-3f;  // 2 pi - kC1
+        const float k = rintf(hi * kInvTwoPi);
+        const float r = (fmaf(-k, kC1, hi) - k * kC2) + lo;
+        sincosf(r, &sn, &cs);
+        return;
+    }
     constexpr double kTwoPi = 6.283185307179586;
     double th = (double)pos * (double)f;
-    th -= kTwoPi * rint(th / kTwoPi);
+    th -= kTwoPi * rint(th * (1.0 / kTwoPi));
     sincosf((float)th, &sn, &cs);
 }
-__device__ __forceinline__ void rope_bf16x2(uint32_t& lo, uint32_t& hi, int i, int pos,
-                                            const float* inv_freq) {
+// The rotation of two pairs by the angles (s0, c0) and (s1, c1).
+__device__ __forceinline__ void rope_apply(uint32_t& lo, uint32_t& hi, float s0, float c0,
+                                           float s1, float c1) {
     const float a0 = __uint_as_float(lo << 16), a1 = __uint_as_float(lo & 0xffff0000u);
     const float b0 = __uint_as_float(hi << 16), b1 = __uint_as_float(hi & 0xffff0000u);
-    float s0, c0, s1, c1;
-    rope_sincos(pos, __ldg(inv_freq + i), s0, c0);
-    rope_sincos(pos, __ldg(inv_freq + i + 1), s1, c1);
     lo = pack_bf16(a0 * c0 - b0 * s0, a1 * c1 - b1 * s1);
     hi = pack_bf16(b0 * c0 + a0 * s0, b1 * c1 + a1 * s1);
+}
+
+// Rows a (position pa) and b (position pb) of a lane, elements i and i + 1 of each:
+// the angles are computed once when the two rows share a position.
+__device__ __forceinline__ void rope_rows(uint32_t& alo, uint32_t& ahi, uint32_t& blo,
+                                          uint32_t& bhi, int i, int pa, int pb,
+                                          const float* inv_freq) {
+    const float f0 = __ldg(inv_freq + i), f1 = __ldg(inv_freq + i + 1);
+    float s0, c0, s1, c1;
+    rope_sincos(pa, f0, s0, c0);
+    rope_sincos(pa, f1, s1, c1);
+    rope_apply(alo, ahi, s0, c0, s1, c1);
+    if (pb != pa) {
+        rope_sincos(pb, f0, s0, c0);
+        rope_sincos(pb, f1, s1, c1);
+    }
+    rope_apply(blo, bhi, s0, c0, s1, c1);
 }
 
 // A K (or V) tile of a slot is kBoxes column boxes of 32 rows x 128 bytes (64 bf16 or 128
@@ -280,10 +311,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
 #pragma unroll
                 for (int ks = 0; ks < D / 32; ++ks) {
                     const int c = ks * 16 + 4 * qd;
-                    rope_bf16x2(qa[ks].x, qa[ks + D / 32].x, c, qpos0, p.rope_inv_freq);
-                    rope_bf16x2(qa[ks].y, qa[ks + D / 32].y, c + 2, qpos0, p.rope_inv_freq);
-                    rope_bf16x2(qb[ks].x, qb[ks + D / 32].x, c, qpos1, p.rope_inv_freq);
-                    rope_bf16x2(qb[ks].y, qb[ks + D / 32].y, c + 2, qpos1, p.rope_inv_freq);
+                    rope_rows(qa[ks].x, qa[ks + D / 32].x, qb[ks].x, qb[ks + D / 32].x, c, qpos0,
+                              qpos1, p.rope_inv_freq);
+                    rope_rows(qa[ks].y, qa[ks + D / 32].y, qb[ks].y, qb[ks + D / 32].y, c + 2,
+                              qpos0, qpos1, p.rope_inv_freq);
                 }
             }
 #pragma unroll
@@ -337,10 +368,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
 #pragma unroll
                 for (int ks = 0; ks < D / 32; ++ks) {
                     const int c = ks * 16 + 2 * qd;
-                    rope_bf16x2(qf[ks][0], qf[ks + D / 32][0], c, qpos0, p.rope_inv_freq);
-                    rope_bf16x2(qf[ks][2], qf[ks + D / 32][2], c + 8, qpos0, p.rope_inv_freq);
-                    rope_bf16x2(qf[ks][1], qf[ks + D / 32][1], c, qpos1, p.rope_inv_freq);
-                    rope_bf16x2(qf[ks][3], qf[ks + D / 32][3], c + 8, qpos1, p.rope_inv_freq);
+                    rope_rows(qf[ks][0], qf[ks + D / 32][0], qf[ks][1], qf[ks + D / 32][1], c,
+                              qpos0, qpos1, p.rope_inv_freq);
+                    rope_rows(qf[ks][2], qf[ks + D / 32][2], qf[ks][3], qf[ks + D / 32][3], c + 8,
+                              qpos0, qpos1, p.rope_inv_freq);
                 }
             }
         }
