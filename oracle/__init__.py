@@ -66,6 +66,8 @@ def _load():
             lib.oracle_prefill.restype = I
             lib.oracle_prefill_sink.argtypes = [P, P, P, I, I, I, L, L, I, D, I, L, P, L, L, P, P]
             lib.oracle_prefill_sink.restype = I
+            lib.oracle_prefill_varlen.argtypes = [P, P, P, I, I, I, P, P, I, D, I, L, P, L, L, P, P]
+            lib.oracle_prefill_varlen.restype = I
             lib.oracle_gather_paged.argtypes = [P, P, L, I, I, I, I, L, P]
             lib.oracle_gather_paged.restype = I
             lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, D, L, L, P, P]
@@ -174,6 +176,31 @@ def prefill(q, k, v, scale, causal, window, threads=None, sink=None):
 
     with ThreadPoolExecutor(max_workers=min(threads or default_threads(), nbh)) as ex:
         for rc in ex.map(run, range(nbh)):
+            _check(rc)
+    return o, lse
+
+
+def prefill_varlen(q, k, v, cu_q, cu_k, scale, causal, window, sink=None, threads=None):
+    """Packed prefill.  q [HQ,SQ,D], k/v [HKV,SKV,D] bf16 bits; cu_q, cu_k int32 [nseq+1]
+    sequence offsets along SQ and SKV -> (o [HQ,SQ,D] f64, lse [HQ,SQ] f64)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    HQ, SQ, D = q.shape
+    HKV, SKV, _ = k.shape
+    cq = np.ascontiguousarray(cu_q, dtype=np.int32)
+    ck = np.ascontiguousarray(cu_k, dtype=np.int32)
+    assert cq.shape == ck.shape and cq[-1] == SQ and ck[-1] == SKV
+    sk = _sinks(sink, HQ)
+    o = np.zeros((HQ, SQ, D), dtype=np.float64)
+    lse = np.full((HQ, SQ), -np.inf, dtype=np.float64)
+    lib = _load()
+
+    def run(h):
+        return lib.oracle_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), HQ, HKV, D, _ptr(cq), _ptr(ck),
+                                         cq.shape[0] - 1, float(scale), int(causal), int(window),
+                                         _ptr(sk), h, h + 1, _ptr(o), _ptr(lse))
+
+    with ThreadPoolExecutor(max_workers=min(threads or default_threads(), HQ)) as ex:
+        for rc in ex.map(run, range(HQ)):
             _check(rc)
     return o, lse
 

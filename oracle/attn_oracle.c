@@ -220,6 +220,45 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int 
                                bh_begin, bh_end, o, lse);
 }
 
+/* Packed (variable-length) prefill: nseq sequences packed along the sequence axis of one
+ * batch, sequence s holding query rows [cu_q[s], cu_q[s+1]) and key rows [cu_k[s],
+ * cu_k[s+1]).  Each sequence is its own attention problem: its queries sit at the tail of
+ * its keys (a key count above the query count is a cached prefix), with the causal and
+ * window masks taken inside the sequence and no key of another sequence allowed
+ * (Flash-Attention: Context (CTE), "Algorithm - the dynamic range_select family": per-row
+ * key bounds for sequence packing and dynamic prefix length).  q [HQ][SQ][D] and k, v
+ * [HKV][SKV][D] with SQ = cu_q[nseq], SKV = cu_k[nseq]; o [HQ][SQ][D], lse [HQ][SQ]; heads
+ * [h_begin, h_end); sink as oracle_prefill_sink. */
+int oracle_prefill_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v, int HQ, int HKV,
+                          int D, const int32_t *cu_q, const int32_t *cu_k, int nseq, double scale,
+                          int causal, long window, const double *sink, long h_begin, long h_end,
+                          double *o, double *lse)
+{
+    if (HKV <= 0 || HQ % HKV != 0 || nseq < 0) return ORACLE_ERR_ARG;
+    for (int s = 0; s < nseq; ++s)
+        if (cu_q[s + 1] < cu_q[s] || cu_k[s + 1] < cu_k[s]) return ORACLE_ERR_ARG;
+    const long SQ = cu_q[nseq], SKV = cu_k[nseq];
+    int rc = ORACLE_OK;
+    for (long h = h_begin; h < h_end && rc == ORACLE_OK; ++h) {
+        int g = oracle_kv_head((int)h, HQ, HKV);
+        for (int s = 0; s < nseq && rc == ORACLE_OK; ++s) {
+            const long q0 = cu_q[s], nq = cu_q[s + 1] - q0, k0 = cu_k[s], nk = cu_k[s + 1] - k0;
+            if (nq == 0) continue;
+            long *qp = (long *)malloc(sizeof(long) * (size_t)nq);
+            if (!qp) return ORACLE_ERR_NOMEM;
+            for (long i = 0; i < nq; ++i) qp[i] = oracle_q_pos(i, nq, nk);
+            rc = oracle_attention_rows_sink(q + ((size_t)h * SQ + q0) * D, nq,
+                                            k + ((size_t)g * SKV + k0) * D,
+                                            v + ((size_t)g * SKV + k0) * D, nk, D, scale, qp,
+                                            causal, window, sink ? sink[h] : -INFINITY,
+                                            o + ((size_t)h * SQ + q0) * D, lse + (size_t)h * SQ + q0,
+                                            NULL);
+            free(qp);
+        }
+    }
+    return rc;
+}
+
 /* Paged gather: logical token j of a sequence lives in physical page table_row[j / page],
  * slot j % page; the cache is [num_pages][hkv][page][d] (Flash-Attention: Decode (TKG),
  * "Paged / block cache": the reference gather is block_cache[active_blocks_table[b]]).

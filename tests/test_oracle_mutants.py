@@ -44,6 +44,10 @@ MUTANTS = {
                                       "const long t = j - (len - s_active) - 1;"),
     "rope_q_at_cache_len": ("oracle_rope_row(qd, D, (double)qp, inv_freq);",
                             "oracle_rope_row(qd, D, (double)len, inv_freq);"),
+    "varlen_alignment_dropped": ("for (long i = 0; i < nq; ++i) qp[i] = oracle_q_pos(i, nq, nk);",
+                                 "for (long i = 0; i < nq; ++i) qp[i] = i;"),
+    "varlen_keys_at_query_offset": ("const long q0 = cu_q[s], nq = cu_q[s + 1] - q0, k0 = cu_k[s], nk = cu_k[s + 1] - k0;",
+                                    "const long q0 = cu_q[s], nq = cu_q[s + 1] - q0, k0 = cu_q[s], nk = cu_k[s + 1] - cu_k[s];"),
     "rotated_rows_not_rounded": ("for (int x = 0; x < D; ++x) qd[x] = round_bf16(qd[x]);",
                                  "for (int x = 0; x < D; ++x) qd[x] = qd[x];"),
 }

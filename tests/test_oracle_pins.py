@@ -664,3 +664,97 @@ def test_decode_rope_rounds_the_rotated_rows_to_bf16():
     o2, l2 = oracle.decode(q2, fk2, fv, None, np.array([n], np.int32), 0.25)
     np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- packed prefill
+# Sequences packed along the sequence axis, each its own problem (CTE "Algorithm - the
+# dynamic range_select family": per-row key bounds for sequence packing / prefix length).
+VARLEN = [
+    # cu_q, cu_k, causal, window
+    ([0, 5, 12, 12, 30], [0, 5, 20, 23, 41], 1, 0),    # prefixes, an empty query range
+    ([0, 9, 10, 25], [0, 9, 10, 25], 1, 4),            # equal lengths, window 4
+    ([0, 7, 16], [0, 3, 30], 1, 0),                    # more queries than keys in sequence 0
+    ([0, 6, 14], [0, 11, 19], 0, 0),                   # non-causal
+]
+
+
+def _varlen_inputs(seed, hq, hkv, cu_q, cu_k, d):
+    q = rand_bits(seed, (hq, cu_q[-1], d), "q")
+    k, v = rand_bits(seed, (hkv, cu_k[-1], d), "k"), rand_bits(seed, (hkv, cu_k[-1], d), "v")
+    return q, k, v
+
+
+def test_varlen_one_sequence_is_plain_prefill():
+    q, k, v = _varlen_inputs(90, 4, 2, [0, 21], [0, 33], 8)
+    for causal, window in ((0, 0), (1, 0), (1, 6)):
+        o1, l1 = oracle.prefill_varlen(q, k, v, [0, 21], [0, 33], 0.3, causal, window)
+        o2, l2 = oracle.prefill(q[None], k[None], v[None], 0.3, causal, window)
+        np.testing.assert_array_equal(o1, o2[0])
+        np.testing.assert_array_equal(l1, l2[0])
+
+
+@pytest.mark.parametrize("cu_q,cu_k,causal,window", VARLEN)
+def test_varlen_zero_q_gives_mean_of_own_sequence(cu_q, cu_k, causal, window):
+    """Q = 0: each row averages the allowed V rows of its own sequence, LSE = ln(count);
+    the allowed keys of row i of sequence s are counted here from the sequence's own
+    bottom-right alignment."""
+    d = 4
+    q = np.zeros((1, cu_q[-1], d), np.uint16)
+    _, k, v = _varlen_inputs(91, 1, 1, cu_q, cu_k, d)
+    o, lse = oracle.prefill_varlen(q, k, v, cu_q, cu_k, 1.0, causal, window)
+    vf = f64(v[0])
+    for s in range(len(cu_q) - 1):
+        nq, nk = cu_q[s + 1] - cu_q[s], cu_k[s + 1] - cu_k[s]
+        for i in range(nq):
+            qp = i + nk - nq
+            hi = min(qp, nk - 1) if causal else nk - 1
+            lo = max(0, qp - window + 1) if window else 0
+            row = cu_q[s] + i
+            if hi < lo:
+                assert (o[0, row] == 0).all() and lse[0, row] == -np.inf
+                continue
+            np.testing.assert_allclose(o[0, row], vf[cu_k[s] + lo: cu_k[s] + hi + 1].mean(0),
+                                       atol=1e-12)
+            assert abs(lse[0, row] - math.log(hi - lo + 1)) < 1e-12
+
+
+def test_varlen_other_sequences_do_not_matter():
+    cu_q, cu_k = [0, 8, 20, 27], [0, 12, 20, 40]
+    q, k, v = _varlen_inputs(92, 2, 1, cu_q, cu_k, 8)
+    o1, l1 = oracle.prefill_varlen(q, k, v, cu_q, cu_k, 0.4, 1, 0)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, cu_k[1]:cu_k[2]] = rand_bits(93, (1, cu_k[2] - cu_k[1], 8), "k")
+    v2[:, cu_k[1]:cu_k[2]] = rand_bits(93, (1, cu_k[2] - cu_k[1], 8), "v")
+    o2, l2 = oracle.prefill_varlen(q, k2, v2, cu_q, cu_k, 0.4, 1, 0)
+    for s in (0, 2):  # sequences 0 and 2 are untouched
+        r = slice(cu_q[s], cu_q[s + 1])
+        np.testing.assert_array_equal(o1[:, r], o2[:, r])
+        np.testing.assert_array_equal(l1[:, r], l2[:, r])
+
+
+@pytest.mark.parametrize("cu_q,cu_k,causal,window", VARLEN)
+def test_varlen_matches_torch_sdpa_with_a_block_mask(cu_q, cu_k, causal, window):
+    """PyTorch's scaled_dot_product_attention (float64) with a boolean mask built here from
+    the sequence offsets: an independent implementation of the packed problem."""
+    import torch
+    import torch.nn.functional as F
+
+    hq, hkv, d = 4, 2, 8
+    q, k, v = _varlen_inputs(94, hq, hkv, cu_q, cu_k, d)
+    o, lse = oracle.prefill_varlen(q, k, v, cu_q, cu_k, 0.35, causal, window)
+    SQ, SKV = cu_q[-1], cu_k[-1]
+    mask = np.zeros((SQ, SKV), bool)
+    for s in range(len(cu_q) - 1):
+        nq, nk = cu_q[s + 1] - cu_q[s], cu_k[s + 1] - cu_k[s]
+        for i in range(nq):
+            qp = i + nk - nq
+            for j in range(nk):
+                ok = (not causal or j <= qp) and (not window or j >= qp - window + 1)
+                mask[cu_q[s] + i, cu_k[s] + j] = ok
+    t = lambda a: torch.from_numpy(f64(a))
+    ref = F.scaled_dot_product_attention(t(q), t(k).repeat_interleave(hq // hkv, 0),
+                                         t(v).repeat_interleave(hq // hkv, 0),
+                                         attn_mask=torch.from_numpy(mask), scale=0.35).numpy()
+    live = mask.any(1)
+    np.testing.assert_allclose(o[:, live], ref[:, live], rtol=0, atol=1e-12)
+    assert (o[:, ~live] == 0).all()
