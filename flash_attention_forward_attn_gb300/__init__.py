@@ -50,7 +50,8 @@ class AttnOpts(ctypes.Structure):
     _fields_ = [("sink", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
                 ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
                 ("window", ctypes.c_int), ("circular", ctypes.c_int),
-                ("rope_inv_freq", ctypes.c_void_p)]
+                ("rope_inv_freq", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p),
+                ("cu_seqlens_k", ctypes.c_void_p), ("nseq", ctypes.c_int)]
 
 
 def load_library(build_if_missing: bool = False):
@@ -204,12 +205,27 @@ def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | N
 
 
 def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
-                        o=None, lse=None, o_dtype=None, sink=None, stream=None):
+                        o=None, lse=None, o_dtype=None, sink=None, cu_seqlens_q=None,
+                        cu_seqlens_k=None, stream=None):
     """attn_fwd_prefill with the attn_opts options: sink, an fp32 [hq] tensor of
-    per-query-head sink logits (scaled-score units) on q's device, or None."""
+    per-query-head sink logits (scaled-score units) on q's device, or None; and packed
+    sequences: cu_seqlens_q / cu_seqlens_k int32 [nseq + 1] offsets along sq and skv of a
+    b = 1 problem (each sequence its own problem, queries at the tail of its keys)."""
+    import torch
+
     lib = load_library()
     o, (b, hq, hkv, sq, skv, d) = _prefill_marshal(q, k, v, o, lse, o_dtype)
     opts = _opts(sink, hq, q.device)
+    if cu_seqlens_q is not None or cu_seqlens_k is not None:
+        if cu_seqlens_q is None or cu_seqlens_k is None:
+            raise ValueError("packed sequences need both cu_seqlens_q and cu_seqlens_k")
+        _req(cu_seqlens_q, "cu_seqlens_q", torch.int32, q.device)
+        _req(cu_seqlens_k, "cu_seqlens_k", torch.int32, q.device)
+        if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape != cu_seqlens_k.shape:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must be int32 [nseq + 1]")
+        opts.cu_seqlens_q = cu_seqlens_q.data_ptr()
+        opts.cu_seqlens_k = cu_seqlens_k.data_ptr()
+        opts.nseq = cu_seqlens_q.shape[0] - 1
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     _check(lib.attn_fwd_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, hq, hkv, sq,
                                    skv, d, sc, int(bool(causal)), int(window),

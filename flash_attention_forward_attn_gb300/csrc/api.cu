@@ -71,6 +71,9 @@ struct Opts {
     int window = 0;
     bool circular = false;
     const float* rope = nullptr;
+    const int32_t* cu_q = nullptr;
+    const int32_t* cu_k = nullptr;
+    int nseq = 0;
 };
 
 bool read_opts(const attn_opts* opts, Opts* o) {
@@ -88,7 +91,15 @@ bool read_opts(const attn_opts* opts, Opts* o) {
     o->window = opts->window;
     o->circular = opts->circular == 1;
     o->rope = opts->rope_inv_freq;
-    return o->rope == nullptr || aligned4(o->rope);
+    if (o->rope && !aligned4(o->rope)) return false;
+    o->cu_q = opts->cu_seqlens_q;
+    o->cu_k = opts->cu_seqlens_k;
+    o->nseq = opts->nseq;
+    if (o->cu_q || o->cu_k) {
+        if (!o->cu_q || !o->cu_k || !aligned4(o->cu_q) || !aligned4(o->cu_k) || o->nseq < 1)
+            return false;
+    }
+    return true;
 }
 
 // Paged-cache arguments shared by decode and append.
@@ -151,6 +162,7 @@ attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, voi
     // prefill reads bf16 K and V and takes its window as an argument; RoPE and a circular
     // cache are decode options
     if (op.e4m3 || op.window != 0 || op.circular || op.rope) return ATTN_ERR_UNSUPPORTED;
+    if (op.cu_q && b != 1) return ATTN_ERR_INVALID_ARG;  // packing is along one batch's rows
     if (sq == 0) return ATTN_OK;
     if (!q || !o || (skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o) || (skv > 0 && (!aligned16(k) || !aligned16(v))))
@@ -158,7 +170,7 @@ attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, voi
     if ((long long)b * hq > 0x7fffffffLL || (long long)b * hkv > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
     attn::PrefillArgs a{q, k, v, o, lse, b, hq, hkv, sq, skv, d, scale, causal ? 1 : 0, window,
-                        o_dtype, op.sink};
+                        o_dtype, op.sink, op.cu_q, op.cu_k, op.nseq};
     return attn::prefill_launch(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -197,6 +209,7 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
     Opts op;
     if (!read_opts(opts, &op)) return ATTN_ERR_INVALID_ARG;
     if (op.e4m3 && d == 64) return ATTN_ERR_UNSUPPORTED;  // half a 128-byte box per row
+    if (op.cu_q) return ATTN_ERR_UNSUPPORTED;  // packed sequences are a prefill option
     // a circular cache is a flat ring that holds every new token's window
     if (op.circular && (block_table || op.window == 0 ||
                         (long long)op.window + s_active - 1 > max_cache_len || max_cache_len % 32 != 0))

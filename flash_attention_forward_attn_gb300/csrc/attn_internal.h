@@ -29,6 +29,9 @@ struct PrefillArgs {
     int causal, window;
     attn_dtype o_dtype;
     const float* sink;  // [hq] sink logits, or NULL
+    const int32_t* cu_seqlens_q;  // packed sequences: [nseq + 1] offsets, or NULL
+    const int32_t* cu_seqlens_k;
+    int nseq;
 };
 
 struct DecodeArgs {

@@ -60,6 +60,10 @@ struct PrefillParams {
     void* o;
     float* lse;
     const float* sink;  // [hq] sink logits of the query heads, or NULL
+    // packed sequences: offsets [nseq + 1] along the query and key rows, or NULL
+    const int* cu_q;
+    const int* cu_k;
+    int nseq;
     int hq, hkv, sq, skv, group, nqt, window, causal, o_f32;
     int nbh;     // b * hq
     int nunits;  // work units of the persistent kernel
@@ -77,11 +81,44 @@ __device__ __forceinline__ int zigzag_unit(int cta, int round, int grid) {
 // address field in the low bits (tiles never straddle the 256 KB field range).
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) { return d + (byte_off >> 4); }
 
+// Packed sequences: the sequence of query row i (the last s with cu_q[s] <= i).
+__device__ __forceinline__ int row_sequence(const PrefillParams& p, int i) {
+    int a = 0, b = p.nseq - 1;
+    while (a < b) {
+        const int m = (a + b + 1) >> 1;
+        if (__ldg(p.cu_q + m) <= i) a = m;
+        else b = m - 1;
+    }
+    return a;
+}
+
+// Packed sequences: key rows [lo, hi] that query row i of sequence s may attend (hi < lo:
+// none).  The sequence's keys are rows [cu_k[s], cu_k[s+1]), its queries sit at the tail of
+// them, and the causal and window bands apply inside it ("Flash-Attention: Context (CTE)",
+// "Algorithm - the dynamic range_select family": per-row key bounds for sequence packing
+// and a dynamic prefix length).
+__device__ __forceinline__ void row_key_bounds(const PrefillParams& p, int i, int s, int& lo,
+                                               int& hi) {
+    const int q0 = __ldg(p.cu_q + s), k0 = __ldg(p.cu_k + s);
+    const int nk = __ldg(p.cu_k + s + 1) - k0;
+    const int qpos = (i - q0) + nk - (__ldg(p.cu_q + s + 1) - q0);
+    hi = k0 + (p.causal ? min(qpos, nk - 1) : nk - 1);
+    lo = k0 + (p.window > 0 ? max(0, qpos - p.window + 1) : 0);
+}
+
+// A query tile and its KV-tile range [kt0, kt0 + n).  One problem per (batch, head): the
+// queries sit at the tail of the keys (q_pos = i + skv - sq).  Packed sequences (kPacked):
+// [all_lo, all_hi] holds the keys every row of the tile may attend (tiles wholly inside
+// need no mask).  Bounds grow with the row inside one sequence, so its first and last rows
+// give them; a tile that spans sequences is masked everywhere, and its range reaches at
+// least to the start of its last sequence (a causal sequence with more queries than keys
+// has leading rows with no key at all).  kPacked is a template parameter so that the
+// unpacked kernels keep their own code.
 struct TileRange {
-    int q0, rows, qpos_lo, qpos_hi, kt0, n;
+    int q0, rows, qpos_lo, qpos_hi, kt0, n, all_lo, all_hi;
 };
 
-template <int BN>
+template <int BN, bool kPacked>
 __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) {
     TileRange r;
     r.q0 = qt * kBM;
@@ -89,13 +126,32 @@ __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) 
     const int off = p.skv - p.sq;  // queries sit at the tail of the keys
     r.qpos_lo = r.q0 + off;
     r.qpos_hi = r.q0 + r.rows - 1 + off;
+    r.all_lo = INT_MAX;
+    r.all_hi = INT_MIN;
     if (r.rows <= 0) {  // a query tile past the end of the sequence
         r.kt0 = 0;
         r.n = 0;
         return r;
     }
-    const int k_end = p.causal ? min(p.skv, r.qpos_hi + 1) : p.skv;
-    const int k_begin = p.window > 0 ? max(0, r.qpos_lo - p.window + 1) : 0;
+    int k_end, k_begin;
+    if constexpr (kPacked) {
+        const int last = r.q0 + r.rows - 1;
+        const int s0 = row_sequence(p, r.q0), s1 = row_sequence(p, last);
+        int lo0, hi0, lo1, hi1;
+        row_key_bounds(p, r.q0, s0, lo0, hi0);
+        row_key_bounds(p, last, s1, lo1, hi1);
+        k_end = min(p.skv, hi1 + 1);
+        k_begin = max(0, lo0);
+        if (s0 == s1) {
+            r.all_lo = lo1;
+            r.all_hi = hi0;
+        } else {
+            k_end = max(k_end, min(p.skv, __ldg(p.cu_k + s1)));
+        }
+    } else {
+        k_end = p.causal ? min(p.skv, r.qpos_hi + 1) : p.skv;
+        k_begin = p.window > 0 ? max(0, r.qpos_lo - p.window + 1) : 0;
+    }
     if (k_end <= k_begin) {
         r.kt0 = 0;
         r.n = 0;
@@ -161,7 +217,7 @@ constexpr int kRegsSoftmax = 160;
 static_assert(256 * kRegsRole + 128 * kRegsSoftmax + 128 * kRegsLaunch4 <= 512 * kRegsLaunch4,
               "register split");
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -188,7 +244,7 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
         bh = w % p.nbh;
         const int bidx = bh / p.hq, h = bh % p.hq;
         kvz = bidx * p.hkv + h / p.group;
-        return tile_range<BN>(p, qt);
+        return tile_range<BN, kPacked>(p, qt);
     };
 
     if (threadIdx.x == 0) {
@@ -377,9 +433,15 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             if (w >= p.nunits) break;
             int bh, kvz;
             const TileRange t = unit_at(w, bh, kvz);
-            const int qpos = t.qpos_lo + row;
-            const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
-            const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+            int key_lo, key_hi;
+            if constexpr (kPacked) {
+                const int qrow = min(t.q0 + row, p.sq - 1);  // rows past sq are never stored
+                row_key_bounds(p, qrow, row_sequence(p, qrow), key_lo, key_hi);
+            } else {
+                const int qpos = t.qpos_lo + row;
+                key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
+                key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+            }
             float m_used = -INFINITY, l_sum = 0.f;
             for (int i = 0; ok && i < t.n; ++i, ++T) {
                 const int b = T & 1;
@@ -390,8 +452,10 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 tc_fence_after();
                 const uint32_t tm_s = tm_row + b * BN;
                 const int k0 = (t.kt0 + i) * BN;
-                const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
-                                  (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
+                const bool edge =
+                    kPacked ? (k0 < t.all_lo || k0 + BN - 1 > t.all_hi)
+                            : ((p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
+                               (p.window > 0 && k0 < t.qpos_hi - p.window + 1));
                 // the S row from TMEM, scaled for scale <= 0, then masked (edge tiles; a
                 // masked key is -inf whatever the sign of the scale)
                 auto load_s = [&](float* v) {
@@ -621,7 +685,7 @@ struct Cfg2Q {
 // that overwrites S_X by the same thread, and one thread's products run in issue order on
 // the tensor pipe.  The first PV of a unit into O_X waits until the previous unit's
 // epilogue has read O_X out of TMEM.
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
@@ -654,8 +718,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
         u.bh = w % p.nbh;
         const int bidx = u.bh / p.hq, h = u.bh % p.hq;
         u.kvz = bidx * p.hkv + h / p.group;
-        u.t[0] = tile_range<BN>(p, 2 * pair);
-        u.t[1] = tile_range<BN>(p, 2 * pair + 1);  // rows <= 0 (past sq) gives n = 0
+        u.t[0] = tile_range<BN, kPacked>(p, 2 * pair);
+        u.t[1] = tile_range<BN, kPacked>(p, 2 * pair + 1);  // rows <= 0 (past sq) gives n = 0
         u.has_b = u.t[1].rows > 0;
         u.u0 = INT_MAX;
         u.u1 = INT_MIN;
@@ -891,9 +955,15 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             const int eidx = ebase + ((x == 1 && u.t[0].rows > 0) ? 1 : 0);
             ebase += (u.t[0].rows > 0 ? 1 : 0) + (u.t[1].rows > 0 ? 1 : 0);
             const int q_row = t.q0 + row;
-            const int qpos = t.qpos_lo + row;
-            const int key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
-            const int key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+            int key_lo, key_hi;
+            if constexpr (kPacked) {
+                const int qrow = min(q_row, p.sq - 1);  // rows past sq are never stored
+                row_key_bounds(p, qrow, row_sequence(p, qrow), key_lo, key_hi);
+            } else {
+                const int qpos = t.qpos_lo + row;
+                key_lo = p.window > 0 ? qpos - p.window + 1 : INT_MIN;
+                key_hi = p.causal ? min(qpos, p.skv - 1) : p.skv - 1;
+            }
             float m_used = -INFINITY, l_sum = 0.f;
             for (int i = 0; ok && i < t.n; ++i, ++cnt) {
                 if (!wait_or_abort(sfull, cnt & 1, &abort_flag)) {
@@ -902,8 +972,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 }
                 tc_fence_after();
                 const int k0 = (t.kt0 + i) * BN;
-                const bool edge = (p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
-                                  (p.window > 0 && k0 < t.qpos_hi - p.window + 1);
+                const bool edge =
+                    kPacked ? (k0 < t.all_lo || k0 + BN - 1 > t.all_hi)
+                            : ((p.causal && k0 + BN - 1 > t.qpos_lo) || (k0 + BN > p.skv) ||
+                               (p.window > 0 && k0 < t.qpos_hi - p.window + 1));
                 // S row of this tile from TMEM, scaled for scale <= 0, then masked (edge tiles;
                 // a masked key is -inf whatever the sign of the scale)
                 auto load_s = [&](float* v) {
@@ -1117,13 +1189,13 @@ int num_sms() {
     return cached[dev];
 }
 
-template <int D>
+template <int D, bool kPacked>
 attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
     using C = CfgW<D>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(prefill_wide_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_wide_kernel<D, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kDynBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
@@ -1131,7 +1203,7 @@ attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, con
         // setmaxnreg.inc waits until the launch's register pool can serve it; the split is
         // sized for exactly kRegsLaunch4 registers per thread at launch.
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, prefill_wide_kernel<D>) != cudaSuccess) {
+        if (cudaFuncGetAttributes(&fa, prefill_wide_kernel<D, kPacked>) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
@@ -1143,18 +1215,18 @@ attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, con
     PrefillParams pp = p;
     pp.nunits = (int)units;
     const int grid = (int)(units < num_sms() ? units : num_sms());
-    prefill_wide_kernel<D><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, pp);
+    prefill_wide_kernel<D, kPacked><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, pp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
 
-template <int D>
+template <int D, bool kPacked>
 attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
     using C = Cfg2Q<D>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(prefill2q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill2q_kernel<D, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kDynBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
@@ -1162,7 +1234,7 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
         // setmaxnreg.inc waits until the launch's register pool can serve it; the split is
         // sized for exactly kRegsLaunch3 registers per thread at launch.
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, prefill2q_kernel<D>) != cudaSuccess) {
+        if (cudaFuncGetAttributes(&fa, prefill2q_kernel<D, kPacked>) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
@@ -1183,7 +1255,7 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
     } else {
         to = tq;
     }
-    prefill2q_kernel<D><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, to, pp);
+    prefill2q_kernel<D, kPacked><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, to, pp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
@@ -1208,6 +1280,9 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     p.o = a.o;
     p.lse = a.lse;
     p.sink = a.sink;
+    p.cu_q = a.cu_seqlens_q;
+    p.cu_k = a.cu_seqlens_k;
+    p.nseq = a.nseq;
     p.hq = a.hq;
     p.hkv = a.hkv;
     p.sq = a.sq;
@@ -1221,9 +1296,11 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     p.nbh = a.b * a.hq;
     p.nunits = 0;
     if constexpr (D <= 128)
-        return prefill2q_launch<D>(a, tq, tk, tv, p, stream);
+        return p.cu_q ? prefill2q_launch<D, true>(a, tq, tk, tv, p, stream)
+                      : prefill2q_launch<D, false>(a, tq, tk, tv, p, stream);
     else
-        return prefill_wide_launch<D>(a, tq, tk, tv, p, stream);
+        return p.cu_q ? prefill_wide_launch<D, true>(a, tq, tk, tv, p, stream)
+                      : prefill_wide_launch<D, false>(a, tq, tk, tv, p, stream);
 }
 
 }  // namespace

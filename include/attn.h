@@ -100,6 +100,17 @@ typedef enum { ATTN_KV_BF16 = 0, ATTN_KV_E4M3 = 1 } attn_kv_dtype;
  *          Keys already in the cache are used as stored (rotated when they were
  *          appended).  The rotated query is rounded to bf16 before the product.  Must be
  *          4-byte aligned.
+ *
+ *   cu_seqlens_q, cu_seqlens_k, nseq : prefill only, packed sequences ("Flash-Attention:
+ *          Context (CTE)", "Algorithm - the dynamic range_select family": per-row key
+ *          bounds for sequence packing and a dynamic prefix length).  DEVICE int32 arrays
+ *          [nseq + 1], non-decreasing from 0 to sq and to skv: sequence s holds query rows
+ *          [cu_seqlens_q[s], cu_seqlens_q[s+1]) and key rows [cu_seqlens_k[s],
+ *          cu_seqlens_k[s+1]) of the one batch (b must be 1).  Each sequence is its own
+ *          problem: its queries sit at the tail of its keys (more keys than queries is a
+ *          cached prefix), the causal and window masks apply inside it, and no row sees a
+ *          key of another sequence.  Offsets that break these rules give unspecified
+ *          results but no out-of-range access.  NULL = one problem per (batch, head).
  */
 typedef struct {
     const float* sink;
@@ -109,6 +120,9 @@ typedef struct {
     int window;
     int circular;
     const float* rope_inv_freq;
+    const int32_t* cu_seqlens_q;
+    const int32_t* cu_seqlens_k;
+    int nseq;
 } attn_opts;
 
 /*
@@ -146,8 +160,9 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* 
 /*
  * attn_fwd_prefill_ex -- attn_fwd_prefill with the options of attn_opts (NULL = none):
  * same arguments, layouts, semantics and errors, plus ATTN_ERR_INVALID_ARG for an
- * invalid option (a misaligned sink pointer) and ATTN_ERR_UNSUPPORTED for an e4m3
- * kv_dtype (prefill reads bf16 K and V).
+ * invalid option (a misaligned sink pointer; packed sequences with b != 1, nseq < 1 or
+ * a missing or misaligned offset array) and ATTN_ERR_UNSUPPORTED for a decode option
+ * (an e4m3 kv_dtype, window, circular or rope_inv_freq).
  */
 attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int b, int hq, int hkv, int sq, int skv, int d, float scale,

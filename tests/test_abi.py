@@ -122,6 +122,14 @@ def test_ex_calls_check_their_options_before_launch(lib):
     assert call(dargs, op(rope_inv_freq=(1 << 20) + 2)) == 1  # misaligned
     for kw in (dict(window=4), dict(circular=1), dict(rope_inv_freq=1 << 20)):
         assert lib.attn_fwd_prefill_ex(*args, op(**kw), None) == 2  # decode options
+    cu = 1 << 20
+    assert lib.attn_fwd_prefill_ex(*args, op(cu_seqlens_q=cu, nseq=2), None) == 1  # no k offsets
+    assert lib.attn_fwd_prefill_ex(*args, op(cu_seqlens_q=cu, cu_seqlens_k=cu, nseq=0), None) == 1
+    assert lib.attn_fwd_prefill_ex(*args, op(cu_seqlens_q=cu + 2, cu_seqlens_k=cu, nseq=1),
+                                   None) == 1
+    b2 = args[:5] + (2,) + args[6:]  # packing needs b = 1
+    assert lib.attn_fwd_prefill_ex(*b2, op(cu_seqlens_q=cu, cu_seqlens_k=cu, nseq=1), None) == 1
+    assert call(dargs, op(cu_seqlens_q=cu, cu_seqlens_k=cu, nseq=1)) == 2  # a prefill option
     # an invalid size is still reported first, with or without options
     dbad = dargs[:8] + (80,) + dargs[9:]  # d = 80
     assert lib.attn_fwd_decode_ex(*dbad, ctypes.byref(none), FAKE, 1 << 30, None) == 2

@@ -1,0 +1,100 @@
+"""Parity of packed (variable-length) prefill (attn_fwd_prefill_ex with cu_seqlens, through
+the C ABI) against the fp64 oracle ("Flash-Attention: Context (CTE)", "Algorithm - the
+dynamic range_select family": per-row key bounds for sequence packing and a dynamic
+prefix length).  Each packed sequence is its own problem, its queries at the tail of its
+keys."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.helpers import assert_lse_close, assert_o_close, tensor_of_bits
+from workloads import configs as C
+from workloads import rng
+
+pytestmark = pytest.mark.gpu
+
+
+def packed_lengths(seed, nseq, q_hi, prefix_hi):
+    """Seeded query lengths in [0, q_hi] and cached-prefix lengths in [0, prefix_hi]."""
+    u = rng.u64_np(seed, 0, 2 * nseq)
+    nq = (u[:nseq] % np.uint64(q_hi + 1)).astype(np.int64)
+    pre = (u[nseq:] % np.uint64(prefix_hi + 1)).astype(np.int64) if prefix_hi else np.zeros(nseq, np.int64)
+    cu_q = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(nq + pre)]).astype(np.int32)
+    return cu_q, cu_k
+
+
+def run_varlen(cu_q, cu_k, hq, hkv, d, causal, window, out, seed, dev, sink=None):
+    import flash_attention_forward_attn_gb300 as A
+
+    w = C.PrefillWorkload("varlen", 1, hq, hkv, int(cu_q[-1]), int(cu_k[-1]), d, causal, window,
+                          seed=seed)
+    qb, kb, vb = C.prefill_inputs_np(w)
+    q, k, v = (tensor_of_bits(x, dev) for x in (qb, kb, vb))
+    lse = torch.empty((1, hq, w.sq), dtype=torch.float32, device=dev)
+    o, _ = A.attn_fwd_prefill_ex(q, k, v, causal=causal, window=window, scale=w.scale, lse=lse,
+                                 o_dtype=out, sink=sink,
+                                 cu_seqlens_q=torch.from_numpy(cu_q).to(dev),
+                                 cu_seqlens_k=torch.from_numpy(cu_k).to(dev))
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    return (qb, kb, vb, w), o, lse
+
+
+CASES = [
+    # name, cu_q, cu_k (or a seeded packing: nseq, q_hi, prefix_hi), hq, hkv, d, causal, window, out
+    ("two_seqs_mid_tile_d128", [0, 100, 300], [0, 100, 300], 4, 2, 128, True, 0, torch.bfloat16),
+    ("prefix_cached_d128", [0, 70, 200, 200, 333], [0, 300, 530, 600, 733], 4, 1, 128, True, 0,
+     torch.float32),
+    ("more_q_than_k_d64", [0, 150, 260], [0, 40, 300], 4, 4, 64, True, 0, torch.float32),
+    ("noncausal_d64", [0, 33, 160, 161], [0, 80, 200, 330], 2, 1, 64, False, 0, torch.bfloat16),
+    ("window_d256", [0, 200, 450], [0, 260, 700], 4, 2, 256, True, 64, torch.bfloat16),
+    ("many_seqs_d128", (40, 180, 0), None, 8, 2, 128, True, 0, torch.bfloat16),
+    ("many_prefixed_d128_w", (30, 150, 400), None, 4, 2, 128, True, 100, torch.float32),
+    ("many_seqs_d256", (24, 200, 100), None, 4, 2, 256, True, 0, torch.float32),
+    ("many_seqs_d64_multi_unit", (60, 300, 64), None, 40, 8, 64, True, 0, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0])
+def test_varlen_prefill_all_rows(case, cuda_device):
+    name, a, b_, hq, hkv, d, causal, window, out = case
+    if b_ is None:
+        cu_q, cu_k = packed_lengths(0xA11 + len(name), *a)
+    else:
+        cu_q, cu_k = np.array(a, np.int32), np.array(b_, np.int32)
+    (qb, kb, vb, w), o, lse = run_varlen(cu_q, cu_k, hq, hkv, d, causal, window, out,
+                                         0x7A0 + len(name), cuda_device)
+    o_ref, lse_ref = oracle.prefill_varlen(qb[0], kb[0], vb[0], cu_q, cu_k, w.scale, causal,
+                                           window)
+    assert_o_close(o[0].float().cpu().numpy(), o_ref, name)
+    assert_lse_close(lse[0].cpu().numpy(), lse_ref, name)
+    masked = np.isneginf(lse_ref)
+    if masked.any():  # rows with no allowed key are exactly zero
+        assert (o[0].float().cpu().numpy()[masked] == 0).all()
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_varlen_one_sequence_is_bit_identical_to_plain_prefill(d, cuda_device):
+    import flash_attention_forward_attn_gb300 as A
+
+    cu = np.array([0, 700], np.int32)
+    (qb, kb, vb, w), o1, l1 = run_varlen(cu, cu, 4, 2, d, True, 0, torch.bfloat16, 0x7B0 + d,
+                                         cuda_device)
+    q, k, v = (tensor_of_bits(x, cuda_device) for x in (qb, kb, vb))
+    l2 = torch.empty_like(l1)
+    o2, _ = A.attn_fwd_prefill(q, k, v, causal=True, scale=w.scale, lse=l2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_varlen_with_sink(cuda_device):
+    cu_q, cu_k = packed_lengths(0xA99, 12, 200, 150)
+    sk = C.sink_logits(8)
+    (qb, kb, vb, w), o, lse = run_varlen(cu_q, cu_k, 8, 2, 128, True, 0, torch.float32, 0x7C0,
+                                         cuda_device, sink=torch.from_numpy(sk).to(cuda_device))
+    o_ref, lse_ref = oracle.prefill_varlen(qb[0], kb[0], vb[0], cu_q, cu_k, w.scale, True, 0,
+                                           sink=sk)
+    assert_o_close(o[0].cpu().numpy(), o_ref, "varlen sink")
+    assert_lse_close(lse[0].cpu().numpy(), lse_ref, "varlen sink")
