@@ -248,6 +248,44 @@ def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False,
     return ent
 
 
+def packed_prefill_entry(pw, dev, steps, warmup, flush, stream, peaks, world):
+    """Time attn_fwd_prefill_ex on packed sequences (attn_opts.cu_seqlens)."""
+    import torch
+
+    import flash_attention_forward_attn_gb300 as A
+    from workloads import configs as C
+
+    w = pw.as_prefill()
+    q, k, v = C.prefill_inputs_torch(w, dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    cu_q, cu_k = (torch.from_numpy(x).to(dev) for x in pw.offsets())
+
+    def step():
+        A.attn_fwd_prefill_ex(q, k, v, causal=True, scale=pw.scale, o=o, lse=lse,
+                              cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, stream=stream)
+
+    ms = time_steps(step, steps, warmup, flush, stream)
+    assert A.attn_get_device_error(stream) == 0
+    mean_ms = sum(ms) / len(ms)
+    flops = pw.flops()
+    value, slowest_s = aggregate_throughput(flops * steps, sum(ms) / 1e3, world, dev)
+    achieved = flops / (mean_ms / 1e3) / 1e12
+    ent = {
+        "workload": pw.name, "value": value / 1e12, "unit": "TFLOP/s", "ms_per_step": mean_ms,
+        "ms_min": min(ms), "flops_per_step": flops, "steps": steps, "gpu_launches": steps,
+        "packing": {"nseq": pw.nseq, "sq": w.sq, "skv": w.skv},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "algorithmic_bytes": pw.io_bytes(),
+                     "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
+        "slowest_rank_s": slowest_s,
+    }
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    return ent
+
+
 def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
     """Same metric through the public API with host buffers: every step copies Q, K, V from
     pinned host memory, calls attn_fwd_prefill, and copies O and LSE back, all inside the
@@ -494,7 +532,10 @@ def main():
 
     if args.workload is not None:
         wx = C.REGISTRY[args.workload]
-        if isinstance(wx, C.PrefillWorkload):
+        if isinstance(wx, C.PackedPrefillWorkload):
+            ent = packed_prefill_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks,
+                                       world)
+        elif isinstance(wx, C.PrefillWorkload):
             ent = prefill_entry(wx, dev, args.steps, args.warmup, flush, stream, peaks, world,
                                 sink=args.sink)
         else:
@@ -521,6 +562,10 @@ def main():
             for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4):
                 extras[wx.name] = decode_entry(wx, dev, max(ext_steps, 50), args.warmup, flush,
                                                stream, peaks, world)
+            # packed sequences (attn_opts.cu_seqlens): 16 causal sequences with cached prefixes
+            ent = packed_prefill_entry(C.PACKED_PREFILL, dev, ext_steps, args.warmup, flush,
+                                       stream, peaks, world)
+            extras[ent["workload"]] = ent
             # the attention sink (attn_opts.sink) on the 2K prefill and the 1-token decode
             ent = prefill_entry(w, dev, ext_steps, args.warmup, flush, stream, peaks, world,
                                 sink=True)

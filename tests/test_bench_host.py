@@ -78,3 +78,20 @@ def test_recorded_traffic_requires_matching_source(tmp_path, monkeypatch):
 def test_measured_peaks_reads_driver_file():
     p = bench.measured_peaks()
     assert p["hbm_gbs"] > 1000 and p["bf16_tflops"] > 100
+
+
+def test_packed_prefill_flops_count_the_allowed_pairs():
+    """The benchmark's FLOP count of a packed workload equals 4 d hq times the allowed
+    (query, key) pairs counted one by one with the oracle's mask predicate."""
+    import oracle
+    from workloads import configs as C
+
+    pw = C.PackedPrefillWorkload("tiny_packed", 2, 1, 8, 5, 3, 40, 17, seed=5)
+    cu_q, cu_k = pw.offsets()
+    pairs = 0
+    for s in range(pw.nseq):
+        nq, nk = cu_q[s + 1] - cu_q[s], cu_k[s + 1] - cu_k[s]
+        for i in range(nq):
+            qp = oracle.q_pos(i, nq, nk)
+            pairs += sum(oracle.allowed(j, nk, qp, True, 0) for j in range(nk))
+    assert pw.flops() == 4 * pw.d * pw.hq * pairs

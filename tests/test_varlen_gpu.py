@@ -98,3 +98,34 @@ def test_varlen_with_sink(cuda_device):
                                            sink=sk)
     assert_o_close(o[0].cpu().numpy(), o_ref, "varlen sink")
     assert_lse_close(lse[0].cpu().numpy(), lse_ref, "varlen sink")
+
+
+def test_packed_benchmark_workload_sampled(cuda_device):
+    """The packed workload the benchmark times, in the same launch; sampled sequences and
+    heads are checked row by row against the oracle over that sequence's own keys."""
+    import flash_attention_forward_attn_gb300 as A
+
+    pw = C.PACKED_PREFILL
+    w = pw.as_prefill()
+    cu_q, cu_k = pw.offsets()
+    q, k, v = C.prefill_inputs_torch(w, cuda_device)
+    lse = torch.empty((1, w.hq, w.sq), dtype=torch.float32, device=cuda_device)
+    o, _ = A.attn_fwd_prefill_ex(q, k, v, causal=True, scale=pw.scale, lse=lse,
+                                 cu_seqlens_q=torch.from_numpy(cu_q).to(cuda_device),
+                                 cu_seqlens_k=torch.from_numpy(cu_k).to(cuda_device))
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    for s in (0, 7, pw.nseq - 1):
+        q0, nq, k0, nk = int(cu_q[s]), int(cu_q[s + 1] - cu_q[s]), int(cu_k[s]), int(cu_k[s + 1] - cu_k[s])
+        rows = sorted({0, 1, nq // 2, nq - 1, min(nq - 1, 127), min(nq - 1, 128)})
+        for h in (0, 21):
+            g = oracle.kv_head(h, pw.hq, pw.hkv)
+            kh = C.prefill_kv_head_np(w, "k", 0, g)[k0:k0 + nk]
+            vh = C.prefill_kv_head_np(w, "v", 0, g)[k0:k0 + nk]
+            qh = np.stack([C.prefill_q_rows_np(w, 0, h, q0 + r, 1)[0] for r in rows])
+            qp = [oracle.q_pos(r, nq, nk) for r in rows]
+            o_ref, lse_ref = oracle.attention_rows(qh, kh, vh, qp, pw.scale, True, 0)
+            got = o[0, h, [q0 + r for r in rows]].float().cpu().numpy()
+            assert_o_close(got, o_ref, f"packed s{s} h{h}")
+            assert_lse_close(lse[0, h, [q0 + r for r in rows]].cpu().numpy(), lse_ref,
+                             f"packed s{s} h{h}")

@@ -313,6 +313,60 @@ def decode_inputs_torch(w: DecodeWorkload, device, permute: bool = True):
     return out
 
 
+# Packed prefill: nseq sequences along the sequence axis of one batch, seeded query
+# lengths in [q_lo, q_hi] and cached-prefix lengths in [0, prefix_hi] (more keys than
+# queries), each sequence causal inside itself.
+@dataclass(frozen=True)
+class PackedPrefillWorkload:
+    name: str
+    hq: int
+    hkv: int
+    d: int
+    nseq: int
+    q_lo: int
+    q_hi: int
+    prefix_hi: int
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def offsets(self):
+        """(cu_q, cu_k) int32 [nseq + 1]."""
+        u = rng.u64_np(self.seed, 0, 2 * self.nseq)
+        nq = self.q_lo + (u[: self.nseq] % np.uint64(self.q_hi - self.q_lo + 1)).astype(np.int64)
+        pre = (u[self.nseq:] % np.uint64(self.prefix_hi + 1)).astype(np.int64)
+        cu_q = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+        cu_k = np.concatenate([[0], np.cumsum(nq + pre)]).astype(np.int32)
+        return cu_q, cu_k
+
+    def flops(self) -> float:
+        """4 d per allowed (query, key) pair: query i of a sequence with nq queries after
+        a prefix of p keys sees p + i + 1 keys."""
+        cu_q, cu_k = self.offsets()
+        nq = np.diff(cu_q).astype(np.float64)
+        pre = np.diff(cu_k).astype(np.float64) - nq
+        pairs = (nq * pre + nq * (nq + 1) / 2).sum()
+        return 4.0 * self.d * self.hq * pairs
+
+    def io_bytes(self) -> int:
+        cu_q, cu_k = self.offsets()
+        sq, skv = int(cu_q[-1]), int(cu_k[-1])
+        return 2 * self.hq * sq * self.d * 2 + 2 * self.hkv * skv * self.d * 2 + self.hq * sq * 4
+
+    def as_prefill(self) -> "PrefillWorkload":
+        """The b = 1 problem the sequences are packed into (for its input tensors)."""
+        cu_q, cu_k = self.offsets()
+        return PrefillWorkload(self.name, 1, self.hq, self.hkv, int(cu_q[-1]), int(cu_k[-1]),
+                               self.d, True, 0, seed=self.seed)
+
+
+PACKED_PREFILL = PackedPrefillWorkload("packed_prefill_h32kv8_d128_16seqs", 32, 8, 128, 16, 256,
+                                       4096, 1024, seed=0x9ACC)
+REGISTRY[PACKED_PREFILL.name] = PACKED_PREFILL
+
+
 # Attention-sink logits, one per query head (scaled-score units): a fixed cycle of a
 # neutral, moderate, dominant (e^9 and e^60 outweigh every key of an N(0,1) row),
 # negligible and absent (-inf) sink, so every regime of the sink is present in a run.
