@@ -18,6 +18,8 @@
 // more arithmetic than the CUDA cores deliver at HBM speed.  Slots past cache_len may
 // hold anything: their scores are replaced by -inf (select, so NaN never propagates)
 // and their V rows are zeroed in registers before the P.V product.
+#include <type_traits>
+
 #include "attn_internal.h"
 #include "attn_ptx.cuh"
 
@@ -506,22 +508,33 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                             vw[r][4 * c + 3] = x.w;
                         }
                     }
+                    // the keep masks only bite on edge tiles (the choice is per tile, so
+                    // warp-uniform): other tiles skip the 64 ANDs
+                    auto pv = [&](auto masked) {
 #pragma unroll
-                    for (int wd = 0; wd < kW; ++wd) {
-                        const uint32_t ab0 = __byte_perm(vw[0][wd], vw[1][wd], 0x5140);
-                        const uint32_t ab1 = __byte_perm(vw[0][wd], vw[1][wd], 0x7362);
-                        const uint32_t cd0 = __byte_perm(vw[2][wd], vw[3][wd], 0x5140);
-                        const uint32_t cd1 = __byte_perm(vw[2][wd], vw[3][wd], 0x7362);
-                        const int np = 4 * wd;
-                        mma_f16_16816(o[np], pa, e4m3x2_to_f16x2(ab0 & 0xffffu) & keep_lo,
-                                      e4m3x2_to_f16x2(cd0 & 0xffffu) & keep_hi);
-                        mma_f16_16816(o[np + 1], pa, e4m3x2_to_f16x2(ab0 >> 16) & keep_lo,
-                                      e4m3x2_to_f16x2(cd0 >> 16) & keep_hi);
-                        mma_f16_16816(o[np + 2], pa, e4m3x2_to_f16x2(ab1 & 0xffffu) & keep_lo,
-                                      e4m3x2_to_f16x2(cd1 & 0xffffu) & keep_hi);
-                        mma_f16_16816(o[np + 3], pa, e4m3x2_to_f16x2(ab1 >> 16) & keep_lo,
-                                      e4m3x2_to_f16x2(cd1 >> 16) & keep_hi);
-                    }
+                        for (int wd = 0; wd < kW; ++wd) {
+                            const uint32_t ab0 = __byte_perm(vw[0][wd], vw[1][wd], 0x5140);
+                            const uint32_t ab1 = __byte_perm(vw[0][wd], vw[1][wd], 0x7362);
+                            const uint32_t cd0 = __byte_perm(vw[2][wd], vw[3][wd], 0x5140);
+                            const uint32_t cd1 = __byte_perm(vw[2][wd], vw[3][wd], 0x7362);
+                            const uint32_t pairs[4][2] = {{ab0 & 0xffffu, cd0 & 0xffffu},
+                                                          {ab0 >> 16, cd0 >> 16},
+                                                          {ab1 & 0xffffu, cd1 & 0xffffu},
+                                                          {ab1 >> 16, cd1 >> 16}};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                uint32_t b0 = e4m3x2_to_f16x2(pairs[e][0]);
+                                uint32_t b1 = e4m3x2_to_f16x2(pairs[e][1]);
+                                if constexpr (decltype(masked)::value) {
+                                    b0 &= keep_lo;
+                                    b1 &= keep_hi;
+                                }
+                                mma_f16_16816(o[4 * wd + e], pa, b0, b1);
+                            }
+                        }
+                    };
+                    if (edge) pv(std::true_type{});
+                    else pv(std::false_type{});
                     continue;
                 }
                 // bf16: V through transposed ldmatrix
