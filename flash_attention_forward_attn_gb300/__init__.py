@@ -235,7 +235,7 @@ def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float 
 
 
 def _decode_marshal(q, k_cache, v_cache, block_table, cache_len, max_cache_len, o, lse,
-                    o_dtype, cache_dtype=None):
+                    o_dtype, cache_dtype=None, want_o=True):
     import torch
 
     _req(q, "q", torch.bfloat16)
@@ -262,9 +262,10 @@ def _decode_marshal(q, k_cache, v_cache, block_table, cache_len, max_cache_len, 
         num_pages, page, max_pages = 0, 0, 0
     if dk != d or cache_len.shape != (b,):
         raise ValueError("head_dim or cache_len shape mismatch")
-    if o is None:
-        o = torch.empty((b, hq, s_active, d), dtype=o_dtype or torch.bfloat16, device=dev)
-    _req(o, "o", o.dtype, dev)
+    if want_o:
+        if o is None:
+            o = torch.empty((b, hq, s_active, d), dtype=o_dtype or torch.bfloat16, device=dev)
+        _req(o, "o", o.dtype, dev)
     if lse is not None:
         _req(lse, "lse", torch.float32, dev)
     dims = (b, hq, hkv, d, s_active, page, max_pages, num_pages, max_cache_len)
@@ -368,9 +369,10 @@ def attn_append_kv(k_new, v_new, k_cache, v_cache, block_table, cache_len, *,
     if k_new.dim() != 4 or v_new.shape != k_new.shape:
         raise ValueError("k_new and v_new must be [b, hkv, s_active, d] with equal shapes")
     b, hkv, s_active, d = k_new.shape
-    q_like = torch.empty((b, hkv, s_active, d), dtype=torch.bfloat16, device=dev)
+    # the new tokens' shape stands in for q: one row per (sequence, kv head, new token)
     _, (_, _, hkv2, _, _, page, max_pages, num_pages, mcl) = _decode_marshal(
-        q_like, k_cache, v_cache, block_table, cache_len, max_cache_len, None, None, None)
+        k_new, k_cache, v_cache, block_table, cache_len, max_cache_len, None, None, None,
+        want_o=False)
     if hkv2 != hkv:
         raise ValueError("k_new and the cache disagree on kv heads")
     opts = _opts(None, hkv, dev, circular=circular, rope_inv_freq=rope_inv_freq, d=d)
