@@ -90,6 +90,8 @@ def load_library(build_if_missing: bool = False):
         lib.attn_fwd_decode_static_ws.restype = I
         lib.attn_gen_mask_decode.argtypes = [P, I, I, I, I, P, P]
         lib.attn_gen_mask_decode.restype = I
+        lib.attn_check_wait_timeout.argtypes = [ctypes.c_longlong, P]
+        lib.attn_check_wait_timeout.restype = I
         lib.attn_get_device_error.argtypes = [P]
         lib.attn_get_device_error.restype = I
         lib.attn_status_string.argtypes = [I]
@@ -141,6 +143,13 @@ def _dtype_code(dtype):
 
 def attn_status_string(status: int) -> str:
     return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_check_wait_timeout(wait_cycles: int, stream=None) -> None:
+    """Launch the failure-path check: a bounded wait on a phase nothing completes, which
+    sets the device timeout word (read it with attn_get_device_error)."""
+    _check(load_library().attn_check_wait_timeout(int(wait_cycles), _stream_ptr(stream)),
+           "attn_check_wait_timeout")
 
 
 def attn_get_device_error(stream=None) -> int:

@@ -303,6 +303,11 @@ attn_status attn_gen_mask_decode(const int32_t* cache_len, int b, int hq, int s_
                                  static_cast<cudaStream_t>(stream));
 }
 
+attn_status attn_check_wait_timeout(long long wait_cycles, void* stream) {
+    if (wait_cycles <= 0 || wait_cycles > (1ll << 33)) return ATTN_ERR_INVALID_ARG;
+    return attn::wait_timeout_check_launch(wait_cycles, static_cast<cudaStream_t>(stream));
+}
+
 attn_status attn_get_device_error(void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;

@@ -99,6 +99,7 @@ bool make_u8_map(CUtensorMap* map, const void* base, int rank, const uint64_t* d
 attn_status prefill_launch(const PrefillArgs& a, cudaStream_t stream);
 attn_status decode_launch(const DecodeArgs& a, cudaStream_t stream);
 attn_status append_launch(const AppendArgs& a, cudaStream_t stream);
+attn_status wait_timeout_check_launch(long long wait_cycles, cudaStream_t stream);
 attn_status gen_mask_launch(const int32_t* cache_len, int b, int hq, int s_active, int max_len,
                             uint8_t* mask, cudaStream_t stream);
 

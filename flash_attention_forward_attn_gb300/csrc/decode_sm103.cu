@@ -718,6 +718,19 @@ __global__ void append_kv_kernel(const __nv_bfloat16* __restrict__ k_new,
     v_cache[row * a.d + i + h] = v_new[src + i + h];
 }
 
+// A check of the failure path: one thread waits, with the kernels' bounded wait, on an
+// mbarrier phase that nothing completes.  After wait_cycles it gives up, sets the device
+// timeout word like a stalled pipeline would, and returns; the context stays usable.
+__global__ void wait_timeout_check_kernel(long long wait_cycles) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, &abort_flag, wait_cycles)) atomicOr(&g_decode_error, kDevErrTimeout);
+}
+
 // The 0/1 decode mask, one byte per (sequence, head, new token, cache position).
 __global__ void gen_mask_kernel(const int32_t* __restrict__ cache_len, int hq, int s_active,
                                 int max_len, uint8_t* __restrict__ mask, long long total) {
@@ -825,6 +838,12 @@ attn_status append_launch(const AppendArgs& a, cudaStream_t stream) {
     append_kv_kernel<<<grid, a.d / 2, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.k_new), static_cast<const __nv_bfloat16*>(a.v_new),
         static_cast<__nv_bfloat16*>(a.k_cache), static_cast<__nv_bfloat16*>(a.v_cache), a);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status wait_timeout_check_launch(long long wait_cycles, cudaStream_t stream) {
+    wait_timeout_check_kernel<<<1, 32, 0, stream>>>(wait_cycles);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

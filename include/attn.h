@@ -302,6 +302,17 @@ attn_status attn_gen_mask_decode(const int32_t* cache_len, int b, int hq, int s_
                                  int max_len, uint8_t* mask_out, void* stream);
 
 /*
+ * attn_check_wait_timeout -- a test export of the failure path.  The library's kernels
+ * never trap: every pipeline wait is bounded, and a wait that runs out sets a device error
+ * word and unwinds.  This call launches one thread that waits, with the same bounded wait,
+ * on an mbarrier phase that nothing completes, gives up after wait_cycles SM clock cycles
+ * (1 .. 2^33), sets the timeout word and returns.  attn_get_device_error() then reports
+ * ATTN_ERR_DEVICE_TIMEOUT and the context stays usable.  Returns INVALID_ARG for a
+ * wait_cycles outside its range, CUDA if the launch fails.
+ */
+attn_status attn_check_wait_timeout(long long wait_cycles, void* stream);
+
+/*
  * attn_get_device_error -- synchronise `stream`, then read and clear the device error
  * words of every kernel in the library on the current device.  Returns ATTN_OK, or the
  * most severe of ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_PAGE_OOB, ATTN_ERR_CACHE_LEN; returns

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
         "attn_fwd_prefill", "attn_decode_workspace_bytes", "attn_fwd_decode",
         "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
         "attn_fwd_decode_static_ws", "attn_fwd_prefill_ex", "attn_fwd_decode_ex",
-        "attn_append_kv"])
+        "attn_append_kv", "attn_check_wait_timeout"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -195,3 +195,9 @@ def test_append_rejects_before_launch(lib):
     assert app(opts=ctypes.byref(A.AttnOpts(circular=1))) == 1  # a paged cache cannot be circular
     assert app(opts=ctypes.byref(A.AttnOpts(kv_dtype=1, k_scale=1.0, v_scale=1.0))) == 2
     assert app(v=ctypes.c_void_p((1 << 20) + 8)) == 1
+
+
+def test_wait_timeout_check_rejects_bad_limits(lib):
+    assert lib.attn_check_wait_timeout(0, None) == 1
+    assert lib.attn_check_wait_timeout(-5, None) == 1
+    assert lib.attn_check_wait_timeout((1 << 33) + 1, None) == 1

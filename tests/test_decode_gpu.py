@@ -150,3 +150,23 @@ def test_gen_mask_full_size(cuda_device):
     m = A.attn_gen_mask_decode(torch.from_numpy(lens).to(cuda_device), 4, w.s_active, w.len_hi)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(m.cpu().numpy(), oracle.decode_mask(lens, 4, w.s_active, w.len_hi))
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(cuda_device):
+    """The failure path without a fault: a bounded wait on a phase nothing completes gives
+    up, sets the timeout word (ATTN_ERR_DEVICE_TIMEOUT), and the library keeps working."""
+    import time
+
+    import flash_attention_forward_attn_gb300 as A
+
+    t0 = time.perf_counter()
+    A.attn_check_wait_timeout(20_000_000)  # about 10 ms of SM clock
+    assert A.attn_get_device_error() == 5  # ATTN_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    assert A.attn_get_device_error() == 0  # reading clears it
+    w = C.DecodeWorkload("after_timeout", 2, 8, 2, 128, 1, len_hi=300, fixed_lens=(100, 257),
+                         seed=13)
+    t = C.decode_inputs_torch(w, cuda_device)
+    o, lse = run_decode(t, w)
+    o_ref, lse_ref = oracle_of(t, w)
+    assert_o_close(o.cpu().numpy(), o_ref, "after timeout")
