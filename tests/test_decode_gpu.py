@@ -170,3 +170,18 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(cuda_device):
     o, lse = run_decode(t, w)
     o_ref, lse_ref = oracle_of(t, w)
     assert_o_close(o.cpu().numpy(), o_ref, "after timeout")
+
+
+@pytest.mark.parametrize("d,sa,paged", [(128, 1, True), (128, 4, True), (64, 3, False),
+                                        (256, 2, True)])
+def test_decode_cache_length_residue_sweep(d, sa, paged, cuda_device):
+    """Cache lengths around the 32-token tile and the split length (kv_chunk 64): every
+    sequence of the batch sits at another residue."""
+    lens = tuple(max(sa, n) for n in (1, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129, 200))
+    w = C.DecodeWorkload(f"residues_{d}_{sa}_{paged}", len(lens), 8, 2, d, sa, len_hi=max(lens) + 3,
+                         paged=paged, fixed_lens=lens, seed=0x5EE1 + d + sa)
+    t = C.decode_inputs_torch(w, cuda_device)
+    o, lse = run_decode(t, w, kv_chunk=64)
+    o_ref, lse_ref = oracle_of(t, w)
+    assert_o_close(o.cpu().numpy(), o_ref, w.name)
+    assert_lse_close(lse.cpu().numpy(), lse_ref, w.name)

@@ -172,3 +172,22 @@ def test_full_gqa_prefill_32k_outliers_sampled(cuda_device):
 
 def test_full_swa_prefill_8k_d256_sampled(cuda_device):
     _check_full(C.SWA_PREFILL_8K, cuda_device, [(0, 0), (1, 17), (1, 31)])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_prefill_tile_boundary_residue_sweep(d, causal, cuda_device):
+    """Every combination of query and key lengths around the 128-row query tile and the
+    64/128-key KV tile (1, one below, at and above each boundary), compared on every row."""
+    sqs = (1, 2, 127, 128, 129, 255, 257)
+    skvs = (1, 63, 64, 65, 128, 129, 256, 385)
+    for sq in sqs:
+        for skv in skvs:
+            name = f"sweep_d{d}_c{int(causal)}_q{sq}_k{skv}"
+            w = C.PrefillWorkload(name, 1, 2, 1, sq, skv, d, causal, 0, seed=0x5EE0 + sq * 1000 + skv)
+            qb, kb, vb = C.prefill_inputs_np(w)
+            q, k, v = (tensor_of_bits(x, cuda_device) for x in (qb, kb, vb))
+            o, lse = run_gpu(q, k, v, causal, 0, w.scale, torch.float32)
+            o_ref, lse_ref = oracle.prefill(qb, kb, vb, w.scale, causal, 0)
+            assert_o_close(o.cpu().numpy(), o_ref, name)
+            assert_lse_close(lse.cpu().numpy(), lse_ref, name)
