@@ -63,6 +63,20 @@ __device__ __forceinline__ int decode_first_slot(int len, int s_active, int wind
     return (window > 0 && !circular) ? (max(0, len - s_active - window + 1) & ~31) : 0;
 }
 
+// The slots a sequence reads, [first, nslots), are cut into ceil(span / chunk) splits of
+// near-equal size in whole 32-token tiles (never longer than chunk, so at most
+// ceil(max_cache_len / chunk) splits): split s covers [lo, hi), empty when lo >= hi.
+__device__ __forceinline__ int decode_nsplits(int nslots, int first, int chunk) {
+    return (nslots - first + chunk - 1) / chunk;
+}
+__device__ __forceinline__ void decode_split_range(int nslots, int first, int chunk, int s,
+                                                   int& lo, int& hi) {
+    const int ns = decode_nsplits(nslots, first, chunk);
+    const int size = (((nslots - first) + ns - 1) / ns + 31) & ~31;
+    lo = first + s * size;
+    hi = min(nslots, lo + size);
+}
+
 // Logical position held by slot r of a circular cache of cap rows whose newest position
 // is len - 1 (r < min(len, cap)).
 __device__ __forceinline__ int circular_pos(int r, int len, int cap) {
@@ -195,9 +209,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
     // this split covers cache slots [tok0, tok1); the combine skips the splits that return here
     const int nslots = decode_nslots(len, p.circular, p.max_cache_len);
     const int first = decode_first_slot(len, p.s_active, p.window, p.circular);
-    const int tok1 = min(nslots, (split + 1) * p.chunk);
-    const int tok0 = max(split * p.chunk, first);
-    if (tok0 >= tok1) return;  // the sequence is shorter than the split, or it precedes the window
+    if (split >= decode_nsplits(nslots, first, p.chunk)) return;  // a split this sequence lacks
+    int tok0, tok1;
+    decode_split_range(nslots, first, p.chunk, split, tok0, tok1);
+    if (tok0 >= tok1) return;  // an empty last split
     const int nblocks = (tok1 - tok0 + kBT - 1) / kBT;
 
     if (threadIdx.x == 0) {
@@ -640,9 +655,15 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __rest
     const int len = cache_len[b];
     float out = 0.f, lse_v = -INFINITY;
     if (len >= s_active && (circular || len <= max_cache_len)) {
-        // the splits that ran: those with a slot in [first, nslots) (as decode_split_kernel)
-        const int s0 = decode_first_slot(len, s_active, window, circular) / chunk;
-        const int ns = (decode_nslots(len, circular, max_cache_len) + chunk - 1) / chunk;
+        // the splits that ran (as decode_split_kernel): the non-empty ones
+        const int first = decode_first_slot(len, s_active, window, circular);
+        const int nslots = decode_nslots(len, circular, max_cache_len);
+        int ns = decode_nsplits(nslots, first, chunk);
+        for (int lo, hi; ns > 0; --ns) {  // drop an empty last split
+            decode_split_range(nslots, first, chunk, ns - 1, lo, hi);
+            if (lo < hi) break;
+        }
+        const int s0 = 0;
         const float* ml = part_ml + rowid * max_splits * 2;
         float M = -INFINITY;
         for (int s = s0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
