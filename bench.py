@@ -273,7 +273,8 @@ def packed_prefill_entry(pw, dev, steps, warmup, flush, stream, peaks, world):
     achieved = flops / (mean_ms / 1e3) / 1e12
     ent = {
         "workload": pw.name, "value": value / 1e12, "unit": "TFLOP/s", "ms_per_step": mean_ms,
-        "ms_min": min(ms), "flops_per_step": flops, "steps": steps, "gpu_launches": steps,
+        "ms_min": min(ms), "flops_per_step": flops, "steps": steps,
+        "gpu_launches": 2 * steps,  # the work-order pass and the prefill kernel
         "packing": {"nseq": pw.nseq, "sq": w.sq, "skv": w.skv},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,

@@ -17,6 +17,7 @@ import threading
 __all__ = [
     "AttnError", "ATTN_BF16", "ATTN_F32", "library_path", "load_library",
     "attn_fwd_prefill", "attn_fwd_decode", "attn_decode_workspace_bytes",
+    "attn_prefill_workspace_bytes",
     "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
     "attn_fwd_decode_static_ws",
 ]
@@ -51,7 +52,9 @@ class AttnOpts(ctypes.Structure):
                 ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
                 ("window", ctypes.c_int), ("circular", ctypes.c_int),
                 ("rope_inv_freq", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p),
-                ("cu_seqlens_k", ctypes.c_void_p), ("nseq", ctypes.c_int)]
+                ("cu_seqlens_k", ctypes.c_void_p), ("nseq", ctypes.c_int),
+                ("prefill_workspace", ctypes.c_void_p),
+                ("prefill_workspace_bytes", ctypes.c_size_t)]
 
 
 def load_library(build_if_missing: bool = False):
@@ -75,6 +78,8 @@ def load_library(build_if_missing: bool = False):
         lib.attn_fwd_prefill.restype = I
         lib.attn_fwd_prefill_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, O, P]
         lib.attn_fwd_prefill_ex.restype = I
+        lib.attn_prefill_workspace_bytes.argtypes = [I]
+        lib.attn_prefill_workspace_bytes.restype = S
         lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
         lib.attn_decode_workspace_bytes.restype = S
         lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, I, I, P,
@@ -215,11 +220,13 @@ def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | N
 
 def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
                         o=None, lse=None, o_dtype=None, sink=None, cu_seqlens_q=None,
-                        cu_seqlens_k=None, stream=None):
+                        cu_seqlens_k=None, balance: bool = True, stream=None):
     """attn_fwd_prefill with the attn_opts options: sink, an fp32 [hq] tensor of
     per-query-head sink logits (scaled-score units) on q's device, or None; and packed
     sequences: cu_seqlens_q / cu_seqlens_k int32 [nseq + 1] offsets along sq and skv of a
-    b = 1 problem (each sequence its own problem, queries at the tail of its keys)."""
+    b = 1 problem (each sequence its own problem, queries at the tail of its keys).  With
+    packed sequences and balance, a scratch buffer is allocated for the library's work
+    order (query tiles by KV-tile count); results do not depend on it."""
     import torch
 
     lib = load_library()
@@ -235,6 +242,13 @@ def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float 
         opts.cu_seqlens_q = cu_seqlens_q.data_ptr()
         opts.cu_seqlens_k = cu_seqlens_k.data_ptr()
         opts.nseq = cu_seqlens_q.shape[0] - 1
+        if balance and sq > 0:
+            nbytes = lib.attn_prefill_workspace_bytes(sq)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+            if stream is not None:
+                ws.record_stream(stream)  # freed only once the call on `stream` is done
+            opts.prefill_workspace = ws.data_ptr()
+            opts.prefill_workspace_bytes = nbytes
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     _check(lib.attn_fwd_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, hq, hkv, sq,
                                    skv, d, sc, int(bool(causal)), int(window),
@@ -297,6 +311,10 @@ def attn_fwd_decode_static_ws(q, k_cache, v_cache, block_table, cache_len, *,
                                          _dtype_code(o.dtype), kv_chunk, _stream_ptr(stream)),
            "attn_fwd_decode_static_ws")
     return o, lse
+
+
+def attn_prefill_workspace_bytes(sq: int) -> int:
+    return int(load_library().attn_prefill_workspace_bytes(sq))
 
 
 def attn_decode_workspace_bytes(b: int, hq: int, s_active: int, d: int, max_cache_len: int,

@@ -74,6 +74,8 @@ struct Opts {
     const int32_t* cu_q = nullptr;
     const int32_t* cu_k = nullptr;
     int nseq = 0;
+    void* pws = nullptr;  // packed-prefill work-order scratch
+    size_t pws_bytes = 0;
 };
 
 bool read_opts(const attn_opts* opts, Opts* o) {
@@ -99,8 +101,13 @@ bool read_opts(const attn_opts* opts, Opts* o) {
         if (!o->cu_q || !o->cu_k || !aligned4(o->cu_q) || !aligned4(o->cu_k) || o->nseq < 1)
             return false;
     }
+    o->pws = opts->prefill_workspace;
+    o->pws_bytes = opts->prefill_workspace_bytes;
+    if (o->pws && !aligned4(o->pws)) return false;
     return true;
 }
+
+size_t prefill_ws_bytes(int sq) { return sq <= 0 ? 0 : (size_t)((sq + 127) / 128) * 4; }
 
 // Paged-cache arguments shared by decode and append.
 bool paged_args_ok(int page_size, int num_pages, int max_pages_per_seq, int max_cache_len) {
@@ -163,6 +170,7 @@ attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, voi
     // cache are decode options
     if (op.e4m3 || op.window != 0 || op.circular || op.rope) return ATTN_ERR_UNSUPPORTED;
     if (op.cu_q && b != 1) return ATTN_ERR_INVALID_ARG;  // packing is along one batch's rows
+    if (op.pws && (!op.cu_q || op.pws_bytes < prefill_ws_bytes(sq))) return ATTN_ERR_INVALID_ARG;
     if (sq == 0) return ATTN_OK;
     if (!q || !o || (skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o) || (skv > 0 && (!aligned16(k) || !aligned16(v))))
@@ -170,7 +178,7 @@ attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, voi
     if ((long long)b * hq > 0x7fffffffLL || (long long)b * hkv > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
     attn::PrefillArgs a{q, k, v, o, lse, b, hq, hkv, sq, skv, d, scale, causal ? 1 : 0, window,
-                        o_dtype, op.sink, op.cu_q, op.cu_k, op.nseq};
+                        o_dtype, op.sink, op.cu_q, op.cu_k, op.nseq, static_cast<int*>(op.pws)};
     return attn::prefill_launch(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -180,6 +188,8 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* 
     return attn_fwd_prefill_ex(q, k, v, o, lse, b, hq, hkv, sq, skv, d, scale, causal, window,
                                o_dtype, nullptr, stream);
 }
+
+size_t attn_prefill_workspace_bytes(int sq) { return prefill_ws_bytes(sq); }
 
 size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_cache_len,
                                    int kv_chunk) {
@@ -209,7 +219,7 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
     Opts op;
     if (!read_opts(opts, &op)) return ATTN_ERR_INVALID_ARG;
     if (op.e4m3 && d == 64) return ATTN_ERR_UNSUPPORTED;  // half a 128-byte box per row
-    if (op.cu_q) return ATTN_ERR_UNSUPPORTED;  // packed sequences are a prefill option
+    if (op.cu_q || op.pws) return ATTN_ERR_UNSUPPORTED;  // prefill options
     // a circular cache is a flat ring that holds every new token's window
     if (op.circular && (block_table || op.window == 0 ||
                         (long long)op.window + s_active - 1 > max_cache_len || max_cache_len % 32 != 0))

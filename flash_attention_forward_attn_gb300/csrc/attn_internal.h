@@ -32,6 +32,7 @@ struct PrefillArgs {
     const int32_t* cu_seqlens_q;  // packed sequences: [nseq + 1] offsets, or NULL
     const int32_t* cu_seqlens_k;
     int nseq;
+    int* order;  // packed: scratch of one int per query tile for the work order, or NULL
 };
 
 struct DecodeArgs {

@@ -64,6 +64,7 @@ struct PrefillParams {
     const int* cu_q;
     const int* cu_k;
     int nseq;
+    const int* order;  // packed: query units heaviest first (unit_order_kernel), or NULL
     int hq, hkv, sq, skv, group, nqt, window, causal, o_f32;
     int nbh;     // b * hq
     int nunits;  // work units of the persistent kernel
@@ -162,6 +163,47 @@ __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) 
     return r;
 }
 
+// Packed sequences: the query units (a 128-row tile, or a pair of them) ordered by their
+// KV-tile count, most first, ties by index.  Unit indices in the persistent kernels then
+// run through this list, so the zig-zag pairs heavy with light units on every CTA as it
+// does for one causal problem, where the index order already is the order of the work.
+// One CTA; the (count, index) keys are sorted by a bitonic network in shared memory.
+constexpr int kOrderMax = 8192;  // units sorted in one CTA (64 KB of keys)
+constexpr int kOrderThreads = 1024;
+
+template <int BN, int kTilesPerUnit>
+__global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const PrefillParams p, int nu,
+                                                                   int* order) {
+    extern __shared__ unsigned long long keys[];
+    int n2 = 1;
+    while (n2 < nu) n2 <<= 1;
+    for (int u = threadIdx.x; u < n2; u += blockDim.x) {
+        unsigned long long key = ~0ull;  // padding sorts last
+        if (u < nu) {
+            int cost = 0;
+            for (int x = 0; x < kTilesPerUnit; ++x) cost += tile_range<BN, true>(p, kTilesPerUnit * u + x).n;
+            key = ((unsigned long long)(0x7fffffff - cost) << 32) | (unsigned)u;
+        }
+        keys[u] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long a = keys[i], b = keys[l];
+                    if ((a > b) == ((i & k) == 0)) {  // ascending where bit k of i is clear
+                        keys[i] = b;
+                        keys[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    for (int u = threadIdx.x; u < nu; u += blockDim.x) order[u] = (int)(keys[u] & 0xffffffffu);
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag) {
     return mbar_wait(bar, parity, reinterpret_cast<volatile int*>(abort_flag));
 }
@@ -240,7 +282,9 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
 
     // unit w -> (query tile, batch*head, kv batch*head) and its KV tile range
     auto unit_at = [&](int w, int& bh, int& kvz) -> TileRange {
-        const int qt = p.nqt - 1 - w / p.nbh;
+        int qt = p.nqt - 1 - w / p.nbh;
+        if constexpr (kPacked)
+            if (p.order) qt = __ldg(p.order + w / p.nbh);
         bh = w % p.nbh;
         const int bidx = bh / p.hq, h = bh % p.hq;
         kvz = bidx * p.hkv + h / p.group;
@@ -714,7 +758,9 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     };
     auto unit_at = [&](int w) -> Unit {
         Unit u;
-        const int pair = npairs - 1 - w / p.nbh;
+        int pair = npairs - 1 - w / p.nbh;
+        if constexpr (kPacked)
+            if (p.order) pair = __ldg(p.order + w / p.nbh);
         u.bh = w % p.nbh;
         const int bidx = u.bh / p.hq, h = u.bh % p.hq;
         u.kvz = bidx * p.hkv + h / p.group;
@@ -1189,6 +1235,26 @@ int num_sms() {
     return cached[dev];
 }
 
+// Writes the packed work order into `order` (nu <= kOrderMax ints) on the stream.
+template <int BN, int kTilesPerUnit>
+bool unit_order_launch(const PrefillParams& p, int nu, int* order, cudaStream_t stream) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(unit_order_kernel<BN, kTilesPerUnit>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kOrderMax * (int)sizeof(unsigned long long)) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        attr_set = true;
+    }
+    int n2 = 1;
+    while (n2 < nu) n2 <<= 1;
+    unit_order_kernel<BN, kTilesPerUnit><<<1, kOrderThreads, n2 * sizeof(unsigned long long), stream>>>(
+        p, nu, order);
+    return cudaGetLastError() == cudaSuccess;
+}
+
 template <int D, bool kPacked>
 attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
@@ -1214,6 +1280,12 @@ attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, con
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     PrefillParams pp = p;
     pp.nunits = (int)units;
+    if constexpr (kPacked) {
+        if (a.order && p.nqt <= kOrderMax) {
+            if (!unit_order_launch<C::BN, 1>(p, p.nqt, a.order, stream)) return ATTN_ERR_CUDA;
+            pp.order = a.order;
+        }
+    }
     const int grid = (int)(units < num_sms() ? units : num_sms());
     prefill_wide_kernel<D, kPacked><<<grid, C::kThreads, C::kDynBytes, stream>>>(tq, tk, tv, pp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
@@ -1245,6 +1317,13 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     PrefillParams pp = p;
     pp.nunits = (int)units;
+    if constexpr (kPacked) {
+        const int npairs = (p.nqt + 1) / 2;
+        if (a.order && npairs <= kOrderMax) {
+            if (!unit_order_launch<C::BN, 2>(p, npairs, a.order, stream)) return ATTN_ERR_CUDA;
+            pp.order = a.order;
+        }
+    }
     const int grid = (int)(units < num_sms() ? units : num_sms());
     CUtensorMap to;  // bf16 O for the TMA stores (unused, never dereferenced, for fp32 O)
     if (a.o_dtype == ATTN_BF16) {
@@ -1283,6 +1362,7 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     p.cu_q = a.cu_seqlens_q;
     p.cu_k = a.cu_seqlens_k;
     p.nseq = a.nseq;
+    p.order = nullptr;
     p.hq = a.hq;
     p.hkv = a.hkv;
     p.sq = a.sq;

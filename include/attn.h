@@ -111,6 +111,14 @@ typedef enum { ATTN_KV_BF16 = 0, ATTN_KV_E4M3 = 1 } attn_kv_dtype;
  *          cached prefix), the causal and window masks apply inside it, and no row sees a
  *          key of another sequence.  Offsets that break these rules give unspecified
  *          results but no out-of-range access.  NULL = one problem per (batch, head).
+ *   prefill_workspace, prefill_workspace_bytes : packed prefill only; NULL / 0 otherwise.
+ *          A DEVICE scratch buffer of at least attn_prefill_workspace_bytes(sq) bytes,
+ *          4-byte aligned, owned by the caller and not read by it until the stream has
+ *          passed the call.  With it, a small pass first orders the query tiles by their
+ *          KV-tile count, most first, so that the persistent kernel's zig-zag hands every
+ *          CTA a near-equal share when sequence lengths differ.  Results are the same with
+ *          or without it (each tile is computed the same way wherever it runs); without it
+ *          the tiles keep their index order.  Ignored for more than 8192 units of work.
  */
 typedef struct {
     const float* sink;
@@ -123,6 +131,8 @@ typedef struct {
     const int32_t* cu_seqlens_q;
     const int32_t* cu_seqlens_k;
     int nseq;
+    void* prefill_workspace;
+    size_t prefill_workspace_bytes;
 } attn_opts;
 
 /*
@@ -161,13 +171,21 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* 
  * attn_fwd_prefill_ex -- attn_fwd_prefill with the options of attn_opts (NULL = none):
  * same arguments, layouts, semantics and errors, plus ATTN_ERR_INVALID_ARG for an
  * invalid option (a misaligned sink pointer; packed sequences with b != 1, nseq < 1 or
- * a missing or misaligned offset array) and ATTN_ERR_UNSUPPORTED for a decode option
- * (an e4m3 kv_dtype, window, circular or rope_inv_freq).
+ * a missing or misaligned offset array; a prefill workspace without packed sequences,
+ * misaligned or smaller than attn_prefill_workspace_bytes(sq)) and ATTN_ERR_UNSUPPORTED
+ * for a decode option (an e4m3 kv_dtype, window, circular or rope_inv_freq).
  */
 attn_status attn_fwd_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int b, int hq, int hkv, int sq, int skv, int d, float scale,
                                 int causal, int window, attn_dtype o_dtype,
                                 const attn_opts* opts, void* stream);
+
+/*
+ * attn_prefill_workspace_bytes -- bytes of the optional packed-prefill scratch
+ * (attn_opts.prefill_workspace) for sq query rows: 4 bytes per 128-row query tile.
+ * Returns 0 for sq <= 0.
+ */
+size_t attn_prefill_workspace_bytes(int sq);
 
 /*
  * attn_decode_workspace_bytes -- bytes of caller-provided scratch that attn_fwd_decode
@@ -228,7 +246,8 @@ attn_status attn_fwd_decode(const void* q, const void* k_cache, const void* v_ca
  * plus ATTN_ERR_INVALID_ARG for an invalid option (a misaligned sink or rope_inv_freq
  * pointer, an unknown kv_dtype, a non-finite scale of an e4m3 cache, a negative window, a
  * circular paged cache or a circular cache whose window does not fit) and
- * ATTN_ERR_UNSUPPORTED for an e4m3 cache with d = 64.  With circular, cache_len[b] may
+ * ATTN_ERR_UNSUPPORTED for an e4m3 cache with d = 64 or a prefill option (packed
+ * sequences or a prefill workspace).  With circular, cache_len[b] may
  * exceed max_cache_len.  The sink is applied where the split-KV chunks are merged and the
  * scales are folded into the chunk pass, so the workspace size is the same for every
  * option.

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
         "attn_fwd_prefill", "attn_decode_workspace_bytes", "attn_fwd_decode",
         "attn_gen_mask_decode", "attn_get_device_error", "attn_status_string",
         "attn_fwd_decode_static_ws", "attn_fwd_prefill_ex", "attn_fwd_decode_ex",
-        "attn_append_kv", "attn_check_wait_timeout"])
+        "attn_append_kv", "attn_check_wait_timeout", "attn_prefill_workspace_bytes"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -130,6 +130,16 @@ def test_ex_calls_check_their_options_before_launch(lib):
     b2 = args[:5] + (2,) + args[6:]  # packing needs b = 1
     assert lib.attn_fwd_prefill_ex(*b2, op(cu_seqlens_q=cu, cu_seqlens_k=cu, nseq=1), None) == 1
     assert call(dargs, op(cu_seqlens_q=cu, cu_seqlens_k=cu, nseq=1)) == 2  # a prefill option
+    # the packed-prefill work-order scratch: only with packing, 4-byte aligned, large enough
+    packed = dict(cu_seqlens_q=cu, cu_seqlens_k=cu, nseq=1)
+    a16 = args[:8] + (16,) + args[9:]  # sq = 16: every call below must fail validation
+    assert lib.attn_fwd_prefill_ex(*a16, op(prefill_workspace=cu, prefill_workspace_bytes=64),
+                                   None) == 1
+    assert lib.attn_fwd_prefill_ex(*a16, op(prefill_workspace=cu + 2, prefill_workspace_bytes=64,
+                                             **packed), None) == 1
+    assert lib.attn_fwd_prefill_ex(*a16, op(prefill_workspace=cu, prefill_workspace_bytes=3,
+                                             **packed), None) == 1  # sq = 16 needs 4 bytes
+    assert call(dargs, op(prefill_workspace=cu, prefill_workspace_bytes=64)) == 2
     # an invalid size is still reported first, with or without options
     dbad = dargs[:8] + (80,) + dargs[9:]  # d = 80
     assert lib.attn_fwd_decode_ex(*dbad, ctypes.byref(none), FAKE, 1 << 30, None) == 2
@@ -201,3 +211,9 @@ def test_wait_timeout_check_rejects_bad_limits(lib):
     assert lib.attn_check_wait_timeout(0, None) == 1
     assert lib.attn_check_wait_timeout(-5, None) == 1
     assert lib.attn_check_wait_timeout((1 << 33) + 1, None) == 1
+
+
+def test_prefill_workspace_bytes(lib):
+    """One int per 128-row query tile."""
+    for sq, n in [(-5, 0), (0, 0), (1, 4), (128, 4), (129, 8), (34910, 4 * 273)]:
+        assert A.attn_prefill_workspace_bytes(sq) == n

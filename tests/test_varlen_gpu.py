@@ -25,7 +25,8 @@ def packed_lengths(seed, nseq, q_hi, prefix_hi):
     return cu_q, cu_k
 
 
-def run_varlen(cu_q, cu_k, hq, hkv, d, causal, window, out, seed, dev, sink=None):
+def run_varlen(cu_q, cu_k, hq, hkv, d, causal, window, out, seed, dev, sink=None,
+               balance=True):
     import flash_attention_forward_attn_gb300 as A
 
     w = C.PrefillWorkload("varlen", 1, hq, hkv, int(cu_q[-1]), int(cu_k[-1]), d, causal, window,
@@ -36,7 +37,7 @@ def run_varlen(cu_q, cu_k, hq, hkv, d, causal, window, out, seed, dev, sink=None
     o, _ = A.attn_fwd_prefill_ex(q, k, v, causal=causal, window=window, scale=w.scale, lse=lse,
                                  o_dtype=out, sink=sink,
                                  cu_seqlens_q=torch.from_numpy(cu_q).to(dev),
-                                 cu_seqlens_k=torch.from_numpy(cu_k).to(dev))
+                                 cu_seqlens_k=torch.from_numpy(cu_k).to(dev), balance=balance)
     torch.cuda.synchronize()
     assert A.attn_get_device_error() == 0
     return (qb, kb, vb, w), o, lse
@@ -86,6 +87,24 @@ def test_varlen_one_sequence_is_bit_identical_to_plain_prefill(d, cuda_device):
     l2 = torch.empty_like(l1)
     o2, _ = A.attn_fwd_prefill(q, k, v, causal=True, scale=w.scale, lse=l2)
     torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d,hq,hkv,packing,causal,window", [
+    (128, 8, 2, (40, 300, 200), True, 0),
+    (64, 16, 4, (60, 400, 64), True, 0),
+    (128, 4, 4, (20, 500, 300), False, 0),  # every tile of a sequence ties
+    (256, 4, 2, (24, 260, 100), True, 64),
+])
+def test_work_order_leaves_results_bit_identical(d, hq, hkv, packing, causal, window,
+                                                 cuda_device):
+    """The work-order pass only decides which CTA runs a query tile and when; every tile is
+    computed the same way, so results are bit-identical with and without it."""
+    cu_q, cu_k = packed_lengths(0xB0 + d, *packing)
+    _, o1, l1 = run_varlen(cu_q, cu_k, hq, hkv, d, causal, window, torch.bfloat16, 0x7D0 + d,
+                           cuda_device, balance=True)
+    _, o2, l2 = run_varlen(cu_q, cu_k, hq, hkv, d, causal, window, torch.bfloat16, 0x7D0 + d,
+                           cuda_device, balance=False)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
