@@ -217,10 +217,11 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
 // =========================================================================== head_dim 256
 // Shared-memory / TMEM plan of the head_dim-256 kernel (BN = 64).  Shared memory: the Q
 // tile (64 KB), a 3-slot K ring and a 2-slot V ring (32 KB slots).  TMEM:
-//   S0 [0, BN)  S1 [BN, 2BN)  P0 [2BN, 2BN + BN/2)  P1 [2BN + BN/2, 3BN)  O [256, 256 + D)
+//   S0 [0, BN)  S1 [BN, 2BN)  P0..P3 [2BN + i BN/2, 2BN + (i+1) BN/2)  O [256, 256 + D)
 // P(T) has columns of its own, so S(T+2) may overwrite S buffer T % 2 as soon as the
 // softmax has read S(T), while PV(T) still reads P(T): the S products and the PV products
-// form two independent chains.
+// form two independent chains.  Four P buffers let the softmax run four tiles ahead of
+// P.V, which covers the wait of a unit's first P.V for the epilogue to read O out.
 template <int D>
 struct CfgW {
     static constexpr int BN = 64;
@@ -234,10 +235,11 @@ struct CfgW {
     static constexpr int kSmem = kVOff + kVSlots * kSlotBytes;
     static constexpr int kDynBytes = kSmem + 1024;
     static constexpr int kTmemCols = 512;
-    static constexpr uint32_t kColP = 2 * BN;  // P buffers at [2 BN, 3 BN)
+    static constexpr int kPBufs = 4;           // P buffers: the softmax runs this far ahead of P.V
+    static constexpr uint32_t kColP = 2 * BN;  // P buffers at [2 BN, 2 BN + kPBufs BN / 2)
     static constexpr uint32_t kColO = 256;     // O at [256, 256 + D)
     static constexpr int kThreads = 512;
-    static_assert(3 * BN <= (int)kColO && kColO + D <= kTmemCols, "TMEM budget");
+    static_assert(2 * BN + kPBufs * BN / 2 <= (int)kColO && kColO + D <= kTmemCols, "TMEM budget");
     static_assert(kDynBytes + 512 <= 232448, "shared memory budget");
 };
 
@@ -267,11 +269,12 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     constexpr int BN = C::BN;
     constexpr int NK = C::kKSlots;
     constexpr int NV = C::kVSlots;
+    constexpr int NP = C::kPBufs;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
-    __shared__ uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+    __shared__ uint64_t s_full[2], s_free[2], p_full[NP], p_free[NP];
     __shared__ uint64_t o_done, o_free, mma_drain, stats_full, stats_free;
     __shared__ float2 stats[kBM];  // per row: the unit's running max and sum, for the epilogue
     __shared__ uint32_t tmem_base_sh;
@@ -305,6 +308,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 128);
+        }
+        for (int i = 0; i < NP; ++i) {
             mbar_init(&p_full[i], 128);
             mbar_init(&p_free[i], 1);
         }
@@ -435,8 +440,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 if (uo > 0 && !wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag)) break;
                 ++uo;
                 for (int i = 0; i < t.n; ++i, ++T) {
-                    const int b = T & 1, slot = T % NV;
-                    if (!wait_or_abort(&p_full[b], (T >> 1) & 1, &abort_flag) ||
+                    const int pb = T % NP, slot = T % NV;
+                    if (!wait_or_abort(&p_full[pb], (T / NP) & 1, &abort_flag) ||
                         !wait_or_abort(&v_full[slot], (T / NV) & 1, &abort_flag)) {
                         ok = false;
                         break;
@@ -445,9 +450,9 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        tc_mma_ts(tmem + C::kColO, tmem + C::kColP + b * (BN / 2) + kk * 8,
+                        tc_mma_ts(tmem + C::kColO, tmem + C::kColP + pb * (BN / 2) + kk * 8,
                                   desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&p_free[b]);      // P buffer b may be rewritten; O holds PV(T)
+                    tc_commit(&p_free[pb]);     // P buffer pb may be rewritten; O holds PV(T)
                     tc_commit(&v_empty[slot]);  // V(T) consumed
                     if (i == t.n - 1) tc_commit(&o_done);
                 }
@@ -572,7 +577,7 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     if (__any_sync(0xffffffffu, need)) {
                         // O holds the unit's products up to PV(T-1): let it land, then scale
                         // it in place
-                        if (!wait_warp(&p_free[(T - 1) & 1], ((T - 1) >> 1) & 1)) {
+                        if (!wait_warp(&p_free[(T - 1) % NP], ((T - 1) / NP) & 1)) {
                             ok = false;
                             break;
                         }
@@ -597,16 +602,17 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 l_sum += l_tile;
                 tc_fence_before();
                 mbar_arrive(&s_free[b]);  // S(T) has been read
-                // P buffer b is free once PV(T-2) is done
-                if (T >= 2 && !wait_warp(&p_free[b], ((T >> 1) - 1) & 1)) {
+                // P buffer T % NP is free once PV(T - NP) is done
+                const int pb = T % NP;
+                if (T >= NP && !wait_warp(&p_free[pb], ((T / NP) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                tmem_st32(tm_row + C::kColP + b * (BN / 2), pk);
+                tmem_st32(tm_row + C::kColP + pb * (BN / 2), pk);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&p_full[b]);
+                mbar_arrive(&p_full[pb]);
             }
             if (t.n > 0) {
                 // hand the unit's (max, sum) to the epilogue warps once they have taken the
