@@ -217,11 +217,11 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
 // =========================================================================== head_dim 256
 // Shared-memory / TMEM plan of the head_dim-256 kernel (BN = 64).  Shared memory: the Q
 // tile (64 KB), a 3-slot K ring and a 2-slot V ring (32 KB slots).  TMEM:
-//   S0 [0, BN)  S1 [BN, 2BN)  P0..P3 [2BN + i BN/2, 2BN + (i+1) BN/2)  O [256, 256 + D)
-// P(T) has columns of its own, so S(T+2) may overwrite S buffer T % 2 as soon as the
-// softmax has read S(T), while PV(T) still reads P(T): the S products and the PV products
-// form two independent chains.  Four P buffers let the softmax run four tiles ahead of
-// P.V, which covers the wait of a unit's first P.V for the epilogue to read O out.
+//   S0..S3 [i BN, (i+1) BN)  O [256, 256 + D)
+// The softmax writes P(T) over the first BN/2 columns of S buffer T % 4, and S(T+4) takes
+// that buffer once PV(T) is done.  Four buffers keep the S chain (S issue, softmax read)
+// from waiting on its own latency, and let the softmax run four tiles ahead of P.V, which
+// covers the wait of a unit's first P.V for the epilogue to read O out.
 template <int D>
 struct CfgW {
     static constexpr int BN = 64;
@@ -235,25 +235,25 @@ struct CfgW {
     static constexpr int kSmem = kVOff + kVSlots * kSlotBytes;
     static constexpr int kDynBytes = kSmem + 1024;
     static constexpr int kTmemCols = 512;
-    static constexpr int kPBufs = 4;           // P buffers: the softmax runs this far ahead of P.V
-    static constexpr uint32_t kColP = 2 * BN;  // P buffers at [2 BN, 2 BN + kPBufs BN / 2)
-    static constexpr uint32_t kColO = 256;     // O at [256, 256 + D)
+    static constexpr int kSBufs = 4;        // S buffers, each also holding its P
+    static constexpr uint32_t kColO = 256;  // O at [256, 256 + D)
     static constexpr int kThreads = 512;
-    static_assert(2 * BN + kPBufs * BN / 2 <= (int)kColO && kColO + D <= kTmemCols, "TMEM budget");
+    static_assert(kSBufs * BN <= (int)kColO && kColO + D <= kTmemCols, "TMEM budget");
     static_assert(kDynBytes + 512 <= 232448, "shared memory budget");
 };
 
 // Persistent: each CTA loops over work units (one 128-row query tile of one head, heaviest
 // first, zig-zag over CTAs).  Roles:
 //   warp 0: Q and K producer      warp 2: V producer (and TMEM owner)
-//   warps 1 / 4: S issuers of the even / odd KV tiles   S(T) = Q K(T)^T into buffer T % 2
+//   warps 1 / 4: S issuers of the even / odd KV tiles   S(T) = Q K(T)^T into buffer T % 4
 //   warp 3: PV issuer  O += P(T) V(T)
 //   warps 8-11: softmax (thread = query row = TMEM lane)
 //   warps 12-15: epilogue -- normalise O, write it and the LSE out
 // An S tile of head_dim 256 takes 16 products of N = BN; two issuers keep that chain ahead
 // of the softmax.  At the end of a unit the softmax hands its (max, sum) per row to the
 // epilogue warps through shared memory and goes on with the next unit's tiles; the next
-// unit's first PV waits until the epilogue has read O out of TMEM.  Register split per
+// unit's first PV waits until the epilogue has read O out of TMEM; that read-out is bound
+// by the latency of the TMEM loads, so it takes 64 columns per load.  Register split per
 // warpgroup: roles kRegsRole, softmax kRegsSoftmax, epilogue the launch budget.
 constexpr int kRegsLaunch4 = 128;  // 512 threads
 constexpr int kRegsRole = 96;
@@ -269,12 +269,12 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     constexpr int BN = C::BN;
     constexpr int NK = C::kKSlots;
     constexpr int NV = C::kVSlots;
-    constexpr int NP = C::kPBufs;
+    constexpr int NS = C::kSBufs;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
-    __shared__ uint64_t s_full[2], s_free[2], p_full[NP], p_free[NP];
+    __shared__ uint64_t s_full[NS], p_full[NS], p_free[NS];
     __shared__ uint64_t o_done, o_free, mma_drain, stats_full, stats_free;
     __shared__ float2 stats[kBM];  // per row: the unit's running max and sum, for the epilogue
     __shared__ uint32_t tmem_base_sh;
@@ -305,11 +305,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 128);
-        }
-        for (int i = 0; i < NP; ++i) {
             mbar_init(&p_full[i], 128);
             mbar_init(&p_free[i], 1);
         }
@@ -397,9 +394,9 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 tc_fence_after();
                 for (int i = 0; i < t.n; ++i, ++T) {
                     if ((T & 1) != par) continue;
-                    const int b = T & 1, slot = T % NK;
-                    // S buffer b is free once the softmax has read S(T-2) out of it
-                    if (T >= 2 && !wait_or_abort(&s_free[b], ((T >> 1) - 1) & 1, &abort_flag)) {
+                    const int b = T % NS, slot = T % NK;
+                    // S buffer b is free once PV(T - NS) has read P(T - NS) out of it
+                    if (T >= NS && !wait_or_abort(&p_free[b], ((T / NS) - 1) & 1, &abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -440,8 +437,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 if (uo > 0 && !wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag)) break;
                 ++uo;
                 for (int i = 0; i < t.n; ++i, ++T) {
-                    const int pb = T % NP, slot = T % NV;
-                    if (!wait_or_abort(&p_full[pb], (T / NP) & 1, &abort_flag) ||
+                    const int b = T % NS, slot = T % NV;
+                    if (!wait_or_abort(&p_full[b], (T / NS) & 1, &abort_flag) ||
                         !wait_or_abort(&v_full[slot], (T / NV) & 1, &abort_flag)) {
                         ok = false;
                         break;
@@ -450,9 +447,9 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        tc_mma_ts(tmem + C::kColO, tmem + C::kColP + pb * (BN / 2) + kk * 8,
+                        tc_mma_ts(tmem + C::kColO, tmem + b * BN + kk * 8,
                                   desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&p_free[pb]);     // P buffer pb may be rewritten; O holds PV(T)
+                    tc_commit(&p_free[b]);      // S buffer b may be rewritten; O holds PV(T)
                     tc_commit(&v_empty[slot]);  // V(T) consumed
                     if (i == t.n - 1) tc_commit(&o_done);
                 }
@@ -493,8 +490,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             }
             float m_used = -INFINITY, l_sum = 0.f;
             for (int i = 0; ok && i < t.n; ++i, ++T) {
-                const int b = T & 1;
-                if (!wait_warp(&s_full[b], (T >> 1) & 1)) {
+                const int b = T % NS;
+                if (!wait_warp(&s_full[b], (T / NS) & 1)) {
                     ok = false;
                     break;
                 }
@@ -577,7 +574,7 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     if (__any_sync(0xffffffffu, need)) {
                         // O holds the unit's products up to PV(T-1): let it land, then scale
                         // it in place
-                        if (!wait_warp(&p_free[(T - 1) % NP], ((T - 1) / NP) & 1)) {
+                        if (!wait_warp(&p_free[(T - 1) % NS], ((T - 1) / NS) & 1)) {
                             ok = false;
                             break;
                         }
@@ -600,19 +597,11 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     l_tile = exps(v, (m_used == -INFINITY) ? 0.f : m_used, pk, pmax);
                 }
                 l_sum += l_tile;
-                tc_fence_before();
-                mbar_arrive(&s_free[b]);  // S(T) has been read
-                // P buffer T % NP is free once PV(T - NP) is done
-                const int pb = T % NP;
-                if (T >= NP && !wait_warp(&p_free[pb], ((T / NP) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_st32(tm_row + C::kColP + pb * (BN / 2), pk);
+                // P(T) over the first BN/2 columns of S buffer b (S(T) has been read)
+                tmem_st32(tm_s, pk);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&p_full[pb]);
+                mbar_arrive(&p_full[b]);
             }
             if (t.n > 0) {
                 // hand the unit's (max, sum) to the epilogue warps once they have taken the
@@ -656,15 +645,15 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             const size_t orow = (size_t)bh * p.sq + q_row;
             if (row_valid && p.lse != nullptr) p.lse[orow] = lse_v;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t rr[32];
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                uint32_t rr[64];
                 if (t.n > 0) {
-                    tmem_ld32(tm_o + c0, rr);
+                    tmem_ld64(tm_o + c0, rr);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                    for (int e = 0; e < 64; ++e) rr[e] = 0u;
                 }
-                if (c0 + 32 == D && t.n > 0) {
+                if (c0 + 64 == D && t.n > 0) {
                     tc_fence_before();
                     mbar_arrive(&o_free);  // O has been read: the next unit may overwrite it
                 }
@@ -672,13 +661,13 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     if (p.o_f32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c0);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
+                        for (int e = 0; e < 16; ++e)
                             dst[e] = make_float4(__uint_as_float(rr[4 * e]) * inv, __uint_as_float(rr[4 * e + 1]) * inv,
                                                  __uint_as_float(rr[4 * e + 2]) * inv, __uint_as_float(rr[4 * e + 3]) * inv);
                     } else {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + c0);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
+                        for (int e = 0; e < 8; ++e)
                             dst[e] = make_uint4(
                                 pack_bf16(__uint_as_float(rr[8 * e]) * inv, __uint_as_float(rr[8 * e + 1]) * inv),
                                 pack_bf16(__uint_as_float(rr[8 * e + 2]) * inv, __uint_as_float(rr[8 * e + 3]) * inv),
