@@ -181,6 +181,15 @@ def recorded_traffic(kind: str, workload: str):
 
 
 # --------------------------------------------------------------------------- GPU timing
+def check_device(stream, what):
+    """Raise with the library's status if a kernel reported a device-side error."""
+    import flash_attention_forward_attn_gb300 as A
+
+    err = A.attn_get_device_error(stream)
+    if err != 0:
+        raise RuntimeError(f"{what}: device error {A.attn_status_string(err)}")
+
+
 def time_steps(fn, steps, warmup, flush_buf, stream):
     """Per-step device time (ms) with CUDA events on `stream`; L2 flushed before each step."""
     import torch
@@ -225,7 +234,7 @@ def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False,
                                lse=lse, stream=stream)
 
     ms = time_steps(step, steps, warmup, flush, stream)
-    assert A.attn_get_device_error(stream) == 0
+    check_device(stream, w.name)
     mean_ms = sum(ms) / len(ms)
     flops = w.flops()
     value, slowest_s = aggregate_throughput(flops * steps, sum(ms) / 1e3, world, dev)
@@ -243,6 +252,7 @@ def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False,
     }
     if e2e:
         ent["e2e"] = prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev)
+        check_device(stream, w.name + " (end to end)")
     del q, k, v, o, lse
     torch.cuda.empty_cache()
     return ent
@@ -266,7 +276,7 @@ def packed_prefill_entry(pw, dev, steps, warmup, flush, stream, peaks, world):
                               cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, stream=stream)
 
     ms = time_steps(step, steps, warmup, flush, stream)
-    assert A.attn_get_device_error(stream) == 0
+    check_device(stream, pw.name)
     mean_ms = sum(ms) / len(ms)
     flops = pw.flops()
     value, slowest_s = aggregate_throughput(flops * steps, sum(ms) / 1e3, world, dev)
@@ -384,7 +394,7 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False,
                               lse=lse, kv_chunk=kv_chunk, workspace=ws, stream=stream)
 
     ms = time_steps(step, steps, warmup, flush, stream)
-    assert A.attn_get_device_error(stream) == 0
+    check_device(stream, w.name)
     mean_ms = sum(ms) / len(ms)
     nbytes = C.decode_io_bytes(w, t["lens"], kv_bytes=1 if e4m3 else 2, window=window) + (
         w.d // 2 * 4 if rope else 0)

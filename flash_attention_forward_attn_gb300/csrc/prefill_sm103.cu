@@ -249,8 +249,8 @@ struct CfgW {
 //   warp 3: PV issuer  O += P(T) V(T)
 //   warps 8-11: softmax (thread = query row = TMEM lane)
 //   warps 12-15: epilogue -- normalise O, write it and the LSE out
-// An S tile of head_dim 256 takes 16 products of N = BN; two issuers keep that chain ahead
-// of the softmax.  At the end of a unit the softmax hands its (max, sum) per row to the
+// An S tile of head_dim 256 takes 16 products of N = BN, more than one thread issues in
+// the time the pipe runs them, so two issuers take alternate tiles.  At the end of a unit the softmax hands its (max, sum) per row to the
 // epilogue warps through shared memory and goes on with the next unit's tiles; the next
 // unit's first PV waits until the epilogue has read O out of TMEM; that read-out is bound
 // by the latency of the TMEM loads, so it takes 64 columns per load.  Register split per
@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[NS], p_full[NS], p_free[NS];
     __shared__ uint64_t o_done, o_free, mma_drain, stats_full, stats_free;
+    __shared__ uint64_t turn[2];   // S issue turns of the even and odd tiles
     __shared__ float2 stats[kBM];  // per row: the unit's running max and sum, for the epilogue
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
@@ -313,6 +314,9 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
         mbar_init(&o_done, 1);
         mbar_init(&o_free, 128);
         mbar_init(&mma_drain, 3);
+        mbar_init(&turn[0], 1);
+        mbar_init(&turn[1], 1);
+        mbar_arrive(&turn[0]);  // the even issuer takes the first turn
         mbar_init(&stats_full, 128);
         mbar_init(&stats_free, 128);
         abort_flag = 0;
@@ -376,12 +380,19 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             }
         } else if ((warp == 1 || warp == 4) && lane == 0) {
             // --------------------------------------------- S issuers (even / odd tiles)
+            // A turn passes from tile T's issuer to tile T+1's once T's waits are done and
+            // before its products are issued, so the two issue at once while every wait runs
+            // in tile order.  That order matters for the K ring: the wait for K(T) on slot
+            // T % NK reads the slot's phase by parity, which is only sound once K(T - NK),
+            // the other issuer's tile when NK is odd, is known to have landed.  Four S
+            // buffers let the issuers drift apart, so nothing else ensures it.
             const int par = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             const uint64_t qd = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
             const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
-            int T = 0;   // tiles of all units so far (= K ring index)
-            int uq = 0;  // units with tiles so far (phase of q_full)
+            int T = 0;      // tiles of all units so far (= K ring index)
+            int uq = 0;     // units with tiles so far (phase of q_full)
+            int turns = 0;  // turns taken so far (phase of turn[par])
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int w = zigzag_unit(cta, r, G);
@@ -395,6 +406,11 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 for (int i = 0; i < t.n; ++i, ++T) {
                     if ((T & 1) != par) continue;
                     const int b = T % NS, slot = T % NK;
+                    if (!wait_or_abort(&turn[par], turns & 1, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ++turns;
                     // S buffer b is free once PV(T - NS) has read P(T - NS) out of it
                     if (T >= NS && !wait_or_abort(&p_free[b], ((T / NS) - 1) & 1, &abort_flag)) {
                         ok = false;
@@ -404,6 +420,7 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                         ok = false;
                         break;
                     }
+                    mbar_arrive(&turn[par ^ 1]);  // tile T+1's issuer may do its waits
                     tc_fence_after();
                     const uint64_t kd = desc_add(kd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
