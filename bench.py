@@ -287,7 +287,8 @@ def packed_prefill_entry(pw, dev, steps, warmup, flush, stream, peaks, world):
         "gpu_launches": 2 * steps,  # the work-order pass and the prefill kernel
         "packing": {"nseq": pw.nseq, "sq": w.sq, "skv": w.skv},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": recorded_traffic("prefill", pw.name),
                      "algorithmic_bytes": pw.io_bytes(),
                      "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
         "slowest_rank_s": slowest_s,
