@@ -7,9 +7,31 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/attn.h"
 
 namespace attn {
+
+// One-time setup of a kernel (its shared-memory limit, a register check) is per device:
+// `done` holds one bit per device id.  needs_setup() is true until mark_setup() has run for
+// the current device (device ids past 63 are set up on every call).
+inline bool needs_setup(const std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return dev < 0 || dev >= 64 || (done.load(std::memory_order_acquire) & (1ull << dev)) == 0;
+}
+inline void mark_setup(std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    if (dev >= 0 && dev < 64) done.fetch_or(1ull << dev, std::memory_order_release);
+}
 
 // Bits of the per-translation-unit device error words (read and cleared by the host).
 enum : unsigned {

@@ -811,14 +811,14 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     p.circular = a.circular;
     p.rope_inv_freq = a.rope_inv_freq;
 
-    static bool attr_set = false;  // benign race: every thread sets the same value
-    if (!attr_set) {
+    static std::atomic<unsigned long long> attr_done{0};  // setting it twice is harmless
+    if (needs_setup(attr_done)) {
         if (cudaFuncSetAttribute(decode_split_kernel<D, kE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes) != cudaSuccess) {
             cudaGetLastError();
             return ATTN_ERR_CUDA;
         }
-        attr_set = true;
+        mark_setup(attr_done);
     }
     dim3 grid(a.max_splits, a.hkv, a.b);
     decode_split_kernel<D, kE4M3><<<grid, kThreads, L::kDynBytes, stream>>>(tk, tv, p);

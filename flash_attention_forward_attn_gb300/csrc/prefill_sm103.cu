@@ -47,7 +47,6 @@ __device__ unsigned g_prefill_error;
 
 constexpr int kBM = 128;           // query rows per tile (= TMEM lanes)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold, log2 units
 // Registers after re-balancing: the TMA/MMA warpgroup gives up registers to the softmax
 // warpgroups.  128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch3 (the launch budget).
@@ -1250,15 +1249,15 @@ int num_sms() {
 // Writes the packed work order into `order` (nu <= kOrderMax ints) on the stream.
 template <int BN, int kTilesPerUnit>
 bool unit_order_launch(const PrefillParams& p, int nu, int* order, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
+    static std::atomic<unsigned long long> attr_done{0};
+    if (needs_setup(attr_done)) {
         if (cudaFuncSetAttribute(unit_order_kernel<BN, kTilesPerUnit>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kOrderMax * (int)sizeof(unsigned long long)) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
-        attr_set = true;
+        mark_setup(attr_done);
     }
     int n2 = 1;
     while (n2 < nu) n2 <<= 1;
@@ -1271,8 +1270,8 @@ template <int D, bool kPacked>
 attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
     using C = CfgW<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static std::atomic<unsigned long long> attr_done{0};
+    if (needs_setup(attr_done)) {
         if (cudaFuncSetAttribute(prefill_wide_kernel<D, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kDynBytes) != cudaSuccess) {
             cudaGetLastError();
@@ -1286,7 +1285,7 @@ attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, con
             return ATTN_ERR_CUDA;
         }
         if (fa.numRegs != kRegsLaunch4) return ATTN_ERR_UNSUPPORTED;
-        attr_set = true;
+        mark_setup(attr_done);
     }
     const long long units = (long long)p.nqt * a.b * a.hq;
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
@@ -1308,8 +1307,8 @@ template <int D, bool kPacked>
 attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
     using C = Cfg2Q<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static std::atomic<unsigned long long> attr_done{0};
+    if (needs_setup(attr_done)) {
         if (cudaFuncSetAttribute(prefill2q_kernel<D, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kDynBytes) != cudaSuccess) {
             cudaGetLastError();
@@ -1323,7 +1322,7 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
             return ATTN_ERR_CUDA;
         }
         if (fa.numRegs != kRegsLaunch3) return ATTN_ERR_UNSUPPORTED;
-        attr_set = true;
+        mark_setup(attr_done);
     }
     const long long units = (long long)((p.nqt + 1) / 2) * a.b * a.hq;
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
