@@ -148,3 +148,67 @@ def test_packed_benchmark_workload_sampled(cuda_device):
             assert_o_close(got, o_ref, f"packed s{s} h{h}")
             assert_lse_close(lse[0, h, [q0 + r for r in rows]].cpu().numpy(), lse_ref,
                              f"packed s{s} h{h}")
+
+
+def _tile_cost(cu_q, cu_k, sq, skv, causal, window, bm, bn, qt):
+    """KV tiles of packed query tile qt (rows [qt*bm, qt*bm + bm)), from the definition of
+    the allowed keys: each row's own sequence, its queries at the tail of its keys."""
+    q0 = qt * bm
+    rows = min(bm, sq - q0)
+    if rows <= 0:
+        return 0
+
+    def bounds(i):
+        s = int(np.searchsorted(cu_q, i, side="right") - 1)
+        nq, k0, nk = int(cu_q[s + 1] - cu_q[s]), int(cu_k[s]), int(cu_k[s + 1] - cu_k[s])
+        qpos = (i - int(cu_q[s])) + nk - nq
+        hi = k0 + (min(qpos, nk - 1) if causal else nk - 1)
+        lo = k0 + (max(0, qpos - window + 1) if window > 0 else 0)
+        return s, lo, hi
+
+    s0, lo0, _ = bounds(q0)
+    s1, _, hi1 = bounds(q0 + rows - 1)
+    k_end, k_begin = min(skv, hi1 + 1), max(0, lo0)
+    if s0 != s1:
+        k_end = max(k_end, min(skv, int(cu_k[s1])))
+    return 0 if k_end <= k_begin else -(-k_end // bn) - k_begin // bn
+
+
+@pytest.mark.parametrize("d,packing,causal,window", [
+    (128, (40, 300, 200), True, 0),
+    (128, (25, 500, 0), False, 0),   # ties: every tile of a sequence has the same count
+    (256, (24, 260, 100), True, 64),
+])
+def test_work_order_is_the_units_sorted_by_kv_tiles(d, packing, causal, window, cuda_device):
+    """The work-order pass writes a permutation of the query units (pairs of 128-row tiles
+    for head_dim <= 128, single tiles for 256), KV-tile counts non-increasing, ties in index
+    order."""
+    import ctypes
+
+    import flash_attention_forward_attn_gb300 as A
+
+    cu_q, cu_k = packed_lengths(0xC0 + d, *packing)
+    w = C.PrefillWorkload("order", 1, 4, 2, int(cu_q[-1]), int(cu_k[-1]), d, causal, window,
+                          seed=0x7E0)
+    q, k, v = C.prefill_inputs_torch(w, cuda_device)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=cuda_device)
+    nbytes = A.attn_prefill_workspace_bytes(w.sq)
+    ws = torch.full((nbytes // 4,), -1, dtype=torch.int32, device=cuda_device)
+    dq, dk = (torch.from_numpy(x).to(cuda_device) for x in (cu_q, cu_k))
+    opts = A.AttnOpts(cu_seqlens_q=dq.data_ptr(), cu_seqlens_k=dk.data_ptr(), nseq=len(cu_q) - 1,
+                      prefill_workspace=ws.data_ptr(), prefill_workspace_bytes=nbytes)
+    lib = A.load_library()
+    st = lib.attn_fwd_prefill_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, 1,
+                                 4, 2, w.sq, w.skv, d, w.scale, int(causal), window, 0,
+                                 ctypes.byref(opts), None)
+    torch.cuda.synchronize()
+    assert st == 0 and A.attn_get_device_error() == 0
+    nqt = -(-w.sq // 128)
+    per, bn = (2, 128) if d <= 128 else (1, 64)
+    nu = -(-nqt // per)
+    cost = [sum(_tile_cost(cu_q, cu_k, w.sq, w.skv, causal, window, 128, bn, per * u + x)
+                for x in range(per)) for u in range(nu)]
+    order = ws[:nu].cpu().numpy().tolist()
+    assert sorted(order) == list(range(nu))
+    keys = [(-cost[u], u) for u in order]
+    assert keys == sorted(keys)
