@@ -568,32 +568,40 @@ def main():
         barrier(world)
         if not args.no_extra:
             ext_steps = max(10, min(args.steps, 30))
-            for wx in (C.GQA_PREFILL_32K, C.SWA_PREFILL_8K):
-                extras[wx.name] = prefill_entry(wx, dev, ext_steps, args.warmup, flush, stream,
-                                                peaks, world)
-            for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4):
-                extras[wx.name] = decode_entry(wx, dev, max(ext_steps, 50), args.warmup, flush,
-                                               stream, peaks, world)
+            dec_steps = max(ext_steps, 50)
+            runs = [(wx.name, lambda wx=wx: prefill_entry(wx, dev, ext_steps, args.warmup, flush,
+                                                         stream, peaks, world))
+                    for wx in (C.GQA_PREFILL_32K, C.SWA_PREFILL_8K)]
+            runs += [(wx.name, lambda wx=wx: decode_entry(wx, dev, dec_steps, args.warmup, flush,
+                                                         stream, peaks, world))
+                     for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4)]
             # packed sequences (attn_opts.cu_seqlens): 16 causal sequences with cached prefixes
-            ent = packed_prefill_entry(C.PACKED_PREFILL, dev, ext_steps, args.warmup, flush,
-                                       stream, peaks, world)
-            extras[ent["workload"]] = ent
+            runs.append((C.PACKED_PREFILL.name, lambda: packed_prefill_entry(
+                C.PACKED_PREFILL, dev, ext_steps, args.warmup, flush, stream, peaks, world)))
             # the attention sink (attn_opts.sink) on the 2K prefill and the 1-token decode
-            ent = prefill_entry(w, dev, ext_steps, args.warmup, flush, stream, peaks, world,
-                                sink=True)
-            extras[ent["workload"]] = ent
-            ent = decode_entry(C.PAGED_DECODE, dev, max(ext_steps, 50), args.warmup, flush,
-                               stream, peaks, world, sink=True)
-            extras[ent["workload"]] = ent
+            runs.append((w.name + "+sink", lambda: prefill_entry(
+                w, dev, ext_steps, args.warmup, flush, stream, peaks, world, sink=True)))
+            runs.append((C.PAGED_DECODE.name + "+sink", lambda: decode_entry(
+                C.PAGED_DECODE, dev, dec_steps, args.warmup, flush, stream, peaks, world,
+                sink=True)))
             # the FP8-e4m3 KV cache (attn_opts.kv_dtype): half the cache bytes
-            for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4):
-                ent = decode_entry(wx, dev, max(ext_steps, 50), args.warmup, flush, stream,
-                                   peaks, world, e4m3=True)
-                extras[ent["workload"]] = ent
+            runs += [(wx.name + "+e4m3", lambda wx=wx: decode_entry(
+                wx, dev, dec_steps, args.warmup, flush, stream, peaks, world, e4m3=True))
+                for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4)]
             # a 4096-token window with RoPE of the queries (the pages' decode options)
-            ent = decode_entry(C.PAGED_DECODE_SPEC4, dev, max(ext_steps, 50), args.warmup, flush,
-                               stream, peaks, world, window=4096, rope=True)
-            extras[ent["workload"]] = ent
+            runs.append((C.PAGED_DECODE_SPEC4.name + "+w4096+rope", lambda: decode_entry(
+                C.PAGED_DECODE_SPEC4, dev, dec_steps, args.warmup, flush, stream, peaks, world,
+                window=4096, rope=True)))
+            for label, run in runs:
+                try:
+                    ent = run()
+                except RuntimeError as e:  # a device-side error report: keep the main line
+                    if world > 1:
+                        raise  # ranks must stay in step for the collectives
+                    torch.cuda.synchronize()
+                    ent = {"workload": label, "error": str(e)}
+                    print(f"bench: {label}: {e}", file=sys.stderr, flush=True)
+                extras[ent["workload"]] = ent
     clocks = clk.summary()
 
     cpu = None
