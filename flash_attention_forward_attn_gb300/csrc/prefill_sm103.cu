@@ -249,11 +249,12 @@ struct CfgW {
 //   warps 8-11: softmax (thread = query row = TMEM lane)
 //   warps 12-15: epilogue -- normalise O, write it and the LSE out
 // An S tile of head_dim 256 takes 16 products of N = BN, more than one thread issues in
-// the time the pipe runs them, so two issuers take alternate tiles.  At the end of a unit the softmax hands its (max, sum) per row to the
-// epilogue warps through shared memory and goes on with the next unit's tiles; the next
-// unit's first PV waits until the epilogue has read O out of TMEM; that read-out is bound
-// by the latency of the TMEM loads, so it takes 64 columns per load.  Register split per
-// warpgroup: roles kRegsRole, softmax kRegsSoftmax, epilogue the launch budget.
+// the time the pipe runs them, so two issuers take alternate tiles.  At the end of a unit
+// the softmax hands its (max, sum) per row to the epilogue warps through shared memory and
+// goes on with the next unit's tiles; the next unit's first PV waits until the epilogue
+// has read O out of TMEM.  That read-out is bound by the latency of the TMEM loads, so it
+// takes 64 columns per load.  Register split per warpgroup: roles kRegsRole, softmax
+// kRegsSoftmax, epilogue the launch budget.
 constexpr int kRegsLaunch4 = 128;  // 512 threads
 constexpr int kRegsRole = 96;
 constexpr int kRegsSoftmax = 160;
