@@ -557,6 +557,37 @@ def test_circular_cache_equals_the_full_cache(n):
     assert np.isfinite(o1).all()
 
 
+@pytest.mark.parametrize("n", [40, 101, 300])
+def test_circular_cache_with_rope_and_new_tokens_equals_the_full_cache(n):
+    """The same equivalence with every decode option at once: RoPE of the queries and of
+    the new keys (given apart from the cache) must use logical positions, never ring rows,
+    so a wrapped ring gives exactly the full cache's result."""
+    hq, hkv, d, sa, cap, window = 4, 2, 8, 3, 32, 28
+    fk, fv, _, _, _ = _flat_and_paged(79, 1, hkv, d, [n], 8, False)
+    kn, vn = fk[:, :, n - sa:n].copy(), fv[:, :, n - sa:n].copy()
+    ck = np.full((1, hkv, cap, d), rng.BF16_NAN_BITS, dtype=np.uint16)
+    cv = ck.copy()
+    for j in range(max(0, n - cap), n - sa):  # the new tokens' rows come from k_new / v_new
+        ck[:, :, j % cap] = fk[:, :, j]
+        cv[:, :, j % cap] = fv[:, :, j]
+    fk2, fv2 = fk.copy(), fv.copy()
+    fk2[:, :, n - sa:n] = rng.BF16_NAN_BITS  # likewise in the full cache
+    fv2[:, :, n - sa:n] = rng.BF16_NAN_BITS
+    q = rand_bits(80, (1, hq, sa, d), "q")
+    cl = np.array([n], np.int32)
+    f = 10000.0 ** (-np.arange(d // 2) / (d // 2))
+    o1, l1 = oracle.decode_ext(q, ck, cv, None, cl, 0.25, window=window, circular=True,
+                               k_new=kn, v_new=vn, inv_freq=f)
+    o2, l2 = oracle.decode_ext(q, fk2, fv2, None, cl, 0.25, window=window, k_new=kn, v_new=vn,
+                               inv_freq=f)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    assert np.isfinite(o1).all()
+    # and the rotation matters: without it the result differs
+    o3, _ = oracle.decode_ext(q, fk2, fv2, None, cl, 0.25, window=window, k_new=kn, v_new=vn)
+    assert not np.array_equal(o1, o3)
+
+
 def test_new_tokens_given_apart_equal_tokens_in_the_cache():
     b, hq, hkv, d, page, sa = 2, 4, 2, 8, 4, 3
     lens = [7, 18]
