@@ -203,3 +203,46 @@ def test_decode_window_repeat_runs_bit_identical(cuda_device):
     for _ in range(10):
         o1, l1 = decode_ex(t, w, window=1000, rope_inv_freq=f)
         assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def _one_sequence(t, w, b):
+    """Sequence b of a paged cache gathered into a one-sequence flat cache (bf16 bits) for
+    the oracle, with its query rows and cache length."""
+    n = int(t["lens"][b])
+    npg = -(-n // w.page_size)
+    idx = torch.from_numpy(t["table"][b, :npg].astype(np.int64)).to(t["q"].device)
+    flat = [bits_of(t[c][idx].permute(1, 0, 2, 3).reshape(1, w.hkv, npg * w.page_size, w.d)
+                    [:, :, :n].contiguous()) for c in ("k_cache", "v_cache")]
+    return bits_of(t["q"][b:b + 1]), flat[0], flat[1], np.array([n], np.int32)
+
+
+def test_window_rope_decode_full_size_sampled(cuda_device):
+    """The benchmark's windowed decode with RoPE of the queries (64 sequences, 4 new tokens,
+    window 4096, inverse frequencies 10000^(-2i/d)), in the launch the benchmark times;
+    sequences are checked one by one against the oracle over their gathered pages."""
+    w = C.PAGED_DECODE_SPEC4
+    t = C.decode_inputs_torch(w, cuda_device)
+    f = inv_freq(w.d)
+    o, lse = decode_ex(t, w, window=4096, rope_inv_freq=torch.from_numpy(f).to(cuda_device))
+    lens = t["lens"]
+    for b in sorted({int(np.argmax(lens)), int(np.argmin(lens)), 5, 41}):
+        q, fk, fv, cl = _one_sequence(t, w, b)
+        o_ref, lse_ref = oracle.decode_ext(q, fk, fv, None, cl, w.scale, window=4096,
+                                           inv_freq=f.astype(np.float64))
+        assert_o_close(o[b:b + 1].cpu().numpy(), o_ref, f"window+rope b{b}")
+        assert_lse_close(lse[b:b + 1].cpu().numpy(), lse_ref, f"window+rope b{b}")
+
+
+def test_sink_decode_full_size_sampled(cuda_device):
+    """The benchmark's decode with per-head sink logits (64 sequences, 1 new token), checked
+    on sampled sequences against the oracle with the same sinks."""
+    w = C.PAGED_DECODE
+    t = C.decode_inputs_torch(w, cuda_device)
+    sk = C.sink_logits(w.hq)
+    o, lse = decode_ex(t, w, sink=torch.from_numpy(sk).to(cuda_device))
+    lens = t["lens"]
+    for b in sorted({int(np.argmax(lens)), int(np.argmin(lens)), 9, 50}):
+        q, fk, fv, cl = _one_sequence(t, w, b)
+        o_ref, lse_ref = oracle.decode(q, fk, fv, None, cl, w.scale, sink=sk)
+        assert_o_close(o[b:b + 1].cpu().numpy(), o_ref, f"sink b{b}")
+        assert_lse_close(lse[b:b + 1].cpu().numpy(), lse_ref, f"sink b{b}")

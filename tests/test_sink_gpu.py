@@ -107,3 +107,34 @@ def test_decode_sink_of_minus_inf_is_bit_identical_to_the_plain_call(cuda_device
                                                                 device=cuda_device), **kw)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_sink_prefill_full_size_sampled(cuda_device):
+    """The benchmark's 2K causal prefill with per-head sink logits, in the launch the
+    benchmark times; sampled rows of heads with a neutral, a dominant (e^9, e^60) and an
+    absent sink are checked against the oracle's rows with the same sink."""
+    import numpy as np
+
+    import flash_attention_forward_attn_gb300 as A
+    from workloads import rng
+
+    w = C.CAUSAL_PREFILL_2K
+    q, k, v = C.prefill_inputs_torch(w, cuda_device)
+    sk = C.sink_logits(w.hq)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=cuda_device)
+    o, _ = A.attn_fwd_prefill_ex(q, k, v, causal=True, scale=w.scale, lse=lse,
+                                 sink=torch.from_numpy(sk).to(cuda_device))
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    u = rng.uniform_np(rng.stream_seed(3, "rows"), 0, 12)
+    rows = sorted({0, 1, 127, 128, 1023, w.sq - 1} | {int(x) for x in (u * w.sq).astype(np.int64)})
+    for h in (0, 3, 5, 7):  # sinks 0, 9, -inf, 60
+        g = oracle.kv_head(h, w.hq, w.hkv)
+        kh = C.prefill_kv_head_np(w, "k", 0, g)
+        vh = C.prefill_kv_head_np(w, "v", 0, g)
+        qr = np.stack([C.prefill_q_rows_np(w, 0, h, r, 1)[0] for r in rows])
+        qp = [oracle.q_pos(r, w.sq, w.skv) for r in rows]
+        o_ref, lse_ref = oracle.attention_rows(qr, kh, vh, qp, w.scale, True, 0,
+                                               sink=float(sk[h]))
+        assert_o_close(o[0, h, rows].float().cpu().numpy(), o_ref, f"2K sink h{h}")
+        assert_lse_close(lse[0, h, rows].cpu().numpy(), lse_ref, f"2K sink h{h}")
