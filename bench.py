@@ -1,11 +1,15 @@
 #!/usr/bin/env python3
 """Benchmark of the attention forward on GB300.
 
-One step = one fused prefill call (attn_fwd_prefill) on the causal 7B-shaped workload
-(batch 1, 32 heads, 2048 x 2048, head_dim 128, bf16) with inputs resident in HBM.
-The line also carries the other hot-path workloads, each timed the same way:
-the 32K GQA causal prefill with Q outliers, the 8K head_dim-256 sliding-window prefill,
-and the paged decode (split-KV + log-sum-exp combine) with 1 and 4 new tokens.
+One step = one fused prefill call (attn_fwd_prefill) on the headline workload, the
+long-context GQA causal prefill (batch 1, 32 query heads over 8 kv heads, 32768 x 32768,
+head_dim 128, bf16, 1% of Q elements scaled x8), with inputs resident in HBM.  The final
+line also carries, end to end, the same call with host buffers (copies inside the timed
+region), and a summary of the other hot-path workloads, each timed the same way and printed
+in full on a line of its own before it: the tiny and the 2K prefills, the 8K head_dim-256
+sliding-window prefill, the paged decode (split-KV + log-sum-exp combine) with 1 and 4 new
+tokens, packed sequences, the attention sink, the FP8-e4m3 cache, and a windowed decode
+with RoPE.  Each line carries the fp64 CPU oracle timed on the host cores beside it.
 
 Timing: W untimed warm-up steps, then exactly K timed steps; every step is bracketed
 by CUDA events on the launching stream, and a 256 MiB buffer is written between steps
@@ -14,7 +18,7 @@ region; with N > 1 ranks each rank runs its own replica and the max over ranks i
 SM clocks are sampled with nvidia-smi while the timed regions run.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference that exists for this
-path) on bounded samples of the same workload on the host cores.
+path) on bounded samples of the headline workload on the host cores.
 """
 from __future__ import annotations
 
@@ -211,9 +215,11 @@ def time_steps(fn, steps, warmup, flush_buf, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False, sink=False):
+def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False, sink=False,
+                  cpu_threads=0):
     """Time attn_fwd_prefill on workload w (with sink=True: attn_fwd_prefill_ex with the
-    per-head sink logits of workloads.configs.sink_logits)."""
+    per-head sink logits of workloads.configs.sink_logits).  cpu_threads > 0 also times the
+    fp64 oracle on a bounded sample of the same inputs (after the GPU timing)."""
     import torch
 
     import flash_attention_forward_attn_gb300 as A
@@ -253,12 +259,15 @@ def prefill_entry(w, dev, steps, warmup, flush, stream, peaks, world, e2e=False,
     if e2e:
         ent["e2e"] = prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev)
         check_device(stream, w.name + " (end to end)")
+    if cpu_threads:
+        ent["cpu_baseline"] = cpu_prefill(w, q, k, v, cpu_threads,
+                                          C.sink_logits(w.hq) if sink else None)
     del q, k, v, o, lse
     torch.cuda.empty_cache()
     return ent
 
 
-def packed_prefill_entry(pw, dev, steps, warmup, flush, stream, peaks, world):
+def packed_prefill_entry(pw, dev, steps, warmup, flush, stream, peaks, world, cpu_threads=0):
     """Time attn_fwd_prefill_ex on packed sequences (attn_opts.cu_seqlens)."""
     import torch
 
@@ -293,6 +302,8 @@ def packed_prefill_entry(pw, dev, steps, warmup, flush, stream, peaks, world):
                      "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
         "slowest_rank_s": slowest_s,
     }
+    if cpu_threads:
+        ent["cpu_baseline"] = cpu_packed(pw, q, k, v, cpu_threads)
     del q, k, v, o, lse
     torch.cuda.empty_cache()
     return ent
@@ -363,13 +374,20 @@ def prefill_e2e(w, q, k, v, o, lse, steps, warmup, stream, world, dev):
             "pipelining": "2 buffer sets; per-input upload streams; download stream"}
 
 
+def rope_inv_freq(d):
+    """RoPE inverse frequencies 10000^(-2i/d), i < d/2 (fp32)."""
+    import numpy as np
+
+    return np.array([10000.0 ** (-2.0 * i / d) for i in range(d // 2)], dtype=np.float32)
+
+
 def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False, e4m3=False,
-                 window=0, rope=False, kv_chunk=0):
+                 window=0, rope=False, kv_chunk=0, cpu_threads=0):
     """Time attn_fwd_decode on workload w (with sink=True: attn_fwd_decode_ex with the
     per-head sink logits of workloads.configs.sink_logits; with e4m3=True: attn_fwd_decode_ex
     over the same caches rounded to FP8-e4m3, k_scale = v_scale = 1; window > 0 and rope:
     attn_fwd_decode_ex with that window and RoPE of the queries, inverse frequencies
-    10000^(-2i/d))."""
+    10000^(-2i/d)).  cpu_threads > 0 also times the fp64 oracle on a sample of sequences."""
     import torch
 
     import flash_attention_forward_attn_gb300 as A
@@ -382,8 +400,7 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False,
     lse = torch.empty(t["q"].shape[:3], dtype=torch.float32, device=dev)
     sk = torch.from_numpy(C.sink_logits(w.hq)).to(dev) if sink else None
     args = (t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["cache_len"])
-    inv = (torch.tensor([10000.0 ** (-2.0 * i / w.d) for i in range(w.d // 2)], dtype=torch.float32,
-                        device=dev) if rope else None)
+    inv = torch.from_numpy(rope_inv_freq(w.d)).to(dev) if rope else None
 
     def step():
         if sink or e4m3 or window or rope:
@@ -414,103 +431,256 @@ def decode_entry(w, dev, steps, warmup, flush, stream, peaks, world, sink=False,
                      "peak_source": f"{peaks['source']} HBM copy (MEASURED_PEAKS.json)"},
         "slowest_rank_s": slowest_s,
     }
+    if cpu_threads:
+        ent["cpu_baseline"] = cpu_decode(w, t, cpu_threads, C.sink_logits(w.hq) if sink else None,
+                                         e4m3, window, rope_inv_freq(w.d) if rope else None)
     del t, ws, o, lse
     torch.cuda.empty_cache()
     return ent
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_prefill_sample(w, n_heads: int, rows_per_head: int, threads: int):
-    """Time the fp64 oracle on a bounded sample of a prefill workload.
+# The fp64 oracle, as it stands, timed on the host cores beside each GPU line.  Its inputs
+# are the seeded generator's values already made for the GPU timing, copied to the host (the
+# same bits the kernels read); only the oracle calls are inside the timer.  Workloads whose
+# full oracle run would take minutes are timed on a bounded sample and extrapolated at the
+# measured rate (FLOPs for prefill, algorithmic bytes for decode), labelled as such.
+SAMPLE_ROWS = 256     # query rows per sampled head
+SAMPLE_HEADS = 8      # (batch, head) pairs sampled
+FULL_PREFILL_FLOP = 5e10  # prefills up to this size are timed in full
+DECODE_SAMPLE_SEQS = 2
 
-    The sample is `n_heads` heads, and in each the last `rows_per_head` query rows (or all
-    rows when rows_per_head >= sq): inputs come from the seeded generator, never from a GPU.
-    Returns (seconds, causal-adjusted FLOPs of the sample, description)."""
+
+def _bits(t):
     import numpy as np
+    import torch
 
-    import oracle
+    t = t.detach().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.view(torch.uint8).cpu().numpy()
+
+
+def _timed_pool(fn, jobs, threads):
     from concurrent.futures import ThreadPoolExecutor
-    from workloads import configs as C
-
-    rows = list(range(max(0, w.sq - rows_per_head), w.sq))
-    jobs = []
-    for idx in range(n_heads):
-        b, h = divmod(idx, w.hq)
-        g = oracle.kv_head(h, w.hq, w.hkv)
-        kh = C.prefill_kv_head_np(w, "k", b, g)
-        vh = C.prefill_kv_head_np(w, "v", b, g)
-        qr = C.prefill_q_rows_np(w, b, h, rows[0], len(rows))
-        jobs.append((qr, kh, vh))
-    qp = np.array([oracle.q_pos(r, w.sq, w.skv) for r in rows])
-    chunks = [(j, s) for j in range(len(jobs)) for s in range(0, len(rows), 16)]
-
-    def run(js):
-        j, s = js
-        qr, kh, vh = jobs[j]
-        oracle.attention_rows(qr[s:s + 16], kh, vh, qp[s:s + 16], w.scale, w.causal, w.window)
 
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(run, chunks))
-    secs = time.perf_counter() - t0
-    if w.causal:
-        lo = np.maximum(0, qp - w.window + 1) if w.window > 0 else np.zeros_like(qp)
-        pairs = int((np.minimum(qp, w.skv - 1) - lo + 1).clip(0).sum())
+        list(ex.map(fn, jobs))
+    return time.perf_counter() - t0
+
+
+def _sample_rows(w, n, seed):
+    """Rows 0 and sq-1, the 128-row tile boundaries around them and seeded uniform rows."""
+    import numpy as np
+
+    from workloads import rng
+
+    if n >= w.sq:
+        return np.arange(w.sq)
+    rows = {0, w.sq - 1, 127, 128, 129, w.sq - 128, w.sq - 129}
+    u = rng.uniform_np(rng.stream_seed(seed, "cpu_sample_rows"), 0, 4 * n)
+    for x in (u * w.sq).astype(np.int64):
+        if len(rows) >= n:
+            break
+        rows.add(int(x))
+    return np.array(sorted(r for r in rows if 0 <= r < w.sq))
+
+
+def cpu_prefill(w, q, k, v, threads, sink=None):
+    """Oracle rows of prefill workload w: every row of every head when the workload is at
+    most FULL_PREFILL_FLOP, else SAMPLE_ROWS rows of SAMPLE_HEADS heads."""
+    import numpy as np
+
+    import oracle
+
+    full = w.flops() <= FULL_PREFILL_FLOP
+    pairs = [(b, h) for b in range(w.b) for h in range(w.hq)]
+    if not full:
+        pick = np.linspace(0, len(pairs) - 1, SAMPLE_HEADS).round().astype(int)
+        pairs = [pairs[i] for i in sorted(set(pick))]
+    rows = np.arange(w.sq) if full else _sample_rows(w, SAMPLE_ROWS, w.seed)
+    qp = rows + (w.skv - w.sq)
+    hi = np.minimum(qp, w.skv - 1) if w.causal else np.full_like(qp, w.skv - 1)
+    lo = np.maximum(0, qp - w.window + 1) if w.window > 0 else np.zeros_like(qp)
+    flops = 4.0 * w.d * float(np.clip(hi - lo + 1, 0, None).sum()) * len(pairs)
+    data = {}
+    for (b, h) in pairs:
+        g = oracle.kv_head(h, w.hq, w.hkv)
+        data[(b, h)] = (_bits(q[b, h])[rows], _bits(k[b, g]), _bits(v[b, g]))
+    jobs = [(p, s) for p in pairs for s in range(0, len(rows), 16)]
+
+    def run(job):
+        (b, h), s = job
+        qr, kh, vh = data[(b, h)]
+        oracle.attention_rows(qr[s:s + 16], kh, vh, qp[s:s + 16], w.scale, w.causal, w.window,
+                              sink=None if sink is None else sink[h])
+
+    secs = _timed_pool(run, jobs, threads)
+    rate = flops / secs
+    ent = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "seconds": secs}
+    if full:
+        ent["sample"] = f"all {w.b * w.hq} heads x {w.sq} rows (the whole workload)"
     else:
-        pairs = len(rows) * w.skv
-    flops = 4.0 * w.d * pairs * n_heads
-    desc = (f"{n_heads} head(s) x last {len(rows)} query rows of {w.name} "
-            f"(fp64, full score rows, {threads} threads)")
-    return secs, flops, desc
+        ent["sample"] = (f"{len(pairs)} of {w.b * w.hq} heads x {len(rows)} rows (0, sq-1, tile "
+                         f"boundaries, seeded uniform); rate over the sampled rows' allowed keys")
+        ent["extrapolated_full_s"] = w.flops() / rate
+    return ent
 
 
-def cpu_baseline(w, threads):
-    # about 10-30 CPU-seconds: all 32 heads x all 2048 rows of the 2K workload
-    secs, flops, desc = oracle_prefill_sample(w, n_heads=w.b * w.hq, rows_per_head=w.sq,
-                                              threads=threads)
-    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": desc, "seconds": secs}
+def cpu_packed(pw, q, k, v, threads):
+    """Oracle rows of a packed prefill: SAMPLE_ROWS rows of two heads, each row against its
+    own sequence's keys."""
+    import numpy as np
+
+    import oracle
+
+    cu_q, cu_k = pw.offsets()
+    w = pw.as_prefill()
+    rows = _sample_rows(w, SAMPLE_ROWS, pw.seed)
+    seq = np.searchsorted(cu_q, rows, side="right") - 1
+    jobs, flops = [], 0.0
+    for h in (0, pw.hq - 1):
+        g = oracle.kv_head(h, pw.hq, pw.hkv)
+        qh, kh, vh = _bits(q[0, h]), _bits(k[0, g]), _bits(v[0, g])
+        for s in np.unique(seq):
+            r = rows[seq == s]
+            k0, k1 = int(cu_k[s]), int(cu_k[s + 1])
+            qp = r - cu_q[s] + (k1 - k0) - (cu_q[s + 1] - cu_q[s])
+            jobs.append((qh[r], kh[k0:k1], vh[k0:k1], qp))
+            flops += 4.0 * pw.d * float(np.clip(np.minimum(qp, k1 - k0 - 1) + 1, 0, None).sum())
+
+    def run(job):
+        qr, kk, vv, qp = job
+        oracle.attention_rows(qr, kk, vv, qp, pw.scale, True, 0)
+
+    secs = _timed_pool(run, jobs, threads)
+    rate = flops / secs
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "seconds": secs, "extrapolated_full_s": pw.flops() / rate,
+            "sample": f"2 of {pw.hq} heads x {len(rows)} packed rows, each against its sequence"}
+
+
+def cpu_decode(w, t, threads, sink=None, e4m3=False, window=0, inv_freq=None):
+    """Oracle decode of the first DECODE_SAMPLE_SEQS sequences (all heads, whole caches,
+    gathered through their own compacted page table)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from workloads import configs as C
+
+    n = min(DECODE_SAMPLE_SEQS, w.b)
+    lens = t["lens"][:n]
+    table = t["table"]
+    npg = [-(-int(x) // w.page_size) for x in lens]
+    pages = np.concatenate([table[b, :npg[b]] for b in range(n)]).astype(np.int64)
+    idx = torch.from_numpy(pages).to(t["k_cache"].device)
+    kc, vc = _bits(t["k_cache"][idx]), _bits(t["v_cache"][idx])
+    sub = np.full((n, w.max_pages_per_seq), 0xFFFFFFFF, dtype=np.uint32)
+    off = 0
+    for b in range(n):
+        sub[b, :npg[b]] = np.arange(off, off + npg[b], dtype=np.uint32)
+        off += npg[b]
+    qb = _bits(t["q"][:n])
+    t0 = time.perf_counter()
+    if e4m3:
+        oracle.decode_e4m3(qb, kc, vc, sub, lens, w.scale, 1.0, 1.0, threads=threads, sink=sink)
+    elif window or inv_freq is not None:
+        oracle.decode_ext(qb, kc, vc, sub, lens, w.scale, window=window, inv_freq=inv_freq,
+                          sink=sink, threads=threads)
+    else:
+        oracle.decode(qb, kc, vc, sub, lens, w.scale, threads=threads, sink=sink)
+    secs = time.perf_counter() - t0
+    nbytes = C.decode_io_bytes(w.with_(b=n), lens, kv_bytes=1 if e4m3 else 2, window=window)
+    rate = nbytes / secs
+    full = C.decode_io_bytes(w, t["lens"], kv_bytes=1 if e4m3 else 2, window=window)
+    return {"value": rate / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": secs, "extrapolated_full_s": full / rate,
+            "sample": (f"{n} of {w.b} sequences (cache lens {', '.join(str(int(x)) for x in lens)}),"
+                       f" all {w.hq} heads; rate over their algorithmic bytes")}
 
 
 # --------------------------------------------------------------------------- main
 def run_reference(args, rank, world):
-    """The reference arm: the fp64 CPU oracle on the host cores, rank 0 only."""
+    """The reference arm: the fp64 CPU oracle on the host cores, rank 0 only, on bounded
+    samples of the headline workload: each step is the last 16 query rows (the rows with
+    the most keys) of one head."""
+    import numpy as np
+
+    import oracle
     from workloads import configs as C
 
     if rank != 0:
         return 0
-    w = C.CAUSAL_PREFILL_2K
+    w = HEADLINE(C)
     threads = os.cpu_count() or 1
+    rows = np.arange(w.sq - 16, w.sq)
+    qp = rows + (w.skv - w.sq)
+    kh = C.prefill_kv_head_np(w, "k", 0, 0)
+    vh = C.prefill_kv_head_np(w, "v", 0, 0)
+    qr = C.prefill_q_rows_np(w, 0, 0, int(rows[0]), len(rows))
+    flops = 4.0 * w.d * float((np.minimum(qp, w.skv - 1) + 1).sum())
+
+    def one_step():
+        def run(s):
+            oracle.attention_rows(qr[s:s + 1], kh, vh, qp[s:s + 1], w.scale, w.causal, w.window)
+
+        return _timed_pool(run, range(len(rows)), threads)
+
     for _ in range(args.warmup):
-        oracle_prefill_sample(w, 1, 16, threads)
-    tot_s, tot_f, desc = 0.0, 0.0, ""
-    for _ in range(args.steps):
-        s, f, desc = oracle_prefill_sample(w, 1, 16, threads)
-        tot_s += s
-        tot_f += f
-    value = tot_f / tot_s / 1e12
+        one_step()
+    tot_s = sum(one_step() for _ in range(args.steps))
+    value = flops * args.steps / tot_s / 1e12
+    desc = (f"each step: head 0, the last {len(rows)} query rows of {w.name} (fp64, full "
+            f"score rows, {threads} threads)")
     line = {
         "impl": "reference", "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "b": w.b, "hq": w.hq, "hkv": w.hkv, "sq": w.sq,
-                   "skv": w.skv, "d": w.d, "causal": w.causal},
+        "config": workload_config(w, 1),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": "each step: " + desc},
+                         "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
+def HEADLINE(C):
+    """The headline workload: the largest single-GPU configuration, the 32K GQA prefill."""
+    return C.GQA_PREFILL_32K
+
+
+def workload_config(w, world):
+    return {"workload": w.name, "b": w.b, "hq": w.hq, "hkv": w.hkv, "sq": w.sq, "skv": w.skv,
+            "d": w.d, "causal": w.causal, "window": w.window, "o_dtype": w.o_dtype,
+            "q_outliers": w.outlier_frac,
+            "l2": "flushed between steps (256 MiB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def compact(ent):
+    """One workload's numbers in a few keys, for the summary at the end of the final line."""
+    if "error" in ent:
+        return {"error": ent["error"][:80]}
+    out = {"v": round(ent["value"], 1), "u": ent["unit"], "ms": round(ent["ms_per_step"], 4),
+           "frac": round(ent["roofline"]["frac"], 3)}
+    cpu = ent.get("cpu_baseline")
+    if cpu:
+        out["cpu"] = float(f"{cpu['value']:.3g}")
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-extra", action="store_true", help="only the main workload")
+    ap.add_argument("--no-extra", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="time only this named workload (profiling runs); prints its entry")
@@ -540,7 +710,8 @@ def main():
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    w = C.CAUSAL_PREFILL_2K
+    # the oracle beside each line: rank 0 of a single-GPU run only
+    cpu = (os.cpu_count() or 1) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else 0
 
     if args.workload is not None:
         wx = C.REGISTRY[args.workload]
@@ -558,55 +729,61 @@ def main():
             print(json.dumps(ent), flush=True)
         return 0
 
+    w = HEADLINE(C)
     extras = {}
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
         main_ent = prefill_entry(w, dev, args.steps, args.warmup, flush, stream, peaks, world,
-                                 e2e=True)
+                                 e2e=True, cpu_threads=cpu)
         torch.cuda.synchronize()
         barrier(world)
         if not args.no_extra:
             ext_steps = max(10, min(args.steps, 30))
             dec_steps = max(ext_steps, 50)
-            runs = [(wx.name, lambda wx=wx: prefill_entry(wx, dev, ext_steps, args.warmup, flush,
-                                                         stream, peaks, world))
-                    for wx in (C.GQA_PREFILL_32K, C.SWA_PREFILL_8K)]
-            runs += [(wx.name, lambda wx=wx: decode_entry(wx, dev, dec_steps, args.warmup, flush,
-                                                         stream, peaks, world))
-                     for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4)]
-            # packed sequences (attn_opts.cu_seqlens): 16 causal sequences with cached prefixes
-            runs.append((C.PACKED_PREFILL.name, lambda: packed_prefill_entry(
-                C.PACKED_PREFILL, dev, ext_steps, args.warmup, flush, stream, peaks, world)))
-            # the attention sink (attn_opts.sink) on the 2K prefill and the 1-token decode
-            runs.append((w.name + "+sink", lambda: prefill_entry(
-                w, dev, ext_steps, args.warmup, flush, stream, peaks, world, sink=True)))
-            runs.append((C.PAGED_DECODE.name + "+sink", lambda: decode_entry(
-                C.PAGED_DECODE, dev, dec_steps, args.warmup, flush, stream, peaks, world,
-                sink=True)))
-            # the FP8-e4m3 KV cache (attn_opts.kv_dtype): half the cache bytes
-            runs += [(wx.name + "+e4m3", lambda wx=wx: decode_entry(
-                wx, dev, dec_steps, args.warmup, flush, stream, peaks, world, e4m3=True))
-                for wx in (C.PAGED_DECODE, C.PAGED_DECODE_SPEC4)]
-            # a 4096-token window with RoPE of the queries (the pages' decode options)
-            runs.append((C.PAGED_DECODE_SPEC4.name + "+w4096+rope", lambda: decode_entry(
-                C.PAGED_DECODE_SPEC4, dev, dec_steps, args.warmup, flush, stream, peaks, world,
-                window=4096, rope=True)))
+
+            def pre(wx, **kw):
+                return lambda: prefill_entry(wx, dev, ext_steps, args.warmup, flush, stream, peaks,
+                                             world, cpu_threads=cpu, **kw)
+
+            def dec(wx, **kw):
+                return lambda: decode_entry(wx, dev, dec_steps, args.warmup, flush, stream, peaks,
+                                            world, cpu_threads=cpu, **kw)
+
+            runs = [
+                # the five workloads of the problem statement
+                (C.TINY_PREFILL.name, pre(C.TINY_PREFILL)),
+                (C.CAUSAL_PREFILL_2K.name, pre(C.CAUSAL_PREFILL_2K)),
+                (C.SWA_PREFILL_8K.name, pre(C.SWA_PREFILL_8K)),
+                (C.PAGED_DECODE.name, dec(C.PAGED_DECODE)),
+                (C.PAGED_DECODE_SPEC4.name, dec(C.PAGED_DECODE_SPEC4)),
+                # packed sequences (attn_opts.cu_seqlens): 16 causal sequences with prefixes
+                (C.PACKED_PREFILL.name, lambda: packed_prefill_entry(
+                    C.PACKED_PREFILL, dev, ext_steps, args.warmup, flush, stream, peaks, world,
+                    cpu_threads=cpu)),
+                # the attention sink (attn_opts.sink) on the 2K prefill and the 1-token decode
+                (C.CAUSAL_PREFILL_2K.name + "+sink", pre(C.CAUSAL_PREFILL_2K, sink=True)),
+                (C.PAGED_DECODE.name + "+sink", dec(C.PAGED_DECODE, sink=True)),
+                # the FP8-e4m3 KV cache (attn_opts.kv_dtype): half the cache bytes
+                (C.PAGED_DECODE.name + "+e4m3", dec(C.PAGED_DECODE, e4m3=True)),
+                (C.PAGED_DECODE_SPEC4.name + "+e4m3", dec(C.PAGED_DECODE_SPEC4, e4m3=True)),
+                # a 4096-token window with RoPE of the queries (the pages' decode options)
+                (C.PAGED_DECODE_SPEC4.name + "+w4096+rope",
+                 dec(C.PAGED_DECODE_SPEC4, window=4096, rope=True)),
+            ]
             for label, run in runs:
                 try:
                     ent = run()
-                except RuntimeError as e:  # a device-side error report: keep the main line
+                except RuntimeError as e:  # a device-side error report: keep the other lines
                     if world > 1:
                         raise  # ranks must stay in step for the collectives
                     torch.cuda.synchronize()
                     ent = {"workload": label, "error": str(e)}
                     print(f"bench: {label}: {e}", file=sys.stderr, flush=True)
                 extras[ent["workload"]] = ent
+                if rank == 0:  # each workload's full entry on a line of its own
+                    print(json.dumps({"bench_workload": ent}), flush=True)
     clocks = clk.summary()
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, os.cpu_count() or 1)
 
     if rank == 0:
         line = {
@@ -614,17 +791,17 @@ def main():
             "value": main_ent["value"], "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_ent["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) rounded to bf16)",
-            "config": {"workload": w.name, "b": w.b, "hq": w.hq, "hkv": w.hkv, "sq": w.sq,
-                       "skv": w.skv, "d": w.d, "causal": w.causal, "o_dtype": w.o_dtype,
-                       "l2": "flushed between steps (256 MiB write)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "data": "synthetic (seeded N(0,1) rounded to bf16; 1% of Q elements x8)",
+            "config": workload_config(w, world),
             "roofline": main_ent["roofline"],
             "e2e": main_ent["e2e"],
             "gpu_launches": main_ent["gpu_launches"],
             "clocks": clocks,
-            "cpu_baseline": cpu,
-            "workloads": extras,
+            "cpu_baseline": main_ent.get("cpu_baseline"),
+            # last, so that the end of the line carries every workload's numbers:
+            # v = throughput, u = its unit, ms per call, frac = roofline fraction (of
+            # measured peak), cpu = the oracle's rate on the host cores
+            "workloads": {k: compact(e) for k, e in extras.items()},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -95,3 +95,41 @@ def test_packed_prefill_flops_count_the_allowed_pairs():
             qp = oracle.q_pos(i, nq, nk)
             pairs += sum(oracle.allowed(j, nk, qp, True, 0) for j in range(nk))
     assert pw.flops() == 4 * pw.d * pw.hq * pairs
+
+
+def test_cpu_baselines_run_on_small_host_inputs(monkeypatch):
+    """The oracle timing legs of the benchmark on CPU tensors of small workloads: the full
+    and the sampled prefill, the packed prefill and every decode variant the benchmark
+    times (their sampling, page compaction and byte counts)."""
+    import torch
+
+    from workloads import configs as C
+
+    cpu = torch.device("cpu")
+    small = C.PrefillWorkload("small", 1, 2, 1, 300, 300, 64, True, 0, seed=3)
+    big = C.PrefillWorkload("big", 1, 16, 4, 1024, 1024, 64, True, 200, seed=4)
+    monkeypatch.setattr(bench, "FULL_PREFILL_FLOP", 1e8)  # small is below it, big above
+    for w, full in ((small, True), (big, False)):
+        q, k, v = C.prefill_inputs_torch(w, cpu)
+        ent = bench.cpu_prefill(w, q, k, v, 2, C.sink_logits(w.hq))
+        assert ent["value"] > 0 and ent["kind"] == "oracle" and ent["cores"] == 2
+        assert ("extrapolated_full_s" in ent) == (not full)
+    pw = C.PackedPrefillWorkload("small_packed", 4, 2, 64, 5, 20, 200, 50, seed=9)
+    q, k, v = C.prefill_inputs_torch(pw.as_prefill(), cpu)
+    assert bench.cpu_packed(pw, q, k, v, 2)["value"] > 0
+    wd = C.DecodeWorkload("small_decode", 3, 8, 2, 128, 4, len_lo=40, len_hi=300, seed=8)
+    t = C.decode_inputs_torch(wd, cpu)
+    te = C.decode_inputs_e4m3_torch(wd, cpu)
+    inv = bench.rope_inv_freq(wd.d)
+    for kw, tt in ((dict(), t), (dict(sink=C.sink_logits(wd.hq)), t), (dict(e4m3=True), te),
+                   (dict(window=64, inv_freq=inv), t)):
+        ent = bench.cpu_decode(wd, tt, 2, **kw)
+        assert ent["value"] > 0 and ent["unit"] == "GB/s" and "2 of 3 sequences" in ent["sample"]
+
+
+def test_final_line_summary_is_compact():
+    ent = {"value": 1454.123, "unit": "TFLOP/s", "ms_per_step": 6.0512, "roofline": {"frac": 0.7461},
+           "cpu_baseline": {"value": 0.0351234}}
+    assert bench.compact(ent) == {"v": 1454.1, "u": "TFLOP/s", "ms": 6.0512, "frac": 0.746,
+                                  "cpu": 0.0351}
+    assert "error" in bench.compact({"workload": "x", "error": "device error"})
