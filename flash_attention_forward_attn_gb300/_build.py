@@ -2,10 +2,17 @@
 
 Each translation unit under ``csrc/`` compiles in parallel, then they link into one
 shared library with the CUDA runtime linked statically (no torch types anywhere in it).
+
+A build is reused only when the stamp written beside the library holds the fingerprint of
+what would be built now: the contents of every source and header, the nvcc flags, nvcc's
+version and the host machine's architecture.  A library that arrives with a copied tree
+(or was built on another machine) therefore never passes for a current one.
 """
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -33,16 +40,35 @@ def _deps():
     return files
 
 
+STAMP = LIB + ".stamp"
+
+
+def fingerprint() -> str:
+    h = hashlib.sha256()
+    for f in sorted(_deps()):
+        h.update(os.path.basename(f).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    h.update(platform.machine().encode())
+    r = subprocess.run([_nvcc(), "--version"], capture_output=True, text=True)
+    h.update(r.stdout.encode())
+    return h.hexdigest()
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(f) <= t for f in _deps())
+    with open(STAMP) as fh:
+        return fh.read().strip() == fingerprint()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+    fp = fingerprint()
+    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
+        with open(STAMP) as fh:
+            if fh.read().strip() == fp:
+                return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
 
@@ -63,6 +89,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP + f".tmp{os.getpid()}", "w") as fh:
+        fh.write(fp + "\n")
+    os.replace(STAMP + f".tmp{os.getpid()}", STAMP)
     return LIB
 
 

@@ -12,7 +12,9 @@ pool (ctypes releases the GIL during each call).
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 from concurrent.futures import ThreadPoolExecutor
@@ -28,15 +30,35 @@ _lib = None
 ORACLE_ERRORS = {1: "invalid argument", 2: "page index out of range", 3: "out of memory"}
 
 
+_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off"]
+_STAMP = _LIB_PATH + ".stamp"
+
+
+def _fingerprint() -> str:
+    """The source, the flags, gcc's version and the machine: a library built from anything
+    else (a copied tree, another architecture) is rebuilt."""
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as fh:
+        h.update(fh.read())
+    h.update(" ".join(_CFLAGS).encode())
+    h.update(platform.machine().encode())
+    h.update(subprocess.run(["gcc", "--version"], capture_output=True, text=True).stdout.encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile attn_oracle.c into liboracle.so (gcc, -O2, strict IEEE: no fast-math)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
+    fp = _fingerprint()
+    if not force and os.path.exists(_LIB_PATH) and os.path.exists(_STAMP):
+        with open(_STAMP) as fh:
+            if fh.read().strip() == fp:
+                return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
-                    "-ffp-contract=off", "-o", tmp, _SRC, "-lm"], check=True)
+    subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
+    with open(_STAMP + f".tmp{os.getpid()}", "w") as fh:
+        fh.write(fp + "\n")
+    os.replace(_STAMP + f".tmp{os.getpid()}", _STAMP)
     return _LIB_PATH
 
 

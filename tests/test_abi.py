@@ -217,3 +217,16 @@ def test_prefill_workspace_bytes(lib):
     """One int per 128-row query tile."""
     for sq, n in [(-5, 0), (0, 0), (1, 4), (128, 4), (129, 8), (34910, 4 * 273)]:
         assert A.attn_prefill_workspace_bytes(sq) == n
+
+
+def test_a_library_without_a_matching_stamp_is_rebuilt(lib, tmp_path, monkeypatch):
+    """The rebuild decision rests on the fingerprint of the sources, flags, compiler and
+    machine, not on file times: a library whose stamp does not match (one copied in with a
+    tree, or built elsewhere) is never taken for a current build."""
+    assert _build.up_to_date()
+    stale = tmp_path / "stale.stamp"
+    stale.write_text("0" * 64 + "\n")
+    monkeypatch.setattr(_build, "STAMP", str(stale))
+    assert not _build.up_to_date()
+    monkeypatch.setattr(_build, "STAMP", str(tmp_path / "missing.stamp"))
+    assert not _build.up_to_date()
