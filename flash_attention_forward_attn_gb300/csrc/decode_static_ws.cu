@@ -16,9 +16,13 @@
 // combine step reads is written earlier in the same call -- so it is never cleared.
 //
 // In host code the array's name is only a stand-in for the symbol, not a device address.
-// The first call on each device (with that device current) looks the real address up
-// with cudaGetSymbolAddress and caches it; that first call should therefore happen before
-// any stream capture begins.
+// Every call made while its stream is not being captured looks the real address up with
+// cudaGetSymbolAddress (on the current device) and remembers it per device; a call made
+// during a stream capture uses the remembered address, because the lookup may load the
+// module, which a capture does not allow.  So the first call on each device should come
+// before any stream capture begins.  A device reset (cudaDeviceReset) unloads the module
+// and may move the array: the next call outside a capture picks up the new address, and
+// graphs captured before the reset must be captured again.
 #include <math.h>
 
 #include <mutex>
@@ -36,18 +40,24 @@ __device__ __align__(256) unsigned char g_decode_static_scratch[kDecodeStaticScr
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the static scratch on the current device (looked up once per device).
-cudaError_t static_scratch_address(void** out) {
+// Device address of the static scratch on the current device: looked up afresh when the
+// stream is not capturing, else the address remembered from an earlier call.
+cudaError_t static_scratch_address(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_decode_static_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
+    } else if (g_scratch_ptr[dev] == nullptr) {
+        return cudaErrorStreamCaptureUnsupported;  // no lookup before the capture began
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;
@@ -71,7 +81,7 @@ extern "C" attn_status attn_fwd_decode_static_ws(
     }
     if (need > attn::kDecodeStaticScratchBytes) return ATTN_ERR_WORKSPACE;
     void* scratch = nullptr;
-    if (attn::static_scratch_address(&scratch) != cudaSuccess) {
+    if (attn::static_scratch_address(static_cast<cudaStream_t>(stream), &scratch) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;
     }

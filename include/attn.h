@@ -296,8 +296,11 @@ attn_status attn_append_kv(const void* k_new, const void* v_new, void* k_cache, 
  * array, so calls that overlap on the GPU (on different streams, or from host threads
  * without ordering between them) race and give unspecified results; order them on one
  * stream.  The array needs no clearing: each call writes every part it later reads.
- * The first call on a device, with that device current, looks up the array's device
- * address (cudaGetSymbolAddress); make that first call before any stream capture begins.
+ * Each call made while `stream` is not being captured looks up the array's device
+ * address on the current device (cudaGetSymbolAddress) and remembers it; a call made
+ * during a capture uses the remembered address, so make the first call on each device
+ * before any stream capture begins (otherwise: ATTN_ERR_CUDA).  After a device reset the
+ * next call outside a capture finds the array's new address.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine is called.
  */
 attn_status attn_fwd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
