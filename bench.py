@@ -770,6 +770,8 @@ def main():
                 # a 4096-token window with RoPE of the queries (the pages' decode options)
                 (C.PAGED_DECODE_SPEC4.name + "+w4096+rope",
                  dec(C.PAGED_DECODE_SPEC4, window=4096, rope=True)),
+                # head_dim 256 decode
+                (C.PAGED_DECODE_D256.name, dec(C.PAGED_DECODE_D256)),
             ]
             for label, run in runs:
                 try:

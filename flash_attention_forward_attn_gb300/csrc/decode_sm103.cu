@@ -28,7 +28,6 @@ namespace {
 
 __device__ unsigned g_decode_error;
 
-constexpr int kBT = 32;          // tokens per pipeline slot
 constexpr int kConsumers = 4;    // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;
 // Consumer warp w takes tiles w, w + kConsumers, ... and waits on slot i % kStages at the
@@ -55,24 +54,27 @@ __device__ __forceinline__ bool decode_allowed_w(int j, int len, int s_active, i
 // cache keeps logical position j in slot j.  A circular flat cache of max_cache_len rows
 // keeps it in row j mod max_cache_len, so only min(len, max_cache_len) slots were ever
 // written and every one is read (the window covers nearly all of them).  Otherwise tiles
-// before the earliest window start are skipped (the start is rounded down to a 32-token tile).
+// before the earliest window start are skipped (the start is rounded down to a whole tile
+// of gran tokens, the kernel's tile: a power of two).
 __device__ __forceinline__ int decode_nslots(int len, int circular, int max_cache_len) {
     return circular ? min(len, max_cache_len) : len;
 }
-__device__ __forceinline__ int decode_first_slot(int len, int s_active, int window, int circular) {
-    return (window > 0 && !circular) ? (max(0, len - s_active - window + 1) & ~31) : 0;
+__device__ __forceinline__ int decode_first_slot(int len, int s_active, int window, int circular,
+                                                 int gran) {
+    return (window > 0 && !circular) ? (max(0, len - s_active - window + 1) & ~(gran - 1)) : 0;
 }
 
 // The slots a sequence reads, [first, nslots), are cut into ceil(span / chunk) splits of
-// near-equal size in whole 32-token tiles (never longer than chunk, so at most
-// ceil(max_cache_len / chunk) splits): split s covers [lo, hi), empty when lo >= hi.
+// near-equal size in whole tiles of gran tokens (at most ceil(max_cache_len / chunk)
+// splits): split s covers [lo, hi), empty when lo >= hi (possible only when chunk is not a
+// multiple of gran).
 __device__ __forceinline__ int decode_nsplits(int nslots, int first, int chunk) {
     return (nslots - first + chunk - 1) / chunk;
 }
-__device__ __forceinline__ void decode_split_range(int nslots, int first, int chunk, int s,
-                                                   int& lo, int& hi) {
+__device__ __forceinline__ void decode_split_range(int nslots, int first, int chunk, int gran,
+                                                   int s, int& lo, int& hi) {
     const int ns = decode_nsplits(nslots, first, chunk);
-    const int size = (((nslots - first) + ns - 1) / ns + 31) & ~31;
+    const int size = (((nslots - first) + ns - 1) / ns + gran - 1) & ~(gran - 1);
     lo = first + s * size;
     hi = min(nslots, lo + size);
 }
@@ -136,10 +138,14 @@ __device__ __forceinline__ void rope_rows(uint32_t& alo, uint32_t& ahi, uint32_t
     rope_apply(blo, bhi, s0, c0, s1, c1);
 }
 
-// A K (or V) tile of a slot is kBoxes column boxes of 32 rows x 128 bytes (64 bf16 or 128
+// A K (or V) tile of a slot is kBoxes column boxes of kBT rows x 128 bytes (64 bf16 or 128
 // e4m3 head dims per box), each written by TMA with the 128-byte swizzle.
 template <int D, bool kE4M3>
 struct DecodeLayout {
+    // Tokens per tile.  (64-token e4m3 tiles, one 16 KB slot per consumer warp, measured
+    // 0.67x the rate of 32-token tiles in two 8 KB slots: a warp then cannot compute one tile
+    // while the next one loads.)
+    static constexpr int kBT = 32;
     // Ring slots.  A CTA keeps kStages tiles in flight; with two CTAs per SM (registers) the
     // bf16 ring of 4 x 16 KB keeps HBM near its copy rate, and the e4m3 ring, with tiles half
     // as large, takes 8 slots (two per consumer warp) to keep the same bytes in flight.
@@ -155,7 +161,19 @@ struct DecodeLayout {
     static constexpr int kPipe = kStages * kSlot;
     static constexpr int kMerge = kConsumers * 16 * D * 4;
     static_assert(kMerge <= kPipe, "merge buffer must fit in the pipeline region");
-    static constexpr int kDynBytes = kPipe + 1024;      // + alignment slack
+    // The Q fragments (identical in every consumer warp) live in shared memory, 16 bytes per
+    // lane and k-step, read back per k-step, instead of D/4 registers per thread: with head_dim
+    // 256 they would not fit beside the 16 x 256 O, and with head_dim <= 128 the freed
+    // registers let three CTAs share an SM (measured on the 1- and 4-token decodes of 64
+    // sequences: bf16 6436 -> 6750 and 6141 -> 6391 GB/s, e4m3 4725 -> 5505 and 4394 ->
+    // 5041 GB/s, against two CTAs per SM with Q in registers).  At the 128 registers that
+    // allows, the bf16 kernel of head_dim 128 spills 24 bytes and still runs faster than
+    // its spill-free two-CTA build.
+    static constexpr bool kQInSmem = true;
+    static constexpr int kQSmem = (D / 16) * 32 * 16;
+    static constexpr int kDynBytes = kPipe + kQSmem + 1024;  // + alignment slack
+    static constexpr int kMinCtas = D > 128 ? 1 : 3;  // CTAs per SM the registers are fitted to
+    static_assert(kMinCtas * (kDynBytes + 1024) <= 232448, "shared memory of kMinCtas CTAs");
 };
 
 struct DecodeParams {
@@ -187,11 +205,12 @@ __device__ __forceinline__ bool mbar_wait_plain(uint64_t* bar, uint32_t parity,
 // f16 (the factor comes back out of the row's softmax scale), so the f16 row holds every
 // bf16 element exactly unless it is below 2^-27 of the row's largest.
 template <int D, bool kE4M3>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(
+__global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) decode_split_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const DecodeParams p) {
     using L = DecodeLayout<D, kE4M3>;
     constexpr int kStages = L::kStages;
+    constexpr int kBT = L::kBT;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* pipe = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -208,10 +227,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
     }
     // this split covers cache slots [tok0, tok1); the combine skips the splits that return here
     const int nslots = decode_nslots(len, p.circular, p.max_cache_len);
-    const int first = decode_first_slot(len, p.s_active, p.window, p.circular);
+    const int first = decode_first_slot(len, p.s_active, p.window, p.circular, kBT);
     if (split >= decode_nsplits(nslots, first, p.chunk)) return;  // a split this sequence lacks
     int tok0, tok1;
-    decode_split_range(nslots, first, p.chunk, split, tok0, tok1);
+    decode_split_range(nslots, first, p.chunk, kBT, split, tok0, tok1);
     if (tok0 >= tok1) return;  // an empty last split
     const int nblocks = (tok1 - tok0 + kBT - 1) / kBT;
 
@@ -392,45 +411,74 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 }
             }
         }
+        // the Q fragments go to shared memory (written once, by warp 0) and are read back per
+        // k-step, one 16-byte load per lane
+        uint4* const qs = reinterpret_cast<uint4*>(pipe + L::kPipe);
+        if constexpr (L::kQInSmem) {
+            if (warp == 0) {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    qs[ks * 32 + lane] = make_uint4(qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+        }
+        auto qfrag = [&](int ks, uint32_t* f) {
+            if constexpr (L::kQInSmem) {
+                const uint4 x = qs[ks * 32 + lane];
+                f[0] = x.x;
+                f[1] = x.y;
+                f[2] = x.z;
+                f[3] = x.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f[e] = qf[ks][e];
+            }
+        };
         float o[D / 8][4];
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        constexpr int kNT = kBT / 8;  // 8-token n-tiles of S per tile
 
         for (int i = warp; i < nblocks; i += kConsumers) {
             const int s = i % kStages;
             if (!mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_flag)) break;
             const uint32_t kbase = smem_u32(pipe + s * L::kSlot);
             const uint32_t vbase = kbase + L::kHalf;
-            // S = Q K^T for 16 rows x 32 tokens
-            float sc[4][4];
+            // S = Q K^T for 16 rows x kBT tokens
+            float sc[kNT][4];
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
             if constexpr (kE4M3) {
                 // token nt*8 + gq, head dims 16 ks + 4 qd .. +3 (chunk ks of its 128-byte row)
                 const uint8_t* kt = pipe + s * L::kSlot;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t qk[4];
+                    qfrag(ks, qk);
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
+                    for (int nt = 0; nt < kNT; ++nt) {
                         const int tok = nt * 8 + gq;
                         const uint32_t w = *reinterpret_cast<const uint32_t*>(
                             kt + (ks >> 3) * L::kBoxBytes + sw128_off(tok, ks & 7) + 4 * qd);
-                        mma_f16_16816(sc[nt], qf[ks], e4m3x2_to_f16x2(w & 0xffffu),
+                        mma_f16_16816(sc[nt], qk, e4m3x2_to_f16x2(w & 0xffffu),
                                       e4m3x2_to_f16x2(w >> 16));
                     }
                 }
             } else {
 #pragma unroll
                 for (int kp = 0; kp < D / 32; ++kp) {
+                    uint32_t qa[4], qb[4];
+                    qfrag(2 * kp, qa);
+                    qfrag(2 * kp + 1, qb);
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
+                    for (int nt = 0; nt < kNT; ++nt) {
                         const uint32_t tok = nt * 8 + (lane & 7);
                         const uint32_t cg = 4 * kp + (lane >> 3);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4(kbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
-                        mma_bf16_16816(sc[nt], qf[2 * kp], b0, b1);
-                        mma_bf16_16816(sc[nt], qf[2 * kp + 1], b2, b3);
+                        mma_bf16_16816(sc[nt], qa, b0, b1);
+                        mma_bf16_16816(sc[nt], qb, b2, b3);
                     }
                 }
             }
@@ -441,7 +489,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                               (p.window > 0 && j0 < len - p.window);
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
+            for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     float x0 = sc[nt][e] * c_row0, x1 = sc[nt][2 + e] * c_row1;
@@ -479,7 +527,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
                 o[n][3] *= a1;
             }
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
+            for (int nt = 0; nt < kNT; ++nt) {
                 sc[nt][0] = ex2(sc[nt][0] - mu0);
                 sc[nt][1] = ex2(sc[nt][1] - mu0);
                 sc[nt][2] = ex2(sc[nt][2] - mu1);
@@ -489,7 +537,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
             }
             // O += P V (P from the score accumulators)
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
+            for (int ks = 0; ks < kBT / 16; ++ks) {
                 uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
                 if (edge) {  // zero V rows of slots past the cache end (they may hold NaN)
                     const int jl = j0 + ks * 16 + 2 * qd;
@@ -647,8 +695,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __rest
                                                            const float* __restrict__ sink,
                                                            OutT* __restrict__ o, float* lse,
                                                            int hq, int s_active, int chunk,
-                                                           int max_splits, int max_cache_len,
-                                                           int window, int circular) {
+                                                           int gran, int max_splits,
+                                                           int max_cache_len, int window,
+                                                           int circular) {
     const size_t rowid = blockIdx.x;
     const int b = (int)(rowid / ((size_t)hq * s_active));
     const int x = threadIdx.x;
@@ -656,11 +705,11 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __rest
     float out = 0.f, lse_v = -INFINITY;
     if (len >= s_active && (circular || len <= max_cache_len)) {
         // the splits that ran (as decode_split_kernel): the non-empty ones
-        const int first = decode_first_slot(len, s_active, window, circular);
+        const int first = decode_first_slot(len, s_active, window, circular, gran);
         const int nslots = decode_nslots(len, circular, max_cache_len);
         int ns = decode_nsplits(nslots, first, chunk);
-        for (int lo, hi; ns > 0; --ns) {  // drop an empty last split
-            decode_split_range(nslots, first, chunk, ns - 1, lo, hi);
+        for (int lo, hi; ns > 0; --ns) {  // drop empty last splits
+            decode_split_range(nslots, first, chunk, gran, ns - 1, lo, hi);
             if (lo < hi) break;
         }
         const int s0 = 0;
@@ -776,6 +825,7 @@ template <int D, bool kE4M3>
 attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     using L = DecodeLayout<D, kE4M3>;
     const bool paged = a.block_table != nullptr;
+    constexpr int kBT = L::kBT;
     const int box_rows = paged ? (a.page_size < kBT ? a.page_size : kBT) : kBT;
     CUtensorMap tk, tv;
     uint64_t rows = paged ? (uint64_t)a.num_pages * a.hkv * a.page_size
@@ -827,11 +877,11 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     if (a.o_dtype == ATTN_BF16)
         decode_combine_kernel<D, __nv_bfloat16><<<nrows, D, 0, stream>>>(
             a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<__nv_bfloat16*>(a.o), a.lse, a.hq,
-            a.s_active, a.kv_chunk, a.max_splits, a.max_cache_len, a.window, a.circular);
+            a.s_active, a.kv_chunk, kBT, a.max_splits, a.max_cache_len, a.window, a.circular);
     else
         decode_combine_kernel<D, float><<<nrows, D, 0, stream>>>(
             a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<float*>(a.o), a.lse, a.hq, a.s_active,
-            a.kv_chunk, a.max_splits, a.max_cache_len, a.window, a.circular);
+            a.kv_chunk, kBT, a.max_splits, a.max_cache_len, a.window, a.circular);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

@@ -40,6 +40,11 @@ SMALL = [
     ("e4m3_flat_d256_sink", 2, 8, 2, 256, 1, 32, (33, 260), False, 64, 0.25, 1.25, True),
     ("e4m3_paged_mha_sa16", 1, 2, 2, 128, 16, 32, (50,), True, 32, 1.0, 1.0, False),
     ("e4m3_len_equals_sa", 2, 4, 1, 128, 4, 32, (4, 33), True, 32, 2.0, 0.5, False),
+    # head_dim 128 reads 64-token tiles: pages larger than a tile, a split length that is not
+    # a multiple of the tile (empty trailing splits), a flat cache of 64 k + 32 rows
+    ("e4m3_paged128_sa2", 2, 8, 2, 128, 2, 128, (300, 1000), True, 0, 1.0, 1.0, False),
+    ("e4m3_paged256_chunk96", 2, 8, 2, 128, 3, 256, (700, 95), True, 96, 1.0, 1.0, True),
+    ("e4m3_flat_rows_64k_plus_32", 2, 8, 2, 128, 1, 32, (100, 281), False, 32, 1.0, 1.0, False),
 ]
 
 

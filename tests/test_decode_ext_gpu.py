@@ -45,6 +45,7 @@ WINDOW = [
     ("win1000_paged16_sa3_d64", 2, 4, 4, 64, 3, 16, (17, 2100), True, 256, 1000, False),
     ("win129_paged64_d256", 2, 4, 2, 256, 2, 64, (70, 700), True, 128, 129, False),
     ("win300_paged_e4m3", 3, 8, 2, 128, 4, 32, (40, 1030, 777), True, 128, 300, True),
+    ("win333_paged128_e4m3_chunk96", 2, 8, 2, 128, 2, 128, (700, 1500), True, 96, 333, True),
 ]
 
 
@@ -83,6 +84,7 @@ CIRCULAR = [
     ("ring512_sa4_wrapped", 2, 8, 2, 128, 4, (1500, 513), 512, 400, 128, False),
     ("ring96_sa2_d64", 2, 4, 1, 64, 2, (95, 1000), 96, 95, 32, False),
     ("ring256_d256_e4m3", 2, 4, 2, 256, 3, (900, 41), 256, 200, 64, True),
+    ("ring288_e4m3_d128", 2, 8, 2, 128, 2, (1000, 150), 288, 250, 96, True),
 ]
 
 

@@ -131,8 +131,13 @@ SWA_PREFILL_8K_B1 = SWA_PREFILL_8K.with_(name="swa_prefill_b1_h32kv16_s8192_d256
 PAGED_DECODE_B16 = PAGED_DECODE.with_(name="paged_decode_b16_h32kv8_d128_sa1", b=16)
 PAGED_DECODE_SPEC4_B16 = PAGED_DECODE_SPEC4.with_(name="paged_decode_b16_h32kv8_d128_sa4", b=16)
 
+# head_dim 256 decode (the pages' head_dim bound), 32 sequences of the same length mix.
+PAGED_DECODE_D256 = DecodeWorkload("paged_decode_b32_h32kv8_d256_sa1", 32, 32, 8, 256, 1,
+                                   seed=0xA77E0006)
+
 REGISTRY = {w.name: w for w in ALL_PREFILL + ALL_DECODE + (
-    GQA_PREFILL_8K, SWA_PREFILL_8K_B1, PAGED_DECODE_B16, PAGED_DECODE_SPEC4_B16)}
+    GQA_PREFILL_8K, SWA_PREFILL_8K_B1, PAGED_DECODE_B16, PAGED_DECODE_SPEC4_B16,
+    PAGED_DECODE_D256)}
 
 
 # =========================================================================== prefill
