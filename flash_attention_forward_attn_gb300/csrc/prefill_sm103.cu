@@ -378,14 +378,16 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
                 if (rq > 0) wait_bounded(&q_full, (rq - 1) & 1);
             }
-        } else if ((warp == 1 || warp == 4) && lane == 0) {
+        } else if (warp == 1 || warp == 4) {
             // --------------------------------------------- S issuers (even / odd tiles)
             // A turn passes from tile T's issuer to tile T+1's once T's waits are done and
             // before its products are issued, so the two issue at once while every wait runs
             // in tile order.  That order matters for the K ring: the wait for K(T) on slot
             // T % NK reads the slot's phase by parity, which is only sound once K(T - NK),
             // the other issuer's tile when NK is odd, is known to have landed.  Four S
-            // buffers let the issuers drift apart, so nothing else ensures it.
+            // buffers let the issuers drift apart, so nothing else ensures it.  The whole
+            // warp runs the issuing code, waits included, and one elected lane issues (see
+            // the two-q-tile kernel): 8K window 1201 -> 1238 TFLOP/s.
             const int par = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             const uint64_t qd = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
@@ -400,45 +402,39 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 int bh, kvz;
                 const TileRange t = unit_at(w, bh, kvz);
                 if (t.n == 0) continue;
-                if (!wait_or_abort(&q_full, uq & 1, &abort_flag)) break;
+                if (!__all_sync(0xffffffffu, wait_or_abort(&q_full, uq & 1, &abort_flag))) break;
                 ++uq;
                 tc_fence_after();
                 for (int i = 0; i < t.n; ++i, ++T) {
                     if ((T & 1) != par) continue;
                     const int b = T % NS, slot = T % NK;
-                    if (!wait_or_abort(&turn[par], turns & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    ++turns;
                     // S buffer b is free once PV(T - NS) has read P(T - NS) out of it
-                    if (T >= NS && !wait_or_abort(&p_free[b], ((T / NS) - 1) & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!wait_or_abort(&k_full[slot], (T / NK) & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive(&turn[par ^ 1]);  // tile T+1's issuer may do its waits
+                    bool okw = wait_or_abort(&turn[par], turns & 1, &abort_flag);
+                    if (okw && T >= NS) okw = wait_or_abort(&p_free[b], ((T / NS) - 1) & 1, &abort_flag);
+                    if (okw) okw = wait_or_abort(&k_full[slot], (T / NK) & 1, &abort_flag);
+                    ok = __all_sync(0xffffffffu, okw);
+                    if (!ok) break;
+                    ++turns;
+                    mbar_arrive_w(&turn[par ^ 1]);  // tile T+1's issuer may do its waits
                     tc_fence_after();
                     const uint64_t kd = desc_add(kd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                         const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-                        tc_mma_ss(tmem + b * BN, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s,
-                                  kk > 0 ? 1u : 0u);
+                        tc_mma_ss_w(tmem + b * BN, desc_add(qd, off_a), desc_add(kd, off_b),
+                                    idesc_s, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(&s_full[b]);
-                    tc_commit(&k_empty[slot]);  // K(T) consumed once this product is done
+                    tc_commit_w(&s_full[b]);
+                    tc_commit_w(&k_empty[slot]);  // K(T) consumed once this product is done
                 }
-                if (ok) tc_commit(&q_empty);  // this issuer's products of the unit read Q no more
+                if (ok) tc_commit_w(&q_empty);  // this issuer's products of the unit read Q no more
             }
-            tc_commit(&mma_drain);
+            tc_commit_w(&mma_drain);
             wait_bounded(&mma_drain, 0);
-        } else if (warp == 3 && lane == 0) {
+        } else if (warp == 3) {
             // ----------------------------------------------------------- PV issuer
+            // (warp-collective like the S issuers)
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
             const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
             int T = 0;
@@ -451,27 +447,28 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 const TileRange t = unit_at(w, bh, kvz);
                 if (t.n == 0) continue;
                 // the previous unit's epilogue must have read O before it is overwritten
-                if (uo > 0 && !wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag)) break;
+                bool oko = true;
+                if (uo > 0) oko = wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag);
+                if (!__all_sync(0xffffffffu, oko)) break;
                 ++uo;
                 for (int i = 0; i < t.n; ++i, ++T) {
                     const int b = T % NS, slot = T % NV;
-                    if (!wait_or_abort(&p_full[b], (T / NS) & 1, &abort_flag) ||
-                        !wait_or_abort(&v_full[slot], (T / NV) & 1, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    const bool okw = wait_or_abort(&p_full[b], (T / NS) & 1, &abort_flag) &&
+                                     wait_or_abort(&v_full[slot], (T / NV) & 1, &abort_flag);
+                    ok = __all_sync(0xffffffffu, okw);
+                    if (!ok) break;
                     tc_fence_after();
                     const uint64_t vd = desc_add(vd0, (uint32_t)(slot * C::kSlotBytes));
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        tc_mma_ts(tmem + C::kColO, tmem + b * BN + kk * 8,
-                                  desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&p_free[b]);      // S buffer b may be rewritten; O holds PV(T)
-                    tc_commit(&v_empty[slot]);  // V(T) consumed
-                    if (i == t.n - 1) tc_commit(&o_done);
+                        tc_mma_ts_w(tmem + C::kColO, tmem + b * BN + kk * 8,
+                                    desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_w(&p_free[b]);      // S buffer b may be rewritten; O holds PV(T)
+                    tc_commit_w(&v_empty[slot]);  // V(T) consumed
+                    if (i == t.n - 1) tc_commit_w(&o_done);
                 }
             }
-            tc_commit(&mma_drain);
+            tc_commit_w(&mma_drain);
             wait_bounded(&mma_drain, 0);
         }
     } else if (warp < 12) {
@@ -883,15 +880,18 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 for (int x = 0; x < 2; ++x)
                     if (nq[x] > 0) wait_bounded(&q_full[x], (nq[x] - 1) & 1);
             }
-        } else if ((warp == 1 || warp == 3) && lane == 0) {
+        } else if (warp == 1 || warp == 3) {
             // ------------------------------------------------ MMA issuers, one per Q tile
-            // One thread issues tcgen05.mma at about one per 80-100 cycles, slower than the
-            // tensor pipe runs an M=128 N=128 K=16 product, and every wait or commit it makes
-            // between products leaves the pipe idle.  So tile A's products come from warp 1
-            // and tile B's from warp 3, taking turns per KV tile (a token passed through the
-            // turn barriers keeps the pipe order PV_A S_A | PV_B S_B | ...): each issuer does
-            // its waits while the other one issues, then its turn's products back to back.
-            // K and V slots are released once both have arrived (count-2 barriers).
+            // Tile A's products come from warp 1 and tile B's from warp 3, taking turns per KV
+            // tile (a token passed through the turn barriers keeps the pipe order
+            // PV_A S_A | PV_B S_B | ...): each issuer does its waits while the other one
+            // issues, then its turn's products back to back.  The whole warp runs this code,
+            // waits included, and one elected lane issues (the warp-collective forms of
+            // attn_ptx.cuh), so the issue keeps the pipe's rate while the softmax warps on the
+            // same sub-partitions run.  (Waits polled by lane 0 alone, with the verdict passed
+            // on by shuffle, made the kernel 2-3x slower in this form; every lane polling
+            // gave 2K 731 -> 760 and 32K 1474 -> 1553 TFLOP/s against the lane-0 issuer.)
+            // K and V slots are released once both issuers have arrived (count-2 barriers).
             const int x = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
@@ -915,9 +915,9 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 const TileRange t = x ? u.t[1] : u.t[0];
                 const bool has_x = x == 0 || u.has_b;  // tile X exists in this unit
                 if (has_x) {
-                    if (!wait_or_abort(&q_full[x], nq & 1, &abort_flag)) break;
+                    if (!__all_sync(0xffffffffu, wait_or_abort(&q_full[x], nq & 1, &abort_flag))) break;
                     ++nq;
-                    if (t.n == 0) tc_commit(&q_empty[x]);  // no product will read Q_X
+                    if (t.n == 0) tc_commit_w(&q_empty[x]);  // no product will read Q_X
                 }
                 // O_X may be overwritten once the epilogue has read out the previous unit
                 // in which tile X had products (o_free completes once per such unit, so it
@@ -931,14 +931,17 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     const bool in_k = have_k && j >= t.kt0 && j < t.kt0 + t.n;
                     const bool in_v = have_v && j - 1 >= t.kt0 && j - 1 < t.kt0 + t.n;
                     const int ks = Lk % NK, vs = (Lv + NV) % NV;
-                    // everything this turn's products need, before taking the turn
-                    if (have_v) ok = wait_or_abort(&v_full[vs], (Lv / NV) & 1, &abort_flag);
-                    if (ok && in_v && !freed) ok = freed = wait_or_abort(&o_free[x], (uo - 1) & 1, &abort_flag);
                     const int i = (j - 1) - t.kt0;  // index of V(j-1) within this tile's range
-                    if (ok && in_v) ok = wait_or_abort(pfull, (cbase + i) & 1, &abort_flag);
-                    if (ok && have_k) ok = wait_or_abort(&k_full[ks], (Lk / NK) & 1, &abort_flag);
-                    if (ok) ok = wait_or_abort(&turn[x], turns & 1, &abort_flag);
+                    // everything this turn's products need, before taking the turn
+                    bool okw = true;
+                    if (have_v) okw = wait_or_abort(&v_full[vs], (Lv / NV) & 1, &abort_flag);
+                    if (okw && in_v && !freed) okw = wait_or_abort(&o_free[x], (uo - 1) & 1, &abort_flag);
+                    if (okw && in_v) okw = wait_or_abort(pfull, (cbase + i) & 1, &abort_flag);
+                    if (okw && have_k) okw = wait_or_abort(&k_full[ks], (Lk / NK) & 1, &abort_flag);
+                    if (okw) okw = wait_or_abort(&turn[x], turns & 1, &abort_flag);
+                    ok = __all_sync(0xffffffffu, okw);
                     if (!ok) break;
+                    if (in_v) freed = true;
                     ++turns;
                     tc_fence_after();
                     if (in_v) {
@@ -946,8 +949,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                         const uint64_t vd = desc_add(vd0, (uint32_t)(vs * C::kSlotBytes));
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
-                            tc_mma_ts(tm_ox, tm_sx + kk * 8, desc_add(vd, kk * 16 * 128), idesc_o,
-                                      (i > 0 || kk > 0) ? 1u : 0u);
+                            tc_mma_ts_w(tm_ox, tm_sx + kk * 8, desc_add(vd, kk * 16 * 128),
+                                        idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     if (in_k) {
                         // S_X = Q_X K(j)^T
@@ -956,32 +959,32 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off_a = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                             const uint32_t off_b = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-                            tc_mma_ss(tm_sx, desc_add(qd, off_a), desc_add(kd, off_b), idesc_s,
-                                      kk > 0 ? 1u : 0u);
+                            tc_mma_ss_w(tm_sx, desc_add(qd, off_a), desc_add(kd, off_b),
+                                        idesc_s, kk > 0 ? 1u : 0u);
                         }
                     }
-                    mbar_arrive(&turn[x ^ 1]);  // the other tile's turn
+                    mbar_arrive_w(&turn[x ^ 1]);  // the other tile's turn
                     if (in_k) {
-                        tc_commit(sfull);
+                        tc_commit_w(sfull);
                         ++cnt;
                     }
-                    if (in_v && i == t.n - 1) tc_commit(&o_done[x]);  // the unit's last into O_X
+                    if (in_v && i == t.n - 1) tc_commit_w(&o_done[x]);  // the unit's last into O_X
                     // this tile is done with V(j-1) and K(j) once the products above finish
                     // (or at once if it never reads them)
                     if (have_v) {
-                        if (in_v) tc_commit(&v_empty[vs]);
-                        else mbar_arrive(&v_empty[vs]);
+                        if (in_v) tc_commit_w(&v_empty[vs]);
+                        else mbar_arrive_w(&v_empty[vs]);
                     }
                     if (have_k) {
-                        if (in_k) tc_commit(&k_empty[ks]);
-                        else mbar_arrive(&k_empty[ks]);
+                        if (in_k) tc_commit_w(&k_empty[ks]);
+                        else mbar_arrive_w(&k_empty[ks]);
                     }
-                    if (in_k && j == t.kt0 + t.n - 1) tc_commit(&q_empty[x]);  // last S of tile X
+                    if (in_k && j == t.kt0 + t.n - 1) tc_commit_w(&q_empty[x]);  // last S of tile X
                 }
                 if (t.n > 0) ++uo;
                 Lbase += nu;
             }
-            tc_commit(&mma_drain);
+            tc_commit_w(&mma_drain);
             wait_bounded(&mma_drain, 0);
         }
     } else {
