@@ -544,10 +544,10 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                     pmax = 0u;
 #pragma unroll
                     for (int e = 0; e < BN / 2; ++e) {
-                        const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
-                        const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
-                        ls[(2 * e) & 7] += p0;
-                        ls[(2 * e + 1) & 7] += p1;
+                        float a0, a1;
+                        ffma2(a0, a1, v[2 * e], v[2 * e + 1], cm, cm, -m_e, -m_e);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        fadd2(ls[(2 * e) & 7], ls[(2 * e + 1) & 7], ls[(2 * e) & 7], ls[(2 * e + 1) & 7], p0, p1);
                         pk[e] = pack_bf16(p0, p1);
                         pmax = __vmaxu2(pmax, pk[e]);
                     }
@@ -932,13 +932,15 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     const bool in_v = have_v && j - 1 >= t.kt0 && j - 1 < t.kt0 + t.n;
                     const int ks = Lk % NK, vs = (Lv + NV) % NV;
                     const int i = (j - 1) - t.kt0;  // index of V(j-1) within this tile's range
-                    // everything this turn's products need, before taking the turn
+                    // everything this turn's products need, before taking the turn; P_X(j-1),
+                    // which the softmax finishes last, is waited for last, so that the turn
+                    // starts one barrier round trip after it
                     bool okw = true;
                     if (have_v) okw = wait_or_abort(&v_full[vs], (Lv / NV) & 1, &abort_flag);
                     if (okw && in_v && !freed) okw = wait_or_abort(&o_free[x], (uo - 1) & 1, &abort_flag);
-                    if (okw && in_v) okw = wait_or_abort(pfull, (cbase + i) & 1, &abort_flag);
                     if (okw && have_k) okw = wait_or_abort(&k_full[ks], (Lk / NK) & 1, &abort_flag);
                     if (okw) okw = wait_or_abort(&turn[x], turns & 1, &abort_flag);
+                    if (okw && in_v) okw = wait_or_abort(pfull, (cbase + i) & 1, &abort_flag);
                     ok = __all_sync(0xffffffffu, okw);
                     if (!ok) break;
                     if (in_v) freed = true;
@@ -1063,10 +1065,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     for (int e = 0; e < 8; ++e) ls[e] = 0.f;
 #pragma unroll
                     for (int e = 0; e < BN / 2; ++e) {
-                        const float p0 = ex2(fmaf(v[2 * e], cm, -m_e));
-                        const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_e));
-                        ls[(2 * e) & 7] += p0;
-                        ls[(2 * e + 1) & 7] += p1;
+                        float a0, a1;
+                        ffma2(a0, a1, v[2 * e], v[2 * e + 1], cm, cm, -m_e, -m_e);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        fadd2(ls[(2 * e) & 7], ls[(2 * e + 1) & 7], ls[(2 * e) & 7], ls[(2 * e + 1) & 7], p0, p1);
                         pk[e] = pack_bf16(p0, p1);
                     }
                     return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
@@ -1103,10 +1105,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                     for (int e = 0; e < 8; ++e) ls[e] = 0.f;
 #pragma unroll
                     for (int e = 0; e < BN / 2; ++e) {
-                        const float p0 = ex2(fmaf(v[2 * e], cm, -m_used));
-                        const float p1 = ex2(fmaf(v[2 * e + 1], cm, -m_used));
-                        ls[(2 * e) & 7] += p0;
-                        ls[(2 * e + 1) & 7] += p1;
+                        float a0, a1;
+                        ffma2(a0, a1, v[2 * e], v[2 * e + 1], cm, cm, -m_used, -m_used);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        fadd2(ls[(2 * e) & 7], ls[(2 * e + 1) & 7], ls[(2 * e) & 7], ls[(2 * e + 1) & 7], p0, p1);
                         pk[e] = pack_bf16(p0, p1);
                         pmax = __vmaxu2(pmax, pk[e]);
                     }
