@@ -220,13 +220,14 @@ def attn_fwd_prefill(q, k, v, *, causal: bool, window: int = 0, scale: float | N
 
 def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float | None = None,
                         o=None, lse=None, o_dtype=None, sink=None, cu_seqlens_q=None,
-                        cu_seqlens_k=None, balance: bool = True, stream=None):
+                        cu_seqlens_k=None, balance: bool = True, workspace=None, stream=None):
     """attn_fwd_prefill with the attn_opts options: sink, an fp32 [hq] tensor of
     per-query-head sink logits (scaled-score units) on q's device, or None; and packed
     sequences: cu_seqlens_q / cu_seqlens_k int32 [nseq + 1] offsets along sq and skv of a
     b = 1 problem (each sequence its own problem, queries at the tail of its keys).  With
-    packed sequences and balance, a scratch buffer is allocated for the library's work
-    order (query tiles by KV-tile count); results do not depend on it."""
+    packed sequences and balance, the library's work order (query units by sequence, then
+    by KV-tile count) goes to `workspace` (a uint8 tensor of attn_prefill_workspace_bytes(sq)
+    bytes on q's device; allocated here when None); results do not depend on it."""
     import torch
 
     lib = load_library()
@@ -244,9 +245,15 @@ def attn_fwd_prefill_ex(q, k, v, *, causal: bool, window: int = 0, scale: float 
         opts.nseq = cu_seqlens_q.shape[0] - 1
         if balance and sq > 0:
             nbytes = lib.attn_prefill_workspace_bytes(sq)
-            ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-            if stream is not None:
-                ws.record_stream(stream)  # freed only once the call on `stream` is done
+            if workspace is None:
+                ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+                if stream is not None:
+                    ws.record_stream(stream)  # freed only once the call on `stream` is done
+            else:
+                _req(workspace, "workspace", torch.uint8, q.device)
+                ws = workspace
+                if ws.numel() < nbytes:
+                    raise ValueError(f"workspace holds {ws.numel()} bytes, {nbytes} needed")
             opts.prefill_workspace = ws.data_ptr()
             opts.prefill_workspace_bytes = nbytes
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)

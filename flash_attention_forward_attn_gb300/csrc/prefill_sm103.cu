@@ -166,7 +166,9 @@ __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) 
 // KV-tile count, most first, ties by index.  Unit indices in the persistent kernels then
 // run through this list, so the zig-zag pairs heavy with light units on every CTA as it
 // does for one causal problem, where the index order already is the order of the work.
-// One CTA; the (count, index) keys are sorted by a bitonic network in shared memory.
+// (Grouping the units by sequence first, so that fewer sequences' K/V are in flight at
+// once, measured 6% slower on 16 sequences: 844 -> 791 TFLOP/s.)  One CTA; the (count,
+// index) keys are sorted by a bitonic network in shared memory.
 constexpr int kOrderMax = 8192;  // units sorted in one CTA (64 KB of keys)
 constexpr int kOrderThreads = 1024;
 
@@ -288,7 +290,10 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
     auto unit_at = [&](int w, int& bh, int& kvz) -> TileRange {
         int qt = p.nqt - 1 - w / p.nbh;
         if constexpr (kPacked)
-            if (p.order) qt = __ldg(p.order + w / p.nbh);
+            if (p.order) {
+                qt = __ldg(p.order + w / p.nbh);
+                if (qt < 0 || qt >= p.nqt) qt = p.nqt;  // never trust an index: past sq = no work
+            }
         bh = w % p.nbh;
         const int bidx = bh / p.hq, h = bh % p.hq;
         kvz = bidx * p.hkv + h / p.group;
@@ -769,7 +774,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
         Unit u;
         int pair = npairs - 1 - w / p.nbh;
         if constexpr (kPacked)
-            if (p.order) pair = __ldg(p.order + w / p.nbh);
+            if (p.order) {
+                pair = __ldg(p.order + w / p.nbh);
+                if (pair < 0 || pair >= npairs) pair = npairs;  // never trust an index: no work
+            }
         u.bh = w % p.nbh;
         const int bidx = u.bh / p.hq, h = u.bh % p.hq;
         u.kvz = bidx * p.hkv + h / p.group;
