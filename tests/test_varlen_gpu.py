@@ -212,4 +212,3 @@ def test_work_order_is_the_units_sorted_by_kv_tiles(d, packing, causal, window, 
     assert sorted(order) == list(range(nu))
     keys = [(-cost[u], u) for u in order]
     assert keys == sorted(keys)
-
