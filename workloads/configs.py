@@ -135,9 +135,11 @@ PAGED_DECODE_SPEC4_B16 = PAGED_DECODE_SPEC4.with_(name="paged_decode_b16_h32kv8_
 PAGED_DECODE_D256 = DecodeWorkload("paged_decode_b32_h32kv8_d256_sa1", 32, 32, 8, 256, 1,
                                    seed=0xA77E0006)
 
+PAGED_DECODE_D256_B8 = PAGED_DECODE_D256.with_(name="paged_decode_b8_h32kv8_d256_sa1", b=8)
+
 REGISTRY = {w.name: w for w in ALL_PREFILL + ALL_DECODE + (
     GQA_PREFILL_8K, SWA_PREFILL_8K_B1, PAGED_DECODE_B16, PAGED_DECODE_SPEC4_B16,
-    PAGED_DECODE_D256)}
+    PAGED_DECODE_D256, PAGED_DECODE_D256_B8)}
 
 
 # =========================================================================== prefill
