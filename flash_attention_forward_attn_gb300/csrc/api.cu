@@ -2,6 +2,7 @@
 // carving, and dispatch to the kernel translation units.  Nothing here allocates device
 // memory or touches tensor contents.
 #include <math.h>
+#include <algorithm>
 #include <stdio.h>
 
 #include "attn_internal.h"
@@ -122,18 +123,24 @@ int resolve_chunk(int kv_chunk, int b, int max_cache_len) {
     return kv_chunk == 0 ? attn::default_kv_chunk(b, max_cache_len) : kv_chunk;
 }
 
-// Split-KV scratch: partial outputs [rows][max_splits][d] fp32, then (m, l) pairs.
+// Split-KV scratch: partial outputs [rows][slots][d] fp32 (256-byte padded), their (m, l)
+// pairs [rows][slots][2] (16-byte padded), then the piece count of every (sequence, kv
+// head) pair (b * hq ints, as hkv <= hq).  A CTA of the split pass reads at least kv_chunk
+// tokens unless it reads the last ones, so a pair of n tokens meets at most
+// ceil(n / kv_chunk) + 1 CTAs: slots = ceil(max_cache_len / kv_chunk) + 1.
 bool decode_scratch_sizes(int b, int hq, int s_active, int d, int max_cache_len, int kv_chunk,
-                          size_t* o_bytes, size_t* ml_bytes, int* max_splits) {
+                          size_t* o_bytes, size_t* ml_bytes, size_t* np_bytes, int* max_slots) {
     if (b <= 0 || hq <= 0 || s_active <= 0 || !head_dim_ok(d) || max_cache_len <= 0) return false;
     if (kv_chunk < 0 || (kv_chunk % 32) != 0) return false;
     const int chunk = resolve_chunk(kv_chunk, b, max_cache_len);
-    const long long splits = (max_cache_len + (long long)chunk - 1) / chunk;
+    const long long slots = (max_cache_len + (long long)chunk - 1) / chunk + 1;
     const long long rows = (long long)b * hq * s_active;
-    *max_splits = (int)splits;
-    *o_bytes = (size_t)(rows * splits * d * 4);
+    *max_slots = (int)slots;
+    *o_bytes = (size_t)(rows * slots * d * 4);
     *o_bytes = (*o_bytes + 255) & ~(size_t)255;
-    *ml_bytes = (size_t)(rows * splits * 2 * 4);
+    *ml_bytes = (size_t)(rows * slots * 2 * 4);
+    *ml_bytes = (*ml_bytes + 15) & ~(size_t)15;
+    *np_bytes = (size_t)b * hq * 4;
     return true;
 }
 
@@ -193,10 +200,11 @@ size_t attn_prefill_workspace_bytes(int sq) { return prefill_ws_bytes(sq); }
 
 size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_cache_len,
                                    int kv_chunk) {
-    size_t ob, mlb;
+    size_t ob, mlb, npb;
     int ms;
-    if (!decode_scratch_sizes(b, hq, s_active, d, max_cache_len, kv_chunk, &ob, &mlb, &ms)) return 0;
-    return ob + mlb;
+    if (!decode_scratch_sizes(b, hq, s_active, d, max_cache_len, kv_chunk, &ob, &mlb, &npb, &ms))
+        return 0;
+    return ob + mlb + npb;
 }
 
 attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -231,11 +239,23 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
     } else if ((long long)b * hkv * max_cache_len > 0x7fffffffLL) {
         return ATTN_ERR_UNSUPPORTED;
     }
-    size_t ob, mlb;
-    int max_splits;
-    if (!decode_scratch_sizes(b, hq, s_active, d, max_cache_len, kv_chunk, &ob, &mlb, &max_splits))
+    size_t ob, mlb, npb;
+    int max_slots;
+    if (!decode_scratch_sizes(b, hq, s_active, d, max_cache_len, kv_chunk, &ob, &mlb, &npb,
+                              &max_slots))
         return ATTN_ERR_INVALID_ARG;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < ob + mlb) return ATTN_ERR_WORKSPACE;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < ob + mlb + npb)
+        return ATTN_ERR_WORKSPACE;
+    const int chunk = resolve_chunk(kv_chunk, b, max_cache_len);
+    if (op.window > 0 && !op.circular) {
+        // A window that does not wrap bounds the slots any sequence reads: its start is
+        // rounded down to a whole tile, so at most window + s_active - 1 + (tile - 1)
+        // slots, and no pair has more pieces than that span allows (the partials keep
+        // the scratch's layout, with this smaller stride).
+        const long long span = std::min<long long>(
+            max_cache_len, (long long)op.window + s_active - 1 + (attn::kDecodeTile - 1));
+        max_slots = (int)std::min<long long>(max_slots, (span + chunk - 1) / chunk + 1);
+    }
     attn::DecodeArgs a;
     a.q = q;
     a.k_cache = k_cache;
@@ -255,10 +275,11 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
     a.o = o;
     a.lse = lse;
     a.o_dtype = o_dtype;
-    a.kv_chunk = resolve_chunk(kv_chunk, b, max_cache_len);
+    a.kv_chunk = chunk;
     a.part_o = static_cast<float*>(workspace);
     a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ob);
-    a.max_splits = max_splits;
+    a.npieces = reinterpret_cast<int*>(static_cast<char*>(workspace) + ob + mlb);
+    a.max_slots = max_slots;
     a.sink = op.sink;
     a.kv_e4m3 = op.e4m3 ? 1 : 0;
     a.k_scale = op.k_scale;

@@ -69,9 +69,10 @@ struct DecodeArgs {
     float* lse;
     attn_dtype o_dtype;
     int kv_chunk;         // resolved (> 0)
-    float* part_o;        // [b*hq*s_active][max_splits][d]
-    float* part_ml;       // [b*hq*s_active][max_splits][2]
-    int max_splits;
+    float* part_o;        // [b*hq*s_active][max_slots][d]: one partial per piece of a pair
+    float* part_ml;       // [b*hq*s_active][max_slots][2]
+    int* npieces;         // [b*hkv]: pieces written for each (sequence, kv head)
+    int max_slots;        // partials a pair may need (kv_chunk bounds the piece count)
     const float* sink;    // [hq] sink logits, or NULL
     int kv_e4m3;          // the caches hold e4m3 bytes
     float k_scale, v_scale;  // their dequantisation scales (1 for bf16)
@@ -91,6 +92,10 @@ struct AppendArgs {
     int b, hkv, d, s_active, page_size, max_pages_per_seq, num_pages, max_cache_len, circular;
     const float* rope_inv_freq;  // [d/2], or NULL
 };
+
+// Tokens per tile of the decode kernels: splits cover whole tiles, and a window's first
+// slot is rounded down to a tile boundary.
+constexpr int kDecodeTile = 32;
 
 // Tokens per split when the caller passes kv_chunk = 0: the largest power of two in
 // [kMinDefaultKvChunk, kMaxDefaultKvChunk] that is at most b * max_cache_len / 128, i.e.

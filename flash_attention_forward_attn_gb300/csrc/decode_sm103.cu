@@ -3,21 +3,22 @@
 // Method ("Flash-Attention: Decode (TKG)"): s_active new tokens per sequence attend the
 // whole cache; the q-head group of one kv head is flattened into one tile of
 // group * s_active <= 16 rows ("GQA / MQA grouped-query broadcast"), so every K/V byte
-// is read once per kv head.  The cache axis is split into chunks of kv_chunk tokens,
-// each chunk keeping its own running max m, sum l and unnormalised output (the online
-// softmax recurrence of "Flash-Attention: Context (CTE)", "The online-softmax
-// recurrence"); a second kernel merges the chunks by log-sum-exp, i.e. the deferred
-// normalise of the TKG flash path.
+// is read once per kv head.  The cache axis is split into pieces, each keeping its own
+// running max m, sum l and unnormalised output (the online softmax recurrence of
+// "Flash-Attention: Context (CTE)", "The online-softmax recurrence"); a second kernel
+// merges the pieces by log-sum-exp, i.e. the deferred normalise of the TKG flash path.
 //
-// GB300 design: one CTA per (chunk, kv head, sequence).  One producer thread streams
-// 32-token K and V tiles with TMA (128-byte swizzle) into a 4-slot shared-memory ring
-// under mbarriers, fetching each page through the block table ("Paged / block cache");
-// four consumer warps take alternate tiles, each with its own (m, l, O) state, and
-// merge through shared memory at the end.  The 16-row contractions run on the warp
-// MMA (m16n8k16, bf16 in, fp32 accumulate): with 16 rows an fp32 FMA path would need
-// more arithmetic than the CUDA cores deliver at HBM speed.  Slots past cache_len may
-// hold anything: their scores are replaced by -inf (select, so NaN never propagates)
-// and their V rows are zeroed in registers before the P.V product.
+// GB300 design: one wave of persistent CTAs (as many as the SMs hold) shares the KV tiles
+// of all (sequence, kv head) pairs evenly, as one stream; a CTA's run is cut into pieces
+// where it crosses from one pair to the next.  One producer thread streams 32-token K and
+// V tiles with TMA (128-byte swizzle) into a shared-memory ring under mbarriers, fetching
+// each page through the block table ("Paged / block cache"), and prepares each piece's Q
+// ahead of it; four consumer warps take alternate tiles, each with its own (m, l, O)
+// state, and merge through shared memory at the end of each piece.  The 16-row
+// contractions run on the warp MMA (m16n8k16, bf16 in, fp32 accumulate): with 16 rows an
+// fp32 FMA path would need more arithmetic than the CUDA cores deliver at HBM speed.
+// Slots past cache_len may hold anything: their scores are replaced by -inf (select, so
+// NaN never propagates) and their V rows are zeroed in registers before the P.V product.
 #include <type_traits>
 
 #include "attn_internal.h"
@@ -64,20 +65,13 @@ __device__ __forceinline__ int decode_first_slot(int len, int s_active, int wind
     return (window > 0 && !circular) ? (max(0, len - s_active - window + 1) & ~(gran - 1)) : 0;
 }
 
-// The slots a sequence reads, [first, nslots), are cut into ceil(span / chunk) splits of
-// near-equal size in whole tiles of gran tokens (at most ceil(max_cache_len / chunk)
-// splits): split s covers [lo, hi), empty when lo >= hi (possible only when chunk is not a
-// multiple of gran).
-__device__ __forceinline__ int decode_nsplits(int nslots, int first, int chunk) {
-    return (nslots - first + chunk - 1) / chunk;
+// Programmatic dependent launch: a grid lets its stream successor (launched with
+// programmatic stream serialisation) start, and that successor waits for its predecessor
+// grid to complete, with its memory visible, before it reads the predecessor's output.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-__device__ __forceinline__ void decode_split_range(int nslots, int first, int chunk, int gran,
-                                                   int s, int& lo, int& hi) {
-    const int ns = decode_nsplits(nslots, first, chunk);
-    const int size = (((nslots - first) + ns - 1) / ns + gran - 1) & ~(gran - 1);
-    lo = first + s * size;
-    hi = min(nslots, lo + size);
-}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Logical position held by slot r of a circular cache of cap rows whose newest position
 // is len - 1 (r < min(len, cap)).
@@ -145,7 +139,7 @@ struct DecodeLayout {
     // Tokens per tile.  (64-token e4m3 tiles, one 16 KB slot per consumer warp, measured
     // 0.67x the rate of 32-token tiles in two 8 KB slots: a warp then cannot compute one tile
     // while the next one loads.)
-    static constexpr int kBT = 32;
+    static constexpr int kBT = kDecodeTile;
     // Ring slots.  A CTA keeps kStages tiles in flight; with two CTAs per SM (registers) the
     // bf16 ring of 4 x 16 KB keeps HBM near its copy rate, and the e4m3 ring, with tiles half
     // as large, takes 8 slots (two per consumer warp) to keep the same bytes in flight.
@@ -159,31 +153,31 @@ struct DecodeLayout {
     static constexpr int kHalf = kBoxes * kBoxBytes;    // K (or V) tile of one slot
     static constexpr int kSlot = 2 * kHalf;
     static constexpr int kPipe = kStages * kSlot;
-    static constexpr int kMerge = kConsumers * 16 * D * 4;
-    static_assert(kMerge <= kPipe, "merge buffer must fit in the pipeline region");
-    // The Q fragments (identical in every consumer warp) live in shared memory, 16 bytes per
-    // lane and k-step, read back per k-step, instead of D/4 registers per thread: with head_dim
-    // 256 they would not fit beside the 16 x 256 O, and with head_dim <= 128 the freed
-    // registers let three CTAs share an SM (measured on the 1- and 4-token decodes of 64
-    // sequences: bf16 6436 -> 6750 and 6141 -> 6391 GB/s, e4m3 4725 -> 5505 and 4394 ->
-    // 5041 GB/s, against two CTAs per SM with Q in registers).  At the 128 registers that
-    // allows, the bf16 kernel of head_dim 128 spills 24 bytes and still runs faster than
-    // its spill-free two-CTA build.
-    static constexpr bool kQInSmem = true;
+    // The Q fragments of a piece (identical in every consumer warp) live in shared memory,
+    // 16 bytes per lane and k-step, read back per k-step, instead of D/4 registers per
+    // thread: with head_dim 256 they would not fit beside the 16 x 256 O, and with head_dim
+    // <= 128 the freed registers let three CTAs share an SM (measured on the 1- and 4-token
+    // decodes of 64 sequences: bf16 6436 -> 6750 and 6141 -> 6391 GB/s, e4m3 4725 -> 5505
+    // and 4394 -> 5041 GB/s, against two CTAs per SM with Q in registers).  Two slots: the
+    // producer prepares the next piece's Q while the consumers work on this one, and a
+    // finished piece's slot (32 D bytes, half of one warp's O) carries the piece's merge.
     static constexpr int kQSmem = (D / 16) * 32 * 16;
-    static constexpr int kDynBytes = kPipe + kQSmem + 1024;  // + alignment slack
+    static constexpr int kDynBytes = kPipe + 2 * kQSmem + 1024;  // + alignment slack
     static constexpr int kMinCtas = D > 128 ? 1 : 3;  // CTAs per SM the registers are fitted to
-    static_assert(kMinCtas * (kDynBytes + 1024) <= 232448, "shared memory of kMinCtas CTAs");
+    // dynamic + static (barriers, piece records, merge maxima: under 1 KB) + the 1 KB the
+    // SM reserves per CTA
+    static_assert(kMinCtas * (kDynBytes + 2048) <= 232448, "shared memory of kMinCtas CTAs");
 };
 
 struct DecodeParams {
     const __nv_bfloat16* q;
     const uint32_t* table;
     const int32_t* cache_len;
-    float* part_o;
-    float* part_ml;
-    int hq, hkv, s_active, page_size, max_pages, num_pages, max_cache_len;
-    int group, rows, chunk, max_splits, paged, box_rows;
+    float* part_o;   // [b*hq*s_active][max_slots][d]: one partial per piece of a pair
+    float* part_ml;  // [b*hq*s_active][max_slots][2]
+    int* npieces;    // [b*hkv]: pieces written for each (sequence, kv head)
+    int b, hq, hkv, s_active, page_size, max_pages, num_pages, max_cache_len;
+    int group, rows, min_tiles, max_slots, paged, box_rows;
     int window, circular;    // decode window (0 = none); circular flat cache
     const float* rope_inv_freq;  // [d/2] RoPE inverse frequencies of Q, or NULL
     float c;        // scale * log2(e) (* k_scale for an e4m3 cache)
@@ -198,12 +192,57 @@ __device__ __forceinline__ bool mbar_wait_plain(uint64_t* bar, uint32_t parity,
     return true;
 }
 
+// Tiles that every kv head of sequence b reads: 0 for a cache_len out of range (the merge
+// reports it).
+__device__ __forceinline__ int pair_tiles(const DecodeParams& p, int b) {
+    const int len = __ldg(p.cache_len + b);
+    if (len < p.s_active || (!p.circular && len > p.max_cache_len)) return 0;
+    const int first = decode_first_slot(len, p.s_active, p.window, p.circular, kDecodeTile);
+    return (decode_nslots(len, p.circular, p.max_cache_len) - first + kDecodeTile - 1) /
+           kDecodeTile;
+}
+
+// True in every consumer thread when pred holds in any of them (a barrier of the consumer
+// warps with an OR reduction: they all take the same branch after it).
+__device__ __forceinline__ bool consumers_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(kConsumers * 32)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+}
+
+// One piece: the tiles of one (sequence, kv head) pair that a CTA reads, handed from the
+// producer to the consumers with the piece's Q fragments.
+struct PieceInfo {
+    int b, g, len, nslots, first;  // sequence, kv head, cache length, slots [first, nslots)
+    int t_off;  // the pair's tile index of the piece's first tile
+    int npc;    // tiles in the piece; 0 ends the CTA's work
+    int i0;     // ring index of the piece's first tile
+    int k;      // the piece's index within its pair: its partial slot
+    float c_row[16];  // softmax scale of each row (log2 units)
+};
+
 // kE4M3: the cache holds e4m3 bytes.  k_scale is folded into p.c and v_scale applied to the
-// chunk's output, so the products run on the exact e4m3 values, converted to f16 (one
+// piece's output, so the products run on the exact e4m3 values, converted to f16 (one
 // instruction per pair): Q.K^T with Q in f16 and P.V with P in f16.  Each Q row is scaled by
 // a power of two that puts its largest |element| in [2^13, 2^14) before it is rounded to
 // f16 (the factor comes back out of the row's softmax scale), so the f16 row holds every
 // bf16 element exactly unless it is below 2^-27 of the row's largest.
+//
+// Work split: the KV tiles of all (sequence, kv head) pairs, sequence-major, form one
+// stream of NT tiles; CTA c of the grid takes tiles [c tpc, (c + 1) tpc) with
+// tpc = max(ceil(NT / gridDim.x), min_tiles).  The grid is one wave (the CTAs the SMs hold),
+// so every CTA streams the same number of bytes and pays its start-up once.  The run of a
+// CTA is cut into pieces at pair boundaries; each piece keeps its own (m, l, O) and writes
+// one partial.  A pair of n tiles meets at most ceil(n / min_tiles) + 1 CTAs, which bounds
+// the partial slots a pair needs.
 template <int D, bool kE4M3>
 __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) decode_split_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -211,33 +250,34 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
     using L = DecodeLayout<D, kE4M3>;
     constexpr int kStages = L::kStages;
     constexpr int kBT = L::kBT;
+    constexpr int kQWords = (D / 16) * 32;  // uint4 words of one Q slot
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* pipe = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+    uint4* const qslots = reinterpret_cast<uint4*>(pipe + L::kPipe);  // [2][kQWords]
+    __shared__ uint64_t full_bar[kStages], empty_bar[kStages], q_full[2], q_empty[2];
+    __shared__ PieceInfo info[2];
     __shared__ float m_sh[kConsumers][16], l_sh[kConsumers][16];
     __shared__ int abort_flag;
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // The merge kernel is launched as this grid's programmatic dependent: it may take free
+    // slots once every CTA here has started (or exited), and waits for this grid to finish
+    // before it reads a partial.
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int len = p.cache_len[b];
-    if (len < p.s_active || (!p.circular && len > p.max_cache_len)) {
-        if (threadIdx.x == 0 && split == 0 && g == 0) atomicOr(&g_decode_error, kDevErrCacheLen);
-        return;
-    }
-    // this split covers cache slots [tok0, tok1); the combine skips the splits that return here
-    const int nslots = decode_nslots(len, p.circular, p.max_cache_len);
-    const int first = decode_first_slot(len, p.s_active, p.window, p.circular, kBT);
-    if (split >= decode_nsplits(nslots, first, p.chunk)) return;  // a split this sequence lacks
-    int tok0, tok1;
-    decode_split_range(nslots, first, p.chunk, kBT, split, tok0, tok1);
-    if (tok0 >= tok1) return;  // an empty last split
-    const int nblocks = (tok1 - tok0 + kBT - 1) / kBT;
+    const int gq = lane >> 2, qd = lane & 3;
+    const int r0 = gq, r1 = gq + 8;
+    const bool v0 = r0 < p.rows, v1 = r1 < p.rows;
+    const int t0 = r0 % p.s_active, t1 = r1 % p.s_active;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], kConsumers);
         }
         abort_flag = 0;
         fence_mbar_init();
@@ -254,63 +294,272 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
         const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;
         int issued = 0;
         bool ok = true;
-        // The rows of 32 tiles are found at once, one tile per lane (a paged cache costs a
-        // dependent block-table load per tile, which one thread would pay tile after tile);
-        // lane 0 then issues the tiles in order.
-        for (int i0 = 0; ok && i0 < nblocks; i0 += 32) {
-            int rl[kBT / 16];  // lane's tile i0 + lane: cache row of each box, -1 = not read
+
+        // Tiles [x0, x1) of a piece of pair (b, g) whose first tile is the pair's tile
+        // t_off, at ring index i0 + x.  The rows of 32 tiles are found at once, one tile per
+        // lane (a paged cache costs a dependent block-table load per tile, which one thread
+        // would pay tile after tile); lane 0 then issues the tiles in order.
+        auto issue = [&](int b, int g, int first, int nslots, int t_off, int i0, int x0,
+                         int x1) {
+            for (int xb = x0; ok && xb < x1; xb += 32) {
+                int rl[kBT / 16];  // lane's tile xb + lane: cache row of each box, -1 = not read
 #pragma unroll
-            for (int bx = 0; bx < kBT / 16; ++bx) {
-                rl[bx] = -1;
-                const int jb = tok0 + (i0 + lane) * kBT + bx * p.box_rows;
-                // a box wholly past the cache end is not read
-                if (bx >= nbox || i0 + lane >= nblocks || jb >= nslots) continue;
-                if (p.paged) {
-                    const uint32_t pg = __ldg(p.table + (size_t)b * p.max_pages + jb / p.page_size);
-                    if (pg >= (uint32_t)p.num_pages) {
-                        atomicOr(&g_decode_error, kDevErrPageOOB);
-                        continue;  // never dereference an out-of-range page
-                    }
-                    rl[bx] = (int)(((long long)pg * p.hkv + g) * p.page_size + jb % p.page_size);
-                } else {
-                    rl[bx] = (int)(((long long)b * p.hkv + g) * p.max_cache_len + jb);
-                }
-            }
-            const int n = min(32, nblocks - i0);
-            for (int t = 0; t < n; ++t) {
-                int rows[kBT / 16];
-#pragma unroll
-                for (int bx = 0; bx < kBT / 16; ++bx) rows[bx] = __shfl_sync(0xffffffffu, rl[bx], t);
-                if (lane == 0) {
-                    const int i = i0 + t;
-                    const int s = i % kStages;
-                    if (i >= kStages && !mbar_wait(&empty_bar[s], ((i / kStages) - 1) & 1, &abort_flag)) {
-                        ok = false;
-                    } else {
-                        uint32_t bytes = 0;
-#pragma unroll
-                        for (int bx = 0; bx < kBT / 16; ++bx)
-                            if (bx < nbox && rows[bx] >= 0) bytes += 2u * (uint32_t)L::kBoxes * box_bytes;
-                        uint8_t* kdst = pipe + s * L::kSlot;
-                        uint8_t* vdst = kdst + L::kHalf;
-                        mbar_arrive_expect_tx(&full_bar[s], bytes);
-#pragma unroll
-                        for (int bx = 0; bx < kBT / 16; ++bx) {
-                            if (bx >= nbox || rows[bx] < 0) continue;
-#pragma unroll
-                            for (int dc = 0; dc < L::kBoxes; ++dc) {
-                                tma_load_2d(kdst + dc * L::kBoxBytes + bx * box_bytes, &tm_k,
-                                            dc * L::kBoxElems, rows[bx], &full_bar[s]);
-                                tma_load_2d(vdst + dc * L::kBoxBytes + bx * box_bytes, &tm_v,
-                                            dc * L::kBoxElems, rows[bx], &full_bar[s]);
-                            }
+                for (int bx = 0; bx < kBT / 16; ++bx) {
+                    rl[bx] = -1;
+                    const int jb = first + (t_off + xb + lane) * kBT + bx * p.box_rows;
+                    // a box wholly past the cache end is not read
+                    if (bx >= nbox || xb + lane >= x1 || jb >= nslots) continue;
+                    if (p.paged) {
+                        const uint32_t pg =
+                            __ldg(p.table + (size_t)b * p.max_pages + jb / p.page_size);
+                        if (pg >= (uint32_t)p.num_pages) {
+                            atomicOr(&g_decode_error, kDevErrPageOOB);
+                            continue;  // never dereference an out-of-range page
                         }
-                        issued = i + 1;
+                        rl[bx] = (int)(((long long)pg * p.hkv + g) * p.page_size + jb % p.page_size);
+                    } else {
+                        rl[bx] = (int)(((long long)b * p.hkv + g) * p.max_cache_len + jb);
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                const int n = min(32, x1 - xb);
+                for (int t = 0; t < n; ++t) {
+                    int rows[kBT / 16];
+#pragma unroll
+                    for (int bx = 0; bx < kBT / 16; ++bx) rows[bx] = __shfl_sync(0xffffffffu, rl[bx], t);
+                    if (lane == 0) {
+                        const int i = i0 + xb + t;
+                        const int s = i % kStages;
+                        if (i >= kStages &&
+                            !mbar_wait(&empty_bar[s], ((i / kStages) - 1) & 1, &abort_flag)) {
+                            ok = false;
+                        } else {
+                            uint32_t bytes = 0;
+#pragma unroll
+                            for (int bx = 0; bx < kBT / 16; ++bx)
+                                if (bx < nbox && rows[bx] >= 0) bytes += 2u * (uint32_t)L::kBoxes * box_bytes;
+                            uint8_t* kdst = pipe + s * L::kSlot;
+                            uint8_t* vdst = kdst + L::kHalf;
+                            mbar_arrive_expect_tx(&full_bar[s], bytes);
+#pragma unroll
+                            for (int bx = 0; bx < kBT / 16; ++bx) {
+                                if (bx >= nbox || rows[bx] < 0) continue;
+#pragma unroll
+                                for (int dc = 0; dc < L::kBoxes; ++dc) {
+                                    tma_load_2d(kdst + dc * L::kBoxBytes + bx * box_bytes, &tm_k,
+                                                dc * L::kBoxElems, rows[bx], &full_bar[s]);
+                                    tma_load_2d(vdst + dc * L::kBoxBytes + bx * box_bytes, &tm_v,
+                                                dc * L::kBoxElems, rows[bx], &full_bar[s]);
+                                }
+                            }
+                            issued = i + 1;
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                }
             }
+        };
+
+        // Q slot j % 2 may be refilled once the consumers have merged piece j - 2.
+        auto q_slot_free = [&](int j) {
+            if (j < 2) return;
+            bool w = true;
+            if (lane == 0) w = mbar_wait(&q_empty[j & 1], ((j >> 1) - 1) & 1, &abort_flag);
+            ok = ok && __shfl_sync(0xffffffffu, w, 0);
+        };
+
+        // The Q fragments of pair (b, g) in the consumers' lane layout (16 bytes per lane and
+        // k-step), and each row's softmax scale.
+        auto prep_q = [&](int b, int g, int len, uint4* qs, float* c_row) {
+            const int qpos0 = len - p.s_active + t0, qpos1 = len - p.s_active + t1;  // RoPE positions
+            const __nv_bfloat16* q0 = nullptr;
+            const __nv_bfloat16* q1 = nullptr;
+            if (v0) q0 = p.q + ((size_t)(b * p.hq + g * p.group + r0 / p.s_active) * p.s_active + t0) * D;
+            if (v1) q1 = p.q + ((size_t)(b * p.hq + g * p.group + r1 / p.s_active) * p.s_active + t1) * D;
+            uint32_t qf[D / 16][4];
+            float c_row0 = p.c, c_row1 = p.c;
+            if constexpr (kE4M3) {
+                // The k index of k-step ks maps 2qd, 2qd+1 to head dims 16 ks + 4 qd + {0, 1} and
+                // 2qd+8, 2qd+9 to 16 ks + 4 qd + {2, 3} (a dot product does not depend on the
+                // order of its terms): one 32-bit shared load then gives a lane the four K bytes
+                // of its k-step.
+                uint2 qa[D / 16], qb[D / 16];
+                float mx_a = 0.f, mx_b = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int c = ks * 16 + 4 * qd;
+                    qa[ks] = v0 ? __ldg(reinterpret_cast<const uint2*>(q0 + c)) : make_uint2(0u, 0u);
+                    qb[ks] = v1 ? __ldg(reinterpret_cast<const uint2*>(q1 + c)) : make_uint2(0u, 0u);
+                }
+                if (p.rope_inv_freq != nullptr) {  // element i of k-step ks pairs with k-step ks + D/32
+#pragma unroll
+                    for (int ks = 0; ks < D / 32; ++ks) {
+                        const int c = ks * 16 + 4 * qd;
+                        rope_rows(qa[ks].x, qa[ks + D / 32].x, qb[ks].x, qb[ks + D / 32].x, c, qpos0,
+                                  qpos1, p.rope_inv_freq);
+                        rope_rows(qa[ks].y, qa[ks + D / 32].y, qb[ks].y, qb[ks + D / 32].y, c + 2,
+                                  qpos0, qpos1, p.rope_inv_freq);
+                    }
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t wa[2] = {qa[ks].x, qa[ks].y}, wb[2] = {qb[ks].x, qb[ks].y};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint32_t ba = (h & 1) ? (wa[h >> 1] & 0xffff0000u) : (wa[h >> 1] << 16);
+                        const uint32_t bb = (h & 1) ? (wb[h >> 1] & 0xffff0000u) : (wb[h >> 1] << 16);
+                        mx_a = fmaxf(mx_a, fabsf(__uint_as_float(ba)));
+                        mx_b = fmaxf(mx_b, fabsf(__uint_as_float(bb)));
+                    }
+                }
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+                // power-of-two row factors 2^sa, 2^sb: the largest |q| lands in [2^13, 2^14)
+                int ea = 0, eb = 0;
+                if (mx_a > 0.f) frexpf(mx_a, &ea);  // mx in [2^(ea-1), 2^ea)
+                if (mx_b > 0.f) frexpf(mx_b, &eb);
+                const int sa = mx_a > 0.f ? 14 - ea : 0, sb = mx_b > 0.f ? 14 - eb : 0;
+                c_row0 = ldexpf(p.c, -sa);
+                c_row1 = ldexpf(p.c, -sb);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t wa[2] = {qa[ks].x, qa[ks].y}, wb[2] = {qb[ks].x, qb[ks].y};
+                    uint32_t fa[2], fb[2];
+#pragma unroll
+                    for (int w2 = 0; w2 < 2; ++w2) {
+                        fa[w2] = pack_f16(ldexpf(__uint_as_float(wa[w2] << 16), sa),
+                                          ldexpf(__uint_as_float(wa[w2] & 0xffff0000u), sa));
+                        fb[w2] = pack_f16(ldexpf(__uint_as_float(wb[w2] << 16), sb),
+                                          ldexpf(__uint_as_float(wb[w2] & 0xffff0000u), sb));
+                    }
+                    qf[ks][0] = fa[0];
+                    qf[ks][2] = fa[1];
+                    qf[ks][1] = fb[0];
+                    qf[ks][3] = fb[1];
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int c = ks * 16 + 2 * qd;
+                    qf[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c)) : 0u;
+                    qf[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c)) : 0u;
+                    qf[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c + 8)) : 0u;
+                    qf[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c + 8)) : 0u;
+                }
+                if (p.rope_inv_freq != nullptr) {  // element i of k-step ks pairs with k-step ks + D/32
+#pragma unroll
+                    for (int ks = 0; ks < D / 32; ++ks) {
+                        const int c = ks * 16 + 2 * qd;
+                        rope_rows(qf[ks][0], qf[ks + D / 32][0], qf[ks][1], qf[ks + D / 32][1], c,
+                                  qpos0, qpos1, p.rope_inv_freq);
+                        rope_rows(qf[ks][2], qf[ks + D / 32][2], qf[ks][3], qf[ks + D / 32][3], c + 8,
+                                  qpos0, qpos1, p.rope_inv_freq);
+                    }
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                qs[ks * 32 + lane] = make_uint4(qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+            if (qd == 0) {
+                c_row[r0] = c_row0;
+                c_row[r1] = c_row1;
+            }
+        };
+
+        // NT, the tiles of every pair, and this CTA's run [lo, hi) of them
+        long long cnt = 0;
+        for (int bb = lane; bb < p.b; bb += 32) cnt += pair_tiles(p, bb);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        const long long nt_all = cnt * p.hkv;
+        const long long tpc =
+            max((nt_all + gridDim.x - 1) / (long long)gridDim.x, (long long)p.min_tiles);
+        const long long lo = (long long)blockIdx.x * tpc;
+        const long long hi = min(nt_all, lo + tpc);
+        int j = 0;  // pieces handed to the consumers
+        if (lo < hi) {
+            // the sequence holding tile lo: 32 sequences at a time, by a prefix sum over lanes
+            int bcur = -1;
+            long long bstart = 0, base = 0;
+            for (int bb0 = 0; bb0 < p.b; bb0 += 32) {
+                const int bb = bb0 + lane;
+                const long long t = bb < p.b ? (long long)pair_tiles(p, bb) * p.hkv : 0;
+                long long incl = t;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const long long excl = incl - t;
+                const unsigned hit =
+                    __ballot_sync(0xffffffffu, t > 0 && lo >= base + excl && lo < base + incl);
+                if (hit != 0u) {
+                    const int l0 = __ffs(hit) - 1;
+                    bcur = bb0 + l0;
+                    bstart = base + __shfl_sync(0xffffffffu, excl, l0);
+                    break;
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            int nt_b = bcur >= 0 ? pair_tiles(p, bcur) : 0;
+            if (nt_b <= 0) ok = false;  // cannot happen: lo < NT lies in some sequence
+            int gcur = ok ? (int)((lo - bstart) / nt_b) : 0;
+            int t_off = ok ? (int)((lo - bstart) % nt_b) : 0;
+            long long pstart = bstart + (long long)gcur * nt_b;  // stream index of the pair's first tile
+            int i = 0;  // ring index of the next tile
+            const int total = (int)(hi - lo);
+            while (ok && i < total) {
+                const int npc = min(nt_b - t_off, total - i);
+                const int k = (int)(blockIdx.x - pstart / tpc);
+                const int len = __ldg(p.cache_len + bcur);
+                const int nslots = decode_nslots(len, p.circular, p.max_cache_len);
+                const int first = decode_first_slot(len, p.s_active, p.window, p.circular, kBT);
+                // The first piece's tiles start loading before its Q is prepared; later
+                // pieces are prepared while the ring still holds the previous piece.
+                const int pre = (j == 0) ? min(npc, kStages) : 0;
+                issue(bcur, gcur, first, nslots, t_off, i, 0, pre);
+                q_slot_free(j);
+                if (!ok) break;
+                PieceInfo& pi = info[j & 1];
+                prep_q(bcur, gcur, len, qslots + (j & 1) * kQWords, pi.c_row);
+                if (lane == 0) {
+                    pi.b = bcur;
+                    pi.g = gcur;
+                    pi.len = len;
+                    pi.nslots = nslots;
+                    pi.first = first;
+                    pi.t_off = t_off;
+                    pi.npc = npc;
+                    pi.i0 = i;
+                    pi.k = k;
+                    // the CTA that reads a pair's last tile records how many pieces it has
+                    if (t_off + npc == nt_b) p.npieces[(size_t)bcur * p.hkv + gcur] = k + 1;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[j & 1]);
+                issue(bcur, gcur, first, nslots, t_off, i, pre, npc);
+                i += npc;
+                ++j;
+                t_off = 0;  // the next pair
+                pstart += nt_b;
+                if (++gcur == p.hkv) {
+                    gcur = 0;
+                    nt_b = 0;
+                    while (nt_b == 0 && ++bcur < p.b) nt_b = pair_tiles(p, bcur);
+                    if (nt_b == 0 && i < total) ok = false;  // cannot happen: tiles remain
+                }
+            }
+        }
+        // the end of this CTA's work
+        if (ok) q_slot_free(j);
+        if (ok) {
+            if (lane == 0) info[j & 1].npc = 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_full[j & 1]);
+        } else if (lane == 0) {
+            abort_flag = 1;  // the consumers stop at their next wait
         }
         if (lane == 0 && abort_flag) {  // let copies already in flight land before the CTA exits
             for (int i = max(0, issued - kStages); i < issued; ++i)
@@ -319,407 +568,367 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
         }
     } else {
         // -------------------------------------------------------------- consumers
-        const int gq = lane >> 2, qd = lane & 3;
-        const int r0 = gq, r1 = gq + 8;
-        const bool v0 = r0 < p.rows, v1 = r1 < p.rows;
-        const int t0 = r0 % p.s_active, t1 = r1 % p.s_active;
-        const int qpos0 = len - p.s_active + t0, qpos1 = len - p.s_active + t1;  // RoPE positions
-        const __nv_bfloat16* q0 = nullptr;
-        const __nv_bfloat16* q1 = nullptr;
-        if (v0) q0 = p.q + ((size_t)(b * p.hq + g * p.group + r0 / p.s_active) * p.s_active + t0) * D;
-        if (v1) q1 = p.q + ((size_t)(b * p.hq + g * p.group + r1 / p.s_active) * p.s_active + t1) * D;
-        uint32_t qf[D / 16][4];
-        float c_row0 = p.c, c_row1 = p.c;  // softmax scale of rows r0, r1 (log2 units)
-        if constexpr (kE4M3) {
-            // The k index of k-step ks maps 2qd, 2qd+1 to head dims 16 ks + 4 qd + {0, 1} and
-            // 2qd+8, 2qd+9 to 16 ks + 4 qd + {2, 3} (a dot product does not depend on the
-            // order of its terms): one 32-bit shared load then gives a lane the four K bytes
-            // of its k-step.
-            uint2 qa[D / 16], qb[D / 16];
-            float mx_a = 0.f, mx_b = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const int c = ks * 16 + 4 * qd;
-                qa[ks] = v0 ? __ldg(reinterpret_cast<const uint2*>(q0 + c)) : make_uint2(0u, 0u);
-                qb[ks] = v1 ? __ldg(reinterpret_cast<const uint2*>(q1 + c)) : make_uint2(0u, 0u);
-            }
-            if (p.rope_inv_freq != nullptr) {  // element i of k-step ks pairs with k-step ks + D/32
-#pragma unroll
-                for (int ks = 0; ks < D / 32; ++ks) {
-                    const int c = ks * 16 + 4 * qd;
-                    rope_rows(qa[ks].x, qa[ks + D / 32].x, qb[ks].x, qb[ks + D / 32].x, c, qpos0,
-                              qpos1, p.rope_inv_freq);
-                    rope_rows(qa[ks].y, qa[ks + D / 32].y, qb[ks].y, qb[ks + D / 32].y, c + 2,
-                              qpos0, qpos1, p.rope_inv_freq);
-                }
-            }
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t wa[2] = {qa[ks].x, qa[ks].y}, wb[2] = {qb[ks].x, qb[ks].y};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint32_t ba = (h & 1) ? (wa[h >> 1] & 0xffff0000u) : (wa[h >> 1] << 16);
-                    const uint32_t bb = (h & 1) ? (wb[h >> 1] & 0xffff0000u) : (wb[h >> 1] << 16);
-                    mx_a = fmaxf(mx_a, fabsf(__uint_as_float(ba)));
-                    mx_b = fmaxf(mx_b, fabsf(__uint_as_float(bb)));
-                }
-            }
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-            // power-of-two row factors 2^sa, 2^sb: the largest |q| lands in [2^13, 2^14)
-            int ea = 0, eb = 0;
-            if (mx_a > 0.f) frexpf(mx_a, &ea);  // mx in [2^(ea-1), 2^ea)
-            if (mx_b > 0.f) frexpf(mx_b, &eb);
-            const int sa = mx_a > 0.f ? 14 - ea : 0, sb = mx_b > 0.f ? 14 - eb : 0;
-            c_row0 = ldexpf(p.c, -sa);
-            c_row1 = ldexpf(p.c, -sb);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t wa[2] = {qa[ks].x, qa[ks].y}, wb[2] = {qb[ks].x, qb[ks].y};
-                uint32_t fa[2], fb[2];
-#pragma unroll
-                for (int w2 = 0; w2 < 2; ++w2) {
-                    fa[w2] = pack_f16(ldexpf(__uint_as_float(wa[w2] << 16), sa),
-                                      ldexpf(__uint_as_float(wa[w2] & 0xffff0000u), sa));
-                    fb[w2] = pack_f16(ldexpf(__uint_as_float(wb[w2] << 16), sb),
-                                      ldexpf(__uint_as_float(wb[w2] & 0xffff0000u), sb));
-                }
-                qf[ks][0] = fa[0];
-                qf[ks][2] = fa[1];
-                qf[ks][1] = fb[0];
-                qf[ks][3] = fb[1];
-            }
-        } else {
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const int c = ks * 16 + 2 * qd;
-                qf[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c)) : 0u;
-                qf[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c)) : 0u;
-                qf[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + c + 8)) : 0u;
-                qf[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + c + 8)) : 0u;
-            }
-            if (p.rope_inv_freq != nullptr) {  // element i of k-step ks pairs with k-step ks + D/32
-#pragma unroll
-                for (int ks = 0; ks < D / 32; ++ks) {
-                    const int c = ks * 16 + 2 * qd;
-                    rope_rows(qf[ks][0], qf[ks + D / 32][0], qf[ks][1], qf[ks + D / 32][1], c,
-                              qpos0, qpos1, p.rope_inv_freq);
-                    rope_rows(qf[ks][2], qf[ks + D / 32][2], qf[ks][3], qf[ks + D / 32][3], c + 8,
-                              qpos0, qpos1, p.rope_inv_freq);
-                }
-            }
-        }
-        // the Q fragments go to shared memory (written once, by warp 0) and are read back per
-        // k-step, one 16-byte load per lane
-        uint4* const qs = reinterpret_cast<uint4*>(pipe + L::kPipe);
-        if constexpr (L::kQInSmem) {
-            if (warp == 0) {
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    qs[ks * 32 + lane] = make_uint4(qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-        }
-        auto qfrag = [&](int ks, uint32_t* f) {
-            if constexpr (L::kQInSmem) {
+        constexpr int kNT = kBT / 8;  // 8-token n-tiles of S per tile
+        for (int j = 0;; ++j) {
+            const int qsl = j & 1;
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&q_full[qsl], (j >> 1) & 1, &abort_flag));
+            if (consumers_any(!got || abort_flag != 0)) break;
+            const PieceInfo& pi = info[qsl];
+            const int npc = pi.npc;
+            if (npc == 0) break;  // the same value in every consumer warp
+            const int b = pi.b, g = pi.g, len = pi.len, nslots = pi.nslots, first = pi.first;
+            const int t_off = pi.t_off, i0 = pi.i0, k = pi.k;
+            const float c_row0 = pi.c_row[r0], c_row1 = pi.c_row[r1];
+            const uint4* const qs = qslots + qsl * kQWords;
+            auto qfrag = [&](int ks, uint32_t* f) {
                 const uint4 x = qs[ks * 32 + lane];
                 f[0] = x.x;
                 f[1] = x.y;
                 f[2] = x.z;
                 f[3] = x.w;
-            } else {
+            };
+            float o[D / 8][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) f[e] = qf[ks][e];
-            }
-        };
-        float o[D / 8][4];
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-        constexpr int kNT = kBT / 8;  // 8-token n-tiles of S per tile
+            for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-        for (int i = warp; i < nblocks; i += kConsumers) {
-            const int s = i % kStages;
-            if (!mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_flag)) break;
-            const uint32_t kbase = smem_u32(pipe + s * L::kSlot);
-            const uint32_t vbase = kbase + L::kHalf;
-            // S = Q K^T for 16 rows x kBT tokens
-            float sc[kNT][4];
+            // this warp's tiles of the piece: ring indices i = warp (mod kConsumers)
+            for (int i = i0 + (warp - i0 % kConsumers + kConsumers) % kConsumers; i < i0 + npc;
+                 i += kConsumers) {
+                const int s = i % kStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_flag)))
+                    break;
+                const uint32_t kbase = smem_u32(pipe + s * L::kSlot);
+                const uint32_t vbase = kbase + L::kHalf;
+                // S = Q K^T for 16 rows x kBT tokens
+                float sc[kNT][4];
 #pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-            if constexpr (kE4M3) {
-                // token nt*8 + gq, head dims 16 ks + 4 qd .. +3 (chunk ks of its 128-byte row)
-                const uint8_t* kt = pipe + s * L::kSlot;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    uint32_t qk[4];
-                    qfrag(ks, qk);
-#pragma unroll
-                    for (int nt = 0; nt < kNT; ++nt) {
-                        const int tok = nt * 8 + gq;
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(
-                            kt + (ks >> 3) * L::kBoxBytes + sw128_off(tok, ks & 7) + 4 * qd);
-                        mma_f16_16816(sc[nt], qk, e4m3x2_to_f16x2(w & 0xffffu),
-                                      e4m3x2_to_f16x2(w >> 16));
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int kp = 0; kp < D / 32; ++kp) {
-                    uint32_t qa[4], qb[4];
-                    qfrag(2 * kp, qa);
-                    qfrag(2 * kp + 1, qb);
-#pragma unroll
-                    for (int nt = 0; nt < kNT; ++nt) {
-                        const uint32_t tok = nt * 8 + (lane & 7);
-                        const uint32_t cg = 4 * kp + (lane >> 3);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
-                        mma_bf16_16816(sc[nt], qa, b0, b1);
-                        mma_bf16_16816(sc[nt], qb, b2, b3);
-                    }
-                }
-            }
-            const int j0 = tok0 + i * kBT;  // first slot of the tile
-            // tiles that touch the new tokens, the cache end or a window start are masked;
-            // every tile of a circular cache is (its slots hold positions of two laps)
-            const bool edge = p.circular || j0 + kBT > len - p.s_active ||
-                              (p.window > 0 && j0 < len - p.window);
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float x0 = sc[nt][e] * c_row0, x1 = sc[nt][2 + e] * c_row1;
-                    if (edge) {
-                        const int r = j0 + nt * 8 + 2 * qd + e;  // slot
-                        const int j = p.circular ? circular_pos(r, len, p.max_cache_len) : r;
-                        const bool in = r < nslots;
-                        if (!(v0 && in && decode_allowed_w(j, len, p.s_active, t0, p.window))) x0 = -INFINITY;
-                        if (!(v1 && in && decode_allowed_w(j, len, p.s_active, t1, p.window))) x1 = -INFINITY;
-                    }
-                    sc[nt][e] = x0;
-                    sc[nt][2 + e] = x1;
-                    mx0 = fmaxf(mx0, x0);
-                    mx1 = fmaxf(mx1, x1);
-                }
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-            // a row with nothing allowed yet keeps exponent base 0: exp2(-inf - 0) = 0
-            const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float a0 = ex2(m_run[0] - mu0), a1 = ex2(m_run[1] - mu1);
-            m_run[0] = mn0;
-            m_run[1] = mn1;
-            l_run[0] *= a0;
-            l_run[1] *= a1;
-#pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                o[n][0] *= a0;
-                o[n][1] *= a0;
-                o[n][2] *= a1;
-                o[n][3] *= a1;
-            }
-#pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) {
-                sc[nt][0] = ex2(sc[nt][0] - mu0);
-                sc[nt][1] = ex2(sc[nt][1] - mu0);
-                sc[nt][2] = ex2(sc[nt][2] - mu1);
-                sc[nt][3] = ex2(sc[nt][3] - mu1);
-                l_run[0] += sc[nt][0] + sc[nt][1];
-                l_run[1] += sc[nt][2] + sc[nt][3];
-            }
-            // O += P V (P from the score accumulators)
-#pragma unroll
-            for (int ks = 0; ks < kBT / 16; ++ks) {
-                uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
-                if (edge) {  // zero V rows of slots past the cache end (they may hold NaN)
-                    const int jl = j0 + ks * 16 + 2 * qd;
-                    keep_lo = (jl < nslots ? 0x0000ffffu : 0u) | (jl + 1 < nslots ? 0xffff0000u : 0u);
-                    keep_hi = (jl + 8 < nslots ? 0x0000ffffu : 0u) | (jl + 9 < nslots ? 0xffff0000u : 0u);
-                }
-                uint32_t pa[4];
+                for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
                 if constexpr (kE4M3) {
-                    // P in f16, V converted to f16.  The n index of n-tile np maps n to head
-                    // dim (D/8) n + np, so a lane (n = gq) reads D/8 consecutive bytes of each
-                    // of its four tokens (k = 2qd, 2qd+1, 2qd+8, 2qd+9) and pairs them bytewise.
-                    pa[0] = pack_f16(sc[2 * ks][0], sc[2 * ks][1]);
-                    pa[1] = pack_f16(sc[2 * ks][2], sc[2 * ks][3]);
-                    pa[2] = pack_f16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-                    pa[3] = pack_f16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
-                    constexpr int kW = D / 32;  // 32-bit words of a lane's bytes per token
-                    const uint8_t* vt = pipe + s * L::kSlot + L::kHalf;
-                    const int ta = ks * 16 + 2 * qd;
-                    uint32_t vw[4][kW];
+                    // token nt*8 + gq, head dims 16 ks + 4 qd .. +3 (chunk ks of its 128-byte row)
+                    const uint8_t* kt = pipe + s * L::kSlot;
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int tok = ta + (r & 1) + (r >> 1) * 8;
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        uint32_t qk[4];
+                        qfrag(ks, qk);
 #pragma unroll
-                        for (int c = 0; c < kW / 4; ++c) {
-                            const int ch = (D / 128) * gq + c;  // 16-byte chunk along the row
-                            const uint4 x = *reinterpret_cast<const uint4*>(
-                                vt + (ch >> 3) * L::kBoxBytes + sw128_off(tok, ch & 7));
-                            vw[r][4 * c] = x.x;
-                            vw[r][4 * c + 1] = x.y;
-                            vw[r][4 * c + 2] = x.z;
-                            vw[r][4 * c + 3] = x.w;
+                        for (int nt = 0; nt < kNT; ++nt) {
+                            const int tok = nt * 8 + gq;
+                            const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                                kt + (ks >> 3) * L::kBoxBytes + sw128_off(tok, ks & 7) + 4 * qd);
+                            mma_f16_16816(sc[nt], qk, e4m3x2_to_f16x2(w & 0xffffu),
+                                          e4m3x2_to_f16x2(w >> 16));
                         }
                     }
-                    // the keep masks only bite on edge tiles (the choice is per tile, so
-                    // warp-uniform): other tiles skip the 64 ANDs
-                    auto pv = [&](auto masked) {
+                } else {
 #pragma unroll
-                        for (int wd = 0; wd < kW; ++wd) {
-                            const uint32_t ab0 = __byte_perm(vw[0][wd], vw[1][wd], 0x5140);
-                            const uint32_t ab1 = __byte_perm(vw[0][wd], vw[1][wd], 0x7362);
-                            const uint32_t cd0 = __byte_perm(vw[2][wd], vw[3][wd], 0x5140);
-                            const uint32_t cd1 = __byte_perm(vw[2][wd], vw[3][wd], 0x7362);
-                            const uint32_t pairs[4][2] = {{ab0 & 0xffffu, cd0 & 0xffffu},
-                                                          {ab0 >> 16, cd0 >> 16},
-                                                          {ab1 & 0xffffu, cd1 & 0xffffu},
-                                                          {ab1 >> 16, cd1 >> 16}};
+                    for (int kp = 0; kp < D / 32; ++kp) {
+                        uint32_t qa[4], qb[4];
+                        qfrag(2 * kp, qa);
+                        qfrag(2 * kp + 1, qb);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                uint32_t b0 = e4m3x2_to_f16x2(pairs[e][0]);
-                                uint32_t b1 = e4m3x2_to_f16x2(pairs[e][1]);
-                                if constexpr (decltype(masked)::value) {
-                                    b0 &= keep_lo;
-                                    b1 &= keep_hi;
-                                }
-                                mma_f16_16816(o[4 * wd + e], pa, b0, b1);
+                        for (int nt = 0; nt < kNT; ++nt) {
+                            const uint32_t tok = nt * 8 + (lane & 7);
+                            const uint32_t cg = 4 * kp + (lane >> 3);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(kbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
+                            mma_bf16_16816(sc[nt], qa, b0, b1);
+                            mma_bf16_16816(sc[nt], qb, b2, b3);
+                        }
+                    }
+                }
+                const int j0 = first + (t_off + (i - i0)) * kBT;  // first slot of the tile
+                // tiles that touch the new tokens, the cache end or a window start are masked;
+                // every tile of a circular cache is (its slots hold positions of two laps)
+                const bool edge = p.circular || j0 + kBT > len - p.s_active ||
+                                  (p.window > 0 && j0 < len - p.window);
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float x0 = sc[nt][e] * c_row0, x1 = sc[nt][2 + e] * c_row1;
+                        if (edge) {
+                            const int r = j0 + nt * 8 + 2 * qd + e;  // slot
+                            const int j = p.circular ? circular_pos(r, len, p.max_cache_len) : r;
+                            const bool in = r < nslots;
+                            if (!(v0 && in && decode_allowed_w(j, len, p.s_active, t0, p.window))) x0 = -INFINITY;
+                            if (!(v1 && in && decode_allowed_w(j, len, p.s_active, t1, p.window))) x1 = -INFINITY;
+                        }
+                        sc[nt][e] = x0;
+                        sc[nt][2 + e] = x1;
+                        mx0 = fmaxf(mx0, x0);
+                        mx1 = fmaxf(mx1, x1);
+                    }
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                // a row with nothing allowed yet keeps exponent base 0: exp2(-inf - 0) = 0
+                const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                const float a0 = ex2(m_run[0] - mu0), a1 = ex2(m_run[1] - mu1);
+                m_run[0] = mn0;
+                m_run[1] = mn1;
+                l_run[0] *= a0;
+                l_run[1] *= a1;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
+                }
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt) {
+                    sc[nt][0] = ex2(sc[nt][0] - mu0);
+                    sc[nt][1] = ex2(sc[nt][1] - mu0);
+                    sc[nt][2] = ex2(sc[nt][2] - mu1);
+                    sc[nt][3] = ex2(sc[nt][3] - mu1);
+                    l_run[0] += sc[nt][0] + sc[nt][1];
+                    l_run[1] += sc[nt][2] + sc[nt][3];
+                }
+                // O += P V (P from the score accumulators)
+#pragma unroll
+                for (int ks = 0; ks < kBT / 16; ++ks) {
+                    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+                    if (edge) {  // zero V rows of slots past the cache end (they may hold NaN)
+                        const int jl = j0 + ks * 16 + 2 * qd;
+                        keep_lo = (jl < nslots ? 0x0000ffffu : 0u) | (jl + 1 < nslots ? 0xffff0000u : 0u);
+                        keep_hi = (jl + 8 < nslots ? 0x0000ffffu : 0u) | (jl + 9 < nslots ? 0xffff0000u : 0u);
+                    }
+                    uint32_t pa[4];
+                    if constexpr (kE4M3) {
+                        // P in f16, V converted to f16.  The n index of n-tile np maps n to head
+                        // dim (D/8) n + np, so a lane (n = gq) reads D/8 consecutive bytes of each
+                        // of its four tokens (k = 2qd, 2qd+1, 2qd+8, 2qd+9) and pairs them bytewise.
+                        pa[0] = pack_f16(sc[2 * ks][0], sc[2 * ks][1]);
+                        pa[1] = pack_f16(sc[2 * ks][2], sc[2 * ks][3]);
+                        pa[2] = pack_f16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+                        pa[3] = pack_f16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+                        constexpr int kW = D / 32;  // 32-bit words of a lane's bytes per token
+                        const uint8_t* vt = pipe + s * L::kSlot + L::kHalf;
+                        const int ta = ks * 16 + 2 * qd;
+                        uint32_t vw[4][kW];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int tok = ta + (r & 1) + (r >> 1) * 8;
+#pragma unroll
+                            for (int c = 0; c < kW / 4; ++c) {
+                                const int ch = (D / 128) * gq + c;  // 16-byte chunk along the row
+                                const uint4 x = *reinterpret_cast<const uint4*>(
+                                    vt + (ch >> 3) * L::kBoxBytes + sw128_off(tok, ch & 7));
+                                vw[r][4 * c] = x.x;
+                                vw[r][4 * c + 1] = x.y;
+                                vw[r][4 * c + 2] = x.z;
+                                vw[r][4 * c + 3] = x.w;
                             }
                         }
-                    };
-                    if (edge) pv(std::true_type{});
-                    else pv(std::false_type{});
-                    continue;
-                }
-                // bf16: V through transposed ldmatrix
-                pa[0] = pack_bf16(sc[2 * ks][0], sc[2 * ks][1]);
-                pa[1] = pack_bf16(sc[2 * ks][2], sc[2 * ks][3]);
-                pa[2] = pack_bf16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-                pa[3] = pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+                        // the keep masks only bite on edge tiles (the choice is per tile, so
+                        // warp-uniform): other tiles skip the 64 ANDs
+                        auto pv = [&](auto masked) {
 #pragma unroll
-                for (int np = 0; np < D / 16; ++np) {
-                    const uint32_t mi = lane >> 3;
-                    const uint32_t tok = ks * 16 + (mi & 1) * 8 + (lane & 7);
-                    const uint32_t cg = 2 * np + (mi >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
-                    b0 &= keep_lo;
-                    b2 &= keep_lo;
-                    b1 &= keep_hi;
-                    b3 &= keep_hi;
-                    mma_bf16_16816(o[2 * np], pa, b0, b1);
-                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                            for (int wd = 0; wd < kW; ++wd) {
+                                const uint32_t ab0 = __byte_perm(vw[0][wd], vw[1][wd], 0x5140);
+                                const uint32_t ab1 = __byte_perm(vw[0][wd], vw[1][wd], 0x7362);
+                                const uint32_t cd0 = __byte_perm(vw[2][wd], vw[3][wd], 0x5140);
+                                const uint32_t cd1 = __byte_perm(vw[2][wd], vw[3][wd], 0x7362);
+                                const uint32_t pairs[4][2] = {{ab0 & 0xffffu, cd0 & 0xffffu},
+                                                              {ab0 >> 16, cd0 >> 16},
+                                                              {ab1 & 0xffffu, cd1 & 0xffffu},
+                                                              {ab1 >> 16, cd1 >> 16}};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    uint32_t b0 = e4m3x2_to_f16x2(pairs[e][0]);
+                                    uint32_t b1 = e4m3x2_to_f16x2(pairs[e][1]);
+                                    if constexpr (decltype(masked)::value) {
+                                        b0 &= keep_lo;
+                                        b1 &= keep_hi;
+                                    }
+                                    mma_f16_16816(o[4 * wd + e], pa, b0, b1);
+                                }
+                            }
+                        };
+                        if (edge) pv(std::true_type{});
+                        else pv(std::false_type{});
+                        continue;
+                    }
+                    // bf16: V through transposed ldmatrix
+                    pa[0] = pack_bf16(sc[2 * ks][0], sc[2 * ks][1]);
+                    pa[1] = pack_bf16(sc[2 * ks][2], sc[2 * ks][3]);
+                    pa[2] = pack_bf16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+                    pa[3] = pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+#pragma unroll
+                    for (int np = 0; np < D / 16; ++np) {
+                        const uint32_t mi = lane >> 3;
+                        const uint32_t tok = ks * 16 + (mi & 1) * 8 + (lane & 7);
+                        const uint32_t cg = 2 * np + (mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vbase + (cg >> 3) * L::kBoxBytes + sw128_off(tok, cg & 7), b0, b1, b2, b3);
+                        b0 &= keep_lo;
+                        b2 &= keep_lo;
+                        b1 &= keep_hi;
+                        b3 &= keep_hi;
+                        mma_bf16_16816(o[2 * np], pa, b0, b1);
+                        mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[s]);
+            }
+            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
+            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
+            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
+            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
+
+            // ------------------------------------------------------ the piece's merge
+            // Warp 0 gathers the other warps' (m, l, O) through the finished piece's Q slot
+            // (32 D bytes: half of one warp's O), one half of one warp at a time, and writes
+            // the piece's partial.
+            if (qd == 0) {
+                m_sh[warp][r0] = m_run[0];
+                l_sh[warp][r0] = l_run[0];
+                m_sh[warp][r1] = m_run[1];
+                l_sh[warp][r1] = l_run[1];
+            }
+            consumers_sync();
+            // merged row maxima (warp 0); a row with nothing allowed keeps exponent base 0
+            float mu0 = 0.f, mu1 = 0.f;
+            if (warp == 0) {
+                float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumers; ++w) {
+                    M0 = fmaxf(M0, m_sh[w][r0]);
+                    M1 = fmaxf(M1, m_sh[w][r1]);
+                }
+                mu0 = (M0 == -INFINITY) ? 0.f : M0;
+                mu1 = (M1 == -INFINITY) ? 0.f : M1;
+                const float w0 = ex2(m_sh[0][r0] - mu0), w1 = ex2(m_sh[0][r1] - mu1);
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    o[n][0] *= w0;
+                    o[n][1] *= w0;
+                    o[n][2] *= w1;
+                    o[n][3] *= w1;
+                }
+            }
+            float* const xb = reinterpret_cast<float*>(qslots + qsl * kQWords);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int w = 1; w < kConsumers; ++w) {
+                    if (warp == w) {
+#pragma unroll
+                        for (int nn = 0; nn < D / 16; ++nn)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) xb[(nn * 4 + e) * 32 + lane] = o[h * (D / 16) + nn][e];
+                    }
+                    consumers_sync();
+                    if (warp == 0) {
+                        const float w0 = ex2(m_sh[w][r0] - mu0), w1 = ex2(m_sh[w][r1] - mu1);
+#pragma unroll
+                        for (int nn = 0; nn < D / 16; ++nn)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                o[h * (D / 16) + nn][e] += (e < 2 ? w0 : w1) * xb[(nn * 4 + e) * 32 + lane];
+                    }
+                    consumers_sync();
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[s]);
-        }
-        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
-        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
-        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
-        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
-
-        // ---------------------------------------------------------- in-CTA merge
-        // Once all four consumer warps are past their loops, every tile the producer
-        // issued has landed (each was waited on), so the ring can hold the merge data.
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-        float* mo = reinterpret_cast<float*>(pipe);  // [kConsumers][16][D]
-        if constexpr (kE4M3) {
+            if (lane == 0) mbar_arrive(&q_empty[qsl]);  // Q slot and merge buffer are free
+            if (warp == 0) {
+                if (k < 0 || k >= p.max_slots) {
+                    // cannot happen while the scratch holds max_slots partials per row: never
+                    // write past it
+                    if (lane == 0) atomicOr(&g_decode_error, kDevErrTimeout);
+                } else {
+                    const float vs = kE4M3 ? p.v_scale : 1.f;
+                    const size_t row0 = ((size_t)b * p.hq + g * p.group + r0 / p.s_active) * p.s_active + t0;
+                    const size_t row1 = ((size_t)b * p.hq + g * p.group + r1 / p.s_active) * p.s_active + t1;
+                    float* const po0 = p.part_o + (row0 * p.max_slots + k) * D;
+                    float* const po1 = p.part_o + (row1 * p.max_slots + k) * D;
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n) {  // n-tile n holds head dims (D/8) * {2qd, 2qd+1} + n
-                const int d0 = (D / 8) * 2 * qd + n, d1 = d0 + D / 8;
-                mo[(warp * 16 + r0) * D + d0] = o[n][0];
-                mo[(warp * 16 + r0) * D + d1] = o[n][1];
-                mo[(warp * 16 + r1) * D + d0] = o[n][2];
-                mo[(warp * 16 + r1) * D + d1] = o[n][3];
-            }
-        } else {
+                    for (int n = 0; n < D / 8; ++n) {
+                        if constexpr (kE4M3) {  // n-tile n holds head dims (D/8) * {2qd, 2qd+1} + n
+                            const int d0 = (D / 8) * 2 * qd + n, d1 = d0 + D / 8;
+                            if (v0) {
+                                po0[d0] = o[n][0] * vs;
+                                po0[d1] = o[n][1] * vs;
+                            }
+                            if (v1) {
+                                po1[d0] = o[n][2] * vs;
+                                po1[d1] = o[n][3] * vs;
+                            }
+                        } else {
+                            const int col = n * 8 + 2 * qd;
+                            if (v0) *reinterpret_cast<float2*>(po0 + col) = make_float2(o[n][0], o[n][1]);
+                            if (v1) *reinterpret_cast<float2*>(po1 + col) = make_float2(o[n][2], o[n][3]);
+                        }
+                    }
+                    if (qd == 0) {
+                        // (max, sum) of the piece; m_sh is rewritten only after the next
+                        // piece's first barrier, which this warp has not reached
+                        float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                const int col = n * 8 + 2 * qd;
-                *reinterpret_cast<float2*>(mo + (warp * 16 + r0) * D + col) = make_float2(o[n][0], o[n][1]);
-                *reinterpret_cast<float2*>(mo + (warp * 16 + r1) * D + col) = make_float2(o[n][2], o[n][3]);
-            }
-        }
-        if (qd == 0) {
-            m_sh[warp][r0] = m_run[0];
-            l_sh[warp][r0] = l_run[0];
-            m_sh[warp][r1] = m_run[1];
-            l_sh[warp][r1] = l_run[1];
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-        const int ctid = threadIdx.x;  // 0 .. 127
-        for (int idx = ctid; idx < p.rows * D; idx += kConsumers * 32) {
-            const int r = idx / D, x = idx % D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, m_sh[w][r]);
-            float acc = 0.f, lsum = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kConsumers; ++w) {
-                    const float wt = ex2(m_sh[w][r] - M);
-                    acc += wt * mo[(w * 16 + r) * D + x];
-                    lsum += wt * l_sh[w][r];
+                        for (int w = 0; w < kConsumers; ++w) {
+                            M0 = fmaxf(M0, m_sh[w][r0]);
+                            M1 = fmaxf(M1, m_sh[w][r1]);
+                            L0 += ex2(m_sh[w][r0] - mu0) * l_sh[w][r0];
+                            L1 += ex2(m_sh[w][r1] - mu1) * l_sh[w][r1];
+                        }
+                        if (v0) {
+                            p.part_ml[(row0 * p.max_slots + k) * 2 + 0] = M0;
+                            p.part_ml[(row0 * p.max_slots + k) * 2 + 1] = L0;
+                        }
+                        if (v1) {
+                            p.part_ml[(row1 * p.max_slots + k) * 2 + 0] = M1;
+                            p.part_ml[(row1 * p.max_slots + k) * 2 + 1] = L1;
+                        }
+                    }
                 }
-            }
-            const int h = g * p.group + r / p.s_active, t = r % p.s_active;
-            const size_t rowid = ((size_t)b * p.hq + h) * p.s_active + t;
-            const size_t slot = rowid * p.max_splits + split;
-            p.part_o[slot * D + x] = kE4M3 ? acc * p.v_scale : acc;
-            if (x == 0) {
-                p.part_ml[slot * 2 + 0] = M;
-                p.part_ml[slot * 2 + 1] = lsum;
             }
         }
     }
 }
 
-// Merge the chunks of one (sequence, head, new token) row by log-sum-exp:
+// Merge the pieces of one (sequence, head, new token) row by log-sum-exp:
 //   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
 //   LSE = (M + log2 L) ln 2   (m_i are in log2 units of the scaled scores);
-// with a sink, the merged row is finished by finish_row (the sink joins M and L).
+// with a sink, the merged row is finished by finish_row (the sink joins M and L).  A row of
+// a sequence whose cache_len is out of range gets O = 0, LSE = -inf and is reported.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __restrict__ cache_len,
                                                            const float* __restrict__ part_o,
                                                            const float* __restrict__ part_ml,
+                                                           const int* __restrict__ npieces,
                                                            const float* __restrict__ sink,
                                                            OutT* __restrict__ o, float* lse,
-                                                           int hq, int s_active, int chunk,
-                                                           int gran, int max_splits,
-                                                           int max_cache_len, int window,
+                                                           int hq, int hkv, int s_active,
+                                                           int max_slots, int max_cache_len,
                                                            int circular) {
     const size_t rowid = blockIdx.x;
     const int b = (int)(rowid / ((size_t)hq * s_active));
+    const int h = (int)((rowid / s_active) % hq);
     const int x = threadIdx.x;
-    const int len = cache_len[b];
+    const int len = cache_len[b];  // not written by the split kernel
+    griddep_wait();                // the split kernel's partials are complete and visible
     float out = 0.f, lse_v = -INFINITY;
     if (len >= s_active && (circular || len <= max_cache_len)) {
-        // the splits that ran (as decode_split_kernel): the non-empty ones
-        const int first = decode_first_slot(len, s_active, window, circular, gran);
-        const int nslots = decode_nslots(len, circular, max_cache_len);
-        int ns = decode_nsplits(nslots, first, chunk);
-        for (int lo, hi; ns > 0; --ns) {  // drop empty last splits
-            decode_split_range(nslots, first, chunk, gran, ns - 1, lo, hi);
-            if (lo < hi) break;
+        int ns = npieces[(size_t)b * hkv + h / (hq / hkv)];
+        if (ns < 1 || ns > max_slots) {  // cannot happen: never read past the slots
+            if (x == 0) atomicOr(&g_decode_error, kDevErrTimeout);
+            ns = 0;
         }
-        const int s0 = 0;
-        const float* ml = part_ml + rowid * max_splits * 2;
+        const float* ml = part_ml + rowid * max_slots * 2;
         float M = -INFINITY;
-        for (int s = s0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
         if (M != -INFINITY) {
             float Lsum = 0.f, acc = 0.f;
-            const float* po = part_o + rowid * max_splits * D + x;
-            for (int s = s0; s < ns; ++s) {
+            const float* po = part_o + rowid * max_slots * D + x;
+            for (int s = 0; s < ns; ++s) {
                 const float wt = ex2(ml[2 * s] - M);
                 Lsum += wt * ml[2 * s + 1];
                 acc += wt * po[(size_t)s * D];
@@ -729,13 +938,15 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __rest
                 lse_v = (M + __log2f(Lsum)) * kLn2;
             } else {
                 float inv;
-                finish_row(true, M, Lsum, sink[(rowid / s_active) % hq], inv, lse_v);
+                finish_row(true, M, Lsum, sink[h], inv, lse_v);
                 out = acc * inv;
             }
         } else if (sink != nullptr) {  // nothing allowed: the sink alone (O = 0, LSE = sink)
             float inv;
-            finish_row(false, 0.f, 0.f, sink[(rowid / s_active) % hq], inv, lse_v);
+            finish_row(false, 0.f, 0.f, sink[h], inv, lse_v);
         }
+    } else if (x == 0 && h == 0 && rowid % s_active == 0) {
+        atomicOr(&g_decode_error, kDevErrCacheLen);
     }
     if constexpr (sizeof(OutT) == 2)
         o[rowid * D + x] = __float2bfloat16_rn(out);
@@ -821,6 +1032,26 @@ __global__ void gen_mask_kernel(const int32_t* __restrict__ cache_len, int hq, i
     }
 }
 
+// SMs of the current device (looked up once per device).
+int device_sms() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 0;
+    }
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 template <int D, bool kE4M3>
 attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     using L = DecodeLayout<D, kE4M3>;
@@ -842,6 +1073,8 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     p.cache_len = a.cache_len;
     p.part_o = a.part_o;
     p.part_ml = a.part_ml;
+    p.npieces = a.npieces;
+    p.b = a.b;
     p.hq = a.hq;
     p.hkv = a.hkv;
     p.s_active = a.s_active;
@@ -851,8 +1084,8 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     p.max_cache_len = a.max_cache_len;
     p.group = a.hq / a.hkv;
     p.rows = p.group * a.s_active;
-    p.chunk = a.kv_chunk;
-    p.max_splits = a.max_splits;
+    p.min_tiles = a.kv_chunk / kBT;
+    p.max_slots = a.max_slots;
     p.paged = paged ? 1 : 0;
     p.box_rows = box_rows;
     p.c = kE4M3 ? a.scale * a.k_scale * kLog2e : a.scale * kLog2e;
@@ -870,19 +1103,36 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
         }
         mark_setup(attr_done);
     }
-    dim3 grid(a.max_splits, a.hkv, a.b);
-    decode_split_kernel<D, kE4M3><<<grid, kThreads, L::kDynBytes, stream>>>(tk, tv, p);
+    // one wave: the CTAs every SM holds at once
+    const int sms = device_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    decode_split_kernel<D, kE4M3><<<sms * L::kMinCtas, kThreads, L::kDynBytes, stream>>>(tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    const unsigned nrows = (unsigned)((size_t)a.b * a.hq * a.s_active);
+    // The merge launches as a programmatic dependent of the split pass, so its launch overlaps
+    // the split pass's last CTAs.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((size_t)a.b * a.hq * a.s_active));
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    const float* po = a.part_o;
+    const float* pml = a.part_ml;
+    const int* np = a.npieces;
     if (a.o_dtype == ATTN_BF16)
-        decode_combine_kernel<D, __nv_bfloat16><<<nrows, D, 0, stream>>>(
-            a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<__nv_bfloat16*>(a.o), a.lse, a.hq,
-            a.s_active, a.kv_chunk, kBT, a.max_splits, a.max_cache_len, a.window, a.circular);
+        e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, __nv_bfloat16>, a.cache_len, po, pml,
+                               np, a.sink, static_cast<__nv_bfloat16*>(a.o), a.lse, a.hq, a.hkv,
+                               a.s_active, a.max_slots, a.max_cache_len, a.circular);
     else
-        decode_combine_kernel<D, float><<<nrows, D, 0, stream>>>(
-            a.cache_len, a.part_o, a.part_ml, a.sink, static_cast<float*>(a.o), a.lse, a.hq, a.s_active,
-            a.kv_chunk, kBT, a.max_splits, a.max_cache_len, a.window, a.circular);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+        e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, float>, a.cache_len, po, pml, np,
+                               a.sink, static_cast<float*>(a.o), a.lse, a.hq, a.hkv, a.s_active,
+                               a.max_slots, a.max_cache_len, a.circular);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
 

@@ -189,8 +189,10 @@ size_t attn_prefill_workspace_bytes(int sq);
 
 /*
  * attn_decode_workspace_bytes -- bytes of caller-provided scratch that attn_fwd_decode
- * needs for these sizes (split-KV partial outputs and their (max, sum) pairs).
- * kv_chunk as for attn_fwd_decode (0 = library default).  Returns 0 for invalid sizes.
+ * needs for these sizes: split-KV partial outputs [b*hq*s_active][slots][d] fp32 and
+ * their (max, sum) pairs, slots = ceil(max_cache_len / kv_chunk) + 1, then one int per
+ * (sequence, head).  kv_chunk as for attn_fwd_decode (0 = library default).  Returns 0
+ * for invalid sizes.
  */
 size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_cache_len,
                                    int kv_chunk);
@@ -205,8 +207,10 @@ size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_c
  *   new token t sits at q_pos = cache_len[b] - s_active + t and attends cache position j
  *   iff j <= q_pos (the validity cut j < cache_len plus the tril block among the new
  *   tokens); the softmax runs over the cache axis; GQA as in attn_fwd_prefill.
- * It runs as a split-KV pass (each (sequence, kv head, chunk of kv_chunk tokens) keeps
- * its own running max, sum and unnormalised output) followed by a log-sum-exp combine.
+ * It runs as a split-KV pass followed by a log-sum-exp combine.  The split pass is one
+ * wave of CTAs that share the KV tiles of all (sequence, kv head) pairs evenly, each CTA
+ * reading at least kv_chunk tokens (unless it reads the last ones); every piece of a pair
+ * that one CTA reads keeps its own running max, sum and unnormalised output.
  *
  * Layouts:
  *   q : bf16 [b, hq, s_active, d]        o : [b, hq, s_active, d] in o_dtype
@@ -223,8 +227,9 @@ size_t attn_decode_workspace_bytes(int b, int hq, int s_active, int d, int max_c
  *   paged: page_size a power of two in [16, 256], max_cache_len <=
  *   max_pages_per_seq * page_size, num_pages >= 1; kv_chunk = 0 or a positive multiple of
  *   32 (and of page_size when page_size > 32).  kv_chunk = 0 picks the largest power of two
- *   in [256, 4096] not above b * max_cache_len / 128 (about 128 splits across the batch
- *   per kv head); attn_decode_workspace_bytes applies the same rule.
+ *   in [256, 4096] not above b * max_cache_len / 128; attn_decode_workspace_bytes applies
+ *   the same rule.  A larger kv_chunk needs less scratch; below the even share of the
+ *   tiles it does not change how the work is split.
  * Workspace: device scratch of at least attn_decode_workspace_bytes(...), 16-byte aligned,
  *   owned by the caller, not read before it is written; calls that share it must not
  *   overlap on the device.

@@ -146,9 +146,11 @@ def test_ex_calls_check_their_options_before_launch(lib):
 
 
 def _ws(b, hq, s_active, d, max_len, chunk):
-    # rows = b*hq*s_active; splits = ceil(max_len / chunk); O partials (256-byte padded) + (m, l)
-    rows, splits = b * hq * s_active, -(-max_len // chunk)
-    return ((rows * splits * d * 4 + 255) // 256) * 256 + rows * splits * 8
+    # rows = b*hq*s_active; slots = ceil(max_len / chunk) + 1; O partials (256-byte padded),
+    # (m, l) pairs (16-byte padded), one int per (sequence, head)
+    rows, slots = b * hq * s_active, -(-max_len // chunk) + 1
+    return (((rows * slots * d * 4 + 255) // 256) * 256 + ((rows * slots * 8 + 15) // 16) * 16
+            + b * hq * 4)
 
 
 @pytest.mark.parametrize("b,max_len,chunk", [
@@ -166,7 +168,7 @@ def test_workspace_default_chunk(lib, b, max_len, chunk):
 
 def test_workspace_bytes_formula(lib):
     assert A.attn_decode_workspace_bytes(64, 32, 4, 128, 32768, 1024) == _ws(64, 32, 4, 128, 32768, 1024)
-    assert A.attn_decode_workspace_bytes(1, 1, 1, 64, 100, 64) == ((2 * 64 * 4 + 255) // 256) * 256 + 16
+    assert A.attn_decode_workspace_bytes(1, 1, 1, 64, 100, 64) == ((3 * 64 * 4 + 255) // 256) * 256 + 32 + 4
     assert A.attn_decode_workspace_bytes(1, 1, 1, 96, 100) == 0
     assert A.attn_decode_workspace_bytes(1, 1, 1, 64, 100, 33) == 0
 

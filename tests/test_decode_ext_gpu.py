@@ -46,6 +46,10 @@ WINDOW = [
     ("win129_paged64_d256", 2, 4, 2, 256, 2, 64, (70, 700), True, 128, 129, False),
     ("win300_paged_e4m3", 3, 8, 2, 128, 4, 32, (40, 1030, 777), True, 128, 300, True),
     ("win333_paged128_e4m3_chunk96", 2, 8, 2, 128, 2, 128, (700, 1500), True, 96, 333, True),
+    # lengths whose window start is rounded down by a whole tile less one slot, so the span
+    # read is window + s_active - 1 + 31: the largest one, which fixes how many splits launch
+    ("win66_flat_sa1_span_bound", 4, 8, 2, 128, 1, 32, (129, 128, 160, 97), False, 96, 66, False),
+    ("win93_paged_sa4_span_bound", 3, 8, 2, 128, 4, 32, (159, 127, 1000), True, 64, 93, False),
 ]
 
 
