@@ -12,8 +12,9 @@ tokens, packed sequences, the attention sink, the FP8-e4m3 cache, and a windowed
 with RoPE.  Each line carries the fp64 CPU oracle timed on the host cores beside it.
 
 Timing: W untimed warm-up steps, then exactly K timed steps; every step is bracketed
-by CUDA events on the launching stream, and a 256 MiB buffer is written between steps
-to flush the 129 MB L2.  A barrier plus torch.cuda.synchronize() bracket the timed
+by CUDA events on the launching stream, and between steps a 256 MiB buffer is written
+(flushing the 129 MB L2) and another 256 MiB read (so the flush leaves no dirty line to be
+written back inside the next step).  A barrier plus torch.cuda.synchronize() bracket the timed
 region; with N > 1 ranks each rank runs its own replica and the max over ranks is used.
 SM clocks are sampled with nvidia-smi while the timed regions run.
 
@@ -194,20 +195,42 @@ def check_device(stream, what):
         raise RuntimeError(f"{what}: device error {A.attn_status_string(err)}")
 
 
-def time_steps(fn, steps, warmup, flush_buf, stream):
+class L2Flush:
+    """The L2 flush between timed steps: a write of L2_FLUSH_BYTES evicts every line the step
+    read, then a read of another L2_FLUSH_BYTES writes the first buffer's dirty lines back.
+    Without the read the L2 would start the timed step holding about its size in dirty lines
+    of the flush buffer, whose write-back would fall inside the timed region (measured: 8 %
+    of the 0.2 ms windowed decode)."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.write_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.read_buf = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def __call__(self, i):
+        self.write_buf.fill_(i & 0xFF)
+        self.read_buf.sum()
+
+
+L2_NOTE = (f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB written, then another "
+           f"{L2_FLUSH_BYTES >> 20} MiB read so no dirty line is left)")
+
+
+def time_steps(fn, steps, warmup, flush, stream):
     """Per-step device time (ms) with CUDA events on `stream`; L2 flushed before each step."""
     import torch
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            flush_buf.fill_(1)
+        for i in range(warmup):
+            flush(i)
             fn()
         torch.cuda.synchronize()
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         for i in range(steps):
-            flush_buf.fill_(i & 0xFF)  # on the timing stream, outside the events
+            flush(i)  # on the timing stream, outside the events
             starts[i].record(stream)
             fn()
             ends[i].record(stream)
@@ -658,7 +681,7 @@ def workload_config(w, world):
     return {"workload": w.name, "b": w.b, "hq": w.hq, "hkv": w.hkv, "sq": w.sq, "skv": w.skv,
             "d": w.d, "causal": w.causal, "window": w.window, "o_dtype": w.o_dtype,
             "q_outliers": w.outlier_frac,
-            "l2": "flushed between steps (256 MiB write)",
+            "l2": L2_NOTE,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -709,7 +732,7 @@ def main():
     A.load_library()
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     # the oracle beside each line: rank 0 of a single-GPU run only
     cpu = (os.cpu_count() or 1) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else 0
 

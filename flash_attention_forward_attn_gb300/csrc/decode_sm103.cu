@@ -87,7 +87,9 @@ __device__ __forceinline__ int circular_pos(int r, int len, int cap) {
 // is held exactly as hi + lo (an FMA gives the product's rounding error; pos < 2^24 is
 // exact in fp32), and 2 pi is taken off k times in two pieces, the first with 8
 // significant bits so that k * piece is exact while |k| < 2^16.  The error stays near
-// 1e-5 rad.  Larger angles (beyond 2^18 rad, rare) are reduced in double.
+// 1e-5 rad.  Larger angles (beyond 2^18 rad, rare) are reduced in double.  The reduced
+// angle (|r| <= pi + 1e-5) goes to the hardware sine and cosine (__sincosf, absolute error
+// about 5e-7 there).
 __device__ __forceinline__ void rope_sincos(int pos, float f, float& sn, float& cs) {
     const float x = (float)pos;
     const float hi = x * f;
@@ -98,13 +100,13 @@ __device__ __forceinline__ void rope_sincos(int pos, float f, float& sn, float& 
         constexpr float kC2 = 1.9353071795864769e-3f;  // 2 pi - kC1
         const float k = rintf(hi * kInvTwoPi);
         const float r = (fmaf(-k, kC1, hi) - k * kC2) + lo;
-        sincosf(r, &sn, &cs);
+        __sincosf(r, &sn, &cs);
         return;
     }
     constexpr double kTwoPi = 6.283185307179586;
     double th = (double)pos * (double)f;
     th -= kTwoPi * rint(th * (1.0 / kTwoPi));
-    sincosf((float)th, &sn, &cs);
+    __sincosf((float)th, &sn, &cs);
 }
 // The rotation of two pairs by the angles (s0, c0) and (s1, c1).
 __device__ __forceinline__ void rope_apply(uint32_t& lo, uint32_t& hi, float s0, float c0,
@@ -116,11 +118,12 @@ __device__ __forceinline__ void rope_apply(uint32_t& lo, uint32_t& hi, float s0,
 }
 
 // Rows a (position pa) and b (position pb) of a lane, elements i and i + 1 of each:
-// the angles are computed once when the two rows share a position.
+// the angles are computed once when the two rows share a position.  inv_freq is the
+// CTA's shared-memory copy of the inverse frequencies.
 __device__ __forceinline__ void rope_rows(uint32_t& alo, uint32_t& ahi, uint32_t& blo,
                                           uint32_t& bhi, int i, int pa, int pb,
                                           const float* inv_freq) {
-    const float f0 = __ldg(inv_freq + i), f1 = __ldg(inv_freq + i + 1);
+    const float f0 = inv_freq[i], f1 = inv_freq[i + 1];
     float s0, c0, s1, c1;
     rope_sincos(pa, f0, s0, c0);
     rope_sincos(pa, f1, s1, c1);
@@ -164,9 +167,9 @@ struct DecodeLayout {
     static constexpr int kQSmem = (D / 16) * 32 * 16;
     static constexpr int kDynBytes = kPipe + 2 * kQSmem + 1024;  // + alignment slack
     static constexpr int kMinCtas = D > 128 ? 1 : 3;  // CTAs per SM the registers are fitted to
-    // dynamic + static (barriers, piece records, merge maxima: under 1 KB) + the 1 KB the
-    // SM reserves per CTA
-    static_assert(kMinCtas * (kDynBytes + 2048) <= 232448, "shared memory of kMinCtas CTAs");
+    // dynamic + static (barriers, piece records, merge maxima, inverse frequencies: under
+    // 1.5 KB) + the 1 KB the SM reserves per CTA, within the SM's 228 KB
+    static_assert(kMinCtas * (kDynBytes + 1536 + 1024) <= 233472, "shared memory of kMinCtas CTAs");
 };
 
 struct DecodeParams {
@@ -258,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages], q_full[2], q_empty[2];
     __shared__ PieceInfo info[2];
     __shared__ float m_sh[kConsumers][16], l_sh[kConsumers][16];
+    __shared__ float inv_freq[D / 2];  // RoPE inverse frequencies (producer only)
     __shared__ int abort_flag;
 
     // The merge kernel is launched as this grid's programmatic dependent: it may take free
@@ -290,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
+        // the inverse frequencies once per CTA: each piece's RoPE then waits on no global load
+        if (p.rope_inv_freq != nullptr)
+            for (int i = lane; i < D / 2; i += 32) inv_freq[i] = __ldg(p.rope_inv_freq + i);
+        __syncwarp();
         const int nbox = kBT / p.box_rows;
         const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;
         int issued = 0;
@@ -396,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
                     for (int ks = 0; ks < D / 32; ++ks) {
                         const int c = ks * 16 + 4 * qd;
                         rope_rows(qa[ks].x, qa[ks + D / 32].x, qb[ks].x, qb[ks + D / 32].x, c, qpos0,
-                                  qpos1, p.rope_inv_freq);
+                                  qpos1, inv_freq);
                         rope_rows(qa[ks].y, qa[ks + D / 32].y, qb[ks].y, qb[ks + D / 32].y, c + 2,
-                                  qpos0, qpos1, p.rope_inv_freq);
+                                  qpos0, qpos1, inv_freq);
                     }
                 }
 #pragma unroll
@@ -453,9 +461,9 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
                     for (int ks = 0; ks < D / 32; ++ks) {
                         const int c = ks * 16 + 2 * qd;
                         rope_rows(qf[ks][0], qf[ks + D / 32][0], qf[ks][1], qf[ks + D / 32][1], c,
-                                  qpos0, qpos1, p.rope_inv_freq);
+                                  qpos0, qpos1, inv_freq);
                         rope_rows(qf[ks][2], qf[ks + D / 32][2], qf[ks][3], qf[ks + D / 32][3], c + 8,
-                                  qpos0, qpos1, p.rope_inv_freq);
+                                  qpos0, qpos1, inv_freq);
                     }
                 }
             }
@@ -576,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
             const PieceInfo& pi = info[qsl];
             const int npc = pi.npc;
             if (npc == 0) break;  // the same value in every consumer warp
-            const int b = pi.b, g = pi.g, len = pi.len, nslots = pi.nslots, first = pi.first;
-            const int t_off = pi.t_off, i0 = pi.i0, k = pi.k;
+            const int len = pi.len, nslots = pi.nslots, first = pi.first;
+            const int t_off = pi.t_off, i0 = pi.i0;
             const float c_row0 = pi.c_row[r0], c_row1 = pi.c_row[r1];
             const uint4* const qs = qslots + qsl * kQWords;
             auto qfrag = [&](int ks, uint32_t* f) {
@@ -837,8 +845,10 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
                     consumers_sync();
                 }
             }
+            // the piece's pair and slot, read before the producer may reuse the record
+            const int b = pi.b, g = pi.g, k = pi.k;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&q_empty[qsl]);  // Q slot and merge buffer are free
+            if (lane == 0) mbar_arrive(&q_empty[qsl]);  // Q slot, record and merge buffer are free
             if (warp == 0) {
                 if (k < 0 || k >= p.max_slots) {
                     // cannot happen while the scratch holds max_slots partials per row: never
