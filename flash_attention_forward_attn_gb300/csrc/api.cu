@@ -246,14 +246,22 @@ attn_status attn_fwd_decode_ex(const void* q, const void* k_cache, const void* v
         return ATTN_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || workspace_bytes < ob + mlb + npb)
         return ATTN_ERR_WORKSPACE;
-    const int chunk = resolve_chunk(kv_chunk, b, max_cache_len);
+    int chunk = resolve_chunk(kv_chunk, b, max_cache_len);
     if (op.window > 0 && !op.circular) {
         // A window that does not wrap bounds the slots any sequence reads: its start is
         // rounded down to a whole tile, so at most window + s_active - 1 + (tile - 1)
         // slots, and no pair has more pieces than that span allows (the partials keep
-        // the scratch's layout, with this smaller stride).
+        // the scratch's layout, with this smaller stride).  With the default kv_chunk the
+        // least share of a CTA is the smallest one the scratch's slots still allow for that
+        // span, so that short windows of a small batch spread over every CTA.
         const long long span = std::min<long long>(
             max_cache_len, (long long)op.window + s_active - 1 + (attn::kDecodeTile - 1));
+        if (kv_chunk == 0) {
+            const long long share = (span + max_slots - 2) / (max_slots - 1);  // max_slots >= 2
+            chunk = (int)std::max<long long>(attn::kDecodeTile,
+                                             (share + attn::kDecodeTile - 1) /
+                                                 attn::kDecodeTile * attn::kDecodeTile);
+        }
         max_slots = (int)std::min<long long>(max_slots, (span + chunk - 1) / chunk + 1);
     }
     attn::DecodeArgs a;

@@ -80,11 +80,21 @@ def check(lens, hkv, sa, window, circular, cap, chunk, grid):
             assert npieces[(b, g)] <= bound
 
 
+def window_default_chunk(cap, chunk, window, sa):
+    """The decode call's least CTA share for a window with kv_chunk = 0: the smallest
+    multiple of 32 tokens for which the window's span still fits the scratch's slots."""
+    slots = -(-cap // chunk) + 1
+    span = min(cap, window + sa - 1 + TILE - 1)
+    share = -(-span // (slots - 1))
+    return max(TILE, -(-share // TILE) * TILE)
+
+
 def test_benchmark_shapes():
     rnd = random.Random(7)
     lens = [rnd.randint(1024, 32768) for _ in range(64)]
     check(lens, 8, 4, 0, False, 32768, 4096, 456)        # 4 new tokens, 3 CTAs x 152 SMs
-    check(lens, 8, 4, 4096, False, 32768, 4096, 456)     # window 4096
+    check(lens, 8, 4, 4096, False, 32768, window_default_chunk(32768, 4096, 4096, 4), 456)
+    check(lens[:16], 8, 4, 4096, False, 32768, window_default_chunk(32768, 4096, 4096, 4), 456)
     check(lens[:32], 8, 1, 0, False, 32768, 4096, 152)   # head_dim 256: one CTA per SM
     check((40, 3000, 300, 33, 1000, 64, 2999, 700), 8, 4, 0, False, 3000, 256, 456)
 
@@ -105,5 +115,7 @@ def test_random_shapes(seed):
         else:  # lengths in range, out of range (skipped) and at the edges
             lens = [rnd.choice([rnd.randint(0, cap), rnd.randint(sa, cap), cap, cap + 5])
                     for _ in range(b)]
-        check(lens, hkv, sa, window, circular, cap, TILE * rnd.randint(1, 40),
-              rnd.choice([1, 3, 7, 456]))
+        chunk = TILE * rnd.randint(1, 40)
+        if window > 0 and not circular and rnd.random() < 0.5:
+            chunk = window_default_chunk(cap, chunk, window, sa)
+        check(lens, hkv, sa, window, circular, cap, chunk, rnd.choice([1, 3, 7, 456]))
