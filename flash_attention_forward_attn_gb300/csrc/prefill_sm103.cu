@@ -63,7 +63,8 @@ struct PrefillParams {
     const int* cu_q;
     const int* cu_k;
     int nseq;
-    const int* order;  // packed: query units heaviest first (unit_order_kernel), or NULL
+    const int* order;  // packed: the work order of the query units (unit_order_kernel), or NULL
+    int* unit_counter; // packed, head_dim <= 128: units handed out at run time from this, or NULL
     int hq, hkv, sq, skv, group, nqt, window, causal, o_f32;
     int nbh;     // b * hq
     int nunits;  // work units of the persistent kernel
@@ -162,19 +163,25 @@ __device__ __forceinline__ TileRange tile_range(const PrefillParams& p, int qt) 
     return r;
 }
 
-// Packed sequences: the query units (a 128-row tile, or a pair of them) ordered by their
-// KV-tile count, most first, ties by index.  Unit indices in the persistent kernels then
-// run through this list, so the zig-zag pairs heavy with light units on every CTA as it
-// does for one causal problem, where the index order already is the order of the work.
-// (Grouping the units by sequence first, so that fewer sequences' K/V are in flight at
-// once, measured 6% slower on 16 sequences: 844 -> 791 TFLOP/s.)  One CTA; the (count,
-// index) keys are sorted by a bitonic network in shared memory.
+// Packed sequences: the work order of the query units (a 128-row tile, or a pair of them).
+// One CTA; the 64-bit keys are sorted by a bitonic network in shared memory, and the unit
+// index is the low 32 bits of each key.
+//  * Static schedule (head_dim 256): KV-tile count, most first, ties by index.  The
+//    persistent kernel's zig-zag then pairs heavy with light units on every CTA as it does
+//    for one causal problem, where the index order already is the order of the work.
+//  * Units handed out at run time (head_dim <= 128, `counter` set): sequence first, then
+//    KV-tile count, most first.  The CTAs draw units from the counter, which this pass
+//    resets, so the units in flight are always a window of this list: the K/V of one or two
+//    sequences, which stays in L2 while their query tiles pass, and the CTAs stay balanced
+//    without a static pairing.  (Against the count order with the zig-zag, on 16 packed
+//    sequences: the count order runs units of every sequence at once, whose K/V (177 MB)
+//    exceed the L2, and read 1.8x the algorithmic bytes.)
 constexpr int kOrderMax = 8192;  // units sorted in one CTA (64 KB of keys)
 constexpr int kOrderThreads = 1024;
 
 template <int BN, int kTilesPerUnit>
 __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const PrefillParams p, int nu,
-                                                                   int* order) {
+                                                                   int* order, int* counter) {
     extern __shared__ unsigned long long keys[];
     int n2 = 1;
     while (n2 < nu) n2 <<= 1;
@@ -183,7 +190,13 @@ __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const Prefill
         if (u < nu) {
             int cost = 0;
             for (int x = 0; x < kTilesPerUnit; ++x) cost += tile_range<BN, true>(p, kTilesPerUnit * u + x).n;
-            key = ((unsigned long long)(0x7fffffff - cost) << 32) | (unsigned)u;
+            if (counter != nullptr) {
+                const int seq = row_sequence(p, min(kTilesPerUnit * u * kBM, p.sq - 1));
+                key = ((unsigned long long)min(seq, 0xffff) << 48) |
+                      ((unsigned long long)(0xffff - min(cost, 0xffff)) << 32) | (unsigned)u;
+            } else {
+                key = ((unsigned long long)(0x7fffffff - cost) << 32) | (unsigned)u;
+            }
         }
         keys[u] = key;
     }
@@ -203,6 +216,7 @@ __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const Prefill
             __syncthreads();
         }
     for (int u = threadIdx.x; u < nu; u += blockDim.x) order[u] = (int)(keys[u] & 0xffffffffu);
+    if (counter != nullptr && threadIdx.x == 0) *counter = 0;
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag) {
@@ -758,12 +772,48 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     __shared__ uint64_t q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[2], p_full[2], o_done[2], o_free[2], mma_drain, stage_free;
     __shared__ uint64_t turn[2];  // MMA issue turns of tiles A and B
+    __shared__ uint64_t unit_full[4], unit_empty[4];  // the ring of units drawn at run time
+    __shared__ int unit_ring[4];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int npairs = (p.nqt + 1) / 2;
     const int G = gridDim.x, cta = blockIdx.x;
+
+    // The units of this CTA, in order.  Fixed: the zig-zag over the work list.  Drawn at run
+    // time (packed sequences with a counter): warp 0 (the K producer, which runs furthest
+    // ahead) takes the next unit from the counter and passes it to the other eleven warps
+    // through a 4-slot ring, which they read in the same order.  A wait that gives up returns
+    // INT_MAX with ok cleared.
+    const bool drawn = kPacked && p.unit_counter != nullptr;
+    auto draw_unit = [&](int r, bool& ok) -> int {  // warp 0, lane 0
+        if (!drawn) return zigzag_unit(cta, r, G);
+        const int slot = r & 3;
+        if (r >= 4 && !mbar_wait(&unit_empty[slot], ((r >> 2) - 1) & 1,
+                                 reinterpret_cast<volatile int*>(&abort_flag))) {
+            ok = false;
+            return INT_MAX;
+        }
+        const int w = atomicAdd(p.unit_counter, 1);
+        unit_ring[slot] = w;
+        mbar_arrive(&unit_full[slot]);
+        return w;
+    };
+    auto read_unit = [&](int r, bool one_lane, bool& ok) -> int {  // the other warps
+        if (!drawn) return zigzag_unit(cta, r, G);
+        const int slot = r & 3;
+        bool got = mbar_wait(&unit_full[slot], (r >> 2) & 1, reinterpret_cast<volatile int*>(&abort_flag));
+        if (!one_lane) got = __all_sync(0xffffffffu, got);
+        if (!got) {
+            ok = false;
+            return INT_MAX;
+        }
+        const int w = unit_ring[slot];
+        if (!one_lane) __syncwarp();
+        if (one_lane || lane == 0) mbar_arrive(&unit_empty[slot]);
+        return w;
+    };
 
     struct Unit {
         int bh, kvz, u0, u1;
@@ -819,6 +869,10 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
         mbar_init(&turn[0], 1);
         mbar_init(&turn[1], 1);
         mbar_arrive(&turn[0]);  // tile A takes the first turn
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&unit_full[i], 1);    // warp 0 wrote the slot
+            mbar_init(&unit_empty[i], 11);  // warps 1-11 read it
+        }
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -850,8 +904,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             int nq[2] = {0, 0};  // Q_A / Q_B loads issued
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int w = zigzag_unit(cta, r, G);
-                if (w >= p.nunits) break;
+                const int w = is_k ? draw_unit(r, ok) : read_unit(r, true, ok);
+                if (!ok || w >= p.nunits) break;
                 const Unit u = unit_at(w);
                 if (!is_k) {
                     // Q_X is reloaded as soon as tile X's last S of the previous unit is done
@@ -917,8 +971,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             int uo = 0;     // units in which tile X had products so far (phase of o_free[x])
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int w = zigzag_unit(cta, r, G);
-                if (w >= p.nunits) break;
+                const int w = read_unit(r, false, ok);
+                if (!ok || w >= p.nunits) break;
                 const Unit u = unit_at(w);
                 const TileRange t = x ? u.t[1] : u.t[0];
                 const bool has_x = x == 0 || u.has_b;  // tile X exists in this unit
@@ -1018,8 +1072,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
         const bool store_thread = (warp & 3) == 0 && lane == 0;
         bool ok = true;
         for (int r = 0;; ++r) {
-            const int w = zigzag_unit(cta, r, G);
-            if (w >= p.nunits) break;
+            const int w = read_unit(r, false, ok);
+            if (!ok || w >= p.nunits) break;
             const Unit u = unit_at(w);
             const TileRange t = x ? u.t[1] : u.t[0];
             // this tile's position in the CTA's sequence of staged output tiles
@@ -1262,7 +1316,8 @@ int num_sms() {
 
 // Writes the packed work order into `order` (nu <= kOrderMax ints) on the stream.
 template <int BN, int kTilesPerUnit>
-bool unit_order_launch(const PrefillParams& p, int nu, int* order, cudaStream_t stream) {
+bool unit_order_launch(const PrefillParams& p, int nu, int* order, int* counter,
+                       cudaStream_t stream) {
     static std::atomic<unsigned long long> attr_done{0};
     if (needs_setup(attr_done)) {
         if (cudaFuncSetAttribute(unit_order_kernel<BN, kTilesPerUnit>,
@@ -1276,7 +1331,7 @@ bool unit_order_launch(const PrefillParams& p, int nu, int* order, cudaStream_t 
     int n2 = 1;
     while (n2 < nu) n2 <<= 1;
     unit_order_kernel<BN, kTilesPerUnit><<<1, kOrderThreads, n2 * sizeof(unsigned long long), stream>>>(
-        p, nu, order);
+        p, nu, order, counter);
     return cudaGetLastError() == cudaSuccess;
 }
 
@@ -1307,7 +1362,7 @@ attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, con
     pp.nunits = (int)units;
     if constexpr (kPacked) {
         if (a.order && p.nqt <= kOrderMax) {
-            if (!unit_order_launch<C::BN, 1>(p, p.nqt, a.order, stream)) return ATTN_ERR_CUDA;
+            if (!unit_order_launch<C::BN, 1>(p, p.nqt, a.order, nullptr, stream)) return ATTN_ERR_CUDA;
             pp.order = a.order;
         }
     }
@@ -1345,8 +1400,11 @@ attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const 
     if constexpr (kPacked) {
         const int npairs = (p.nqt + 1) / 2;
         if (a.order && npairs <= kOrderMax) {
-            if (!unit_order_launch<C::BN, 2>(p, npairs, a.order, stream)) return ATTN_ERR_CUDA;
+            // the counter sits after the order (the scratch holds one int per query tile)
+            int* counter = p.nqt >= npairs + 1 ? a.order + npairs : nullptr;
+            if (!unit_order_launch<C::BN, 2>(p, npairs, a.order, counter, stream)) return ATTN_ERR_CUDA;
             pp.order = a.order;
+            pp.unit_counter = counter;
         }
     }
     const int grid = (int)(units < num_sms() ? units : num_sms());
@@ -1388,6 +1446,7 @@ attn_status prefill_launch_d(const PrefillArgs& a, cudaStream_t stream) {
     p.cu_k = a.cu_seqlens_k;
     p.nseq = a.nseq;
     p.order = nullptr;
+    p.unit_counter = nullptr;
     p.hq = a.hq;
     p.hkv = a.hkv;
     p.sq = a.sq;

@@ -114,11 +114,14 @@ typedef enum { ATTN_KV_BF16 = 0, ATTN_KV_E4M3 = 1 } attn_kv_dtype;
  *   prefill_workspace, prefill_workspace_bytes : packed prefill only; NULL / 0 otherwise.
  *          A DEVICE scratch buffer of at least attn_prefill_workspace_bytes(sq) bytes,
  *          4-byte aligned, owned by the caller and not read by it until the stream has
- *          passed the call.  With it, a small pass first orders the query tiles by their
- *          KV-tile count, most first, so that the persistent kernel's zig-zag hands every
- *          CTA a near-equal share when sequence lengths differ.  Results are the same with
- *          or without it (each tile is computed the same way wherever it runs); without it
- *          the tiles keep their index order.  Ignored for more than 8192 units of work.
+ *          passed the call.  With it, a small pass first writes a work order of the query
+ *          tiles.  Head_dim <= 128: grouped by sequence, most KV tiles first within one, and
+ *          the persistent CTAs draw the tiles from a counter the pass resets (kept after
+ *          the order), so the tiles in flight share one or two sequences' K/V and the CTAs
+ *          stay balanced.  Head_dim 256: ordered by KV-tile count, most first, for the
+ *          persistent kernel's fixed zig-zag.  Results are the same with or without it
+ *          (each tile is computed the same way wherever it runs); without it the tiles
+ *          keep their index order.  Ignored for more than 8192 units of work.
  */
 typedef struct {
     const float* sink;

@@ -180,9 +180,11 @@ def _tile_cost(cu_q, cu_k, sq, skv, causal, window, bm, bn, qt):
     (256, (24, 260, 100), True, 64),
 ])
 def test_work_order_is_the_units_sorted_by_kv_tiles(d, packing, causal, window, cuda_device):
-    """The work-order pass writes a permutation of the query units (pairs of 128-row tiles
-    for head_dim <= 128, single tiles for 256), KV-tile counts non-increasing, ties in index
-    order."""
+    """The work-order pass writes a permutation of the query units.  Head_dim 256 (single
+    128-row tiles, a static schedule): KV-tile counts non-increasing, ties in index order.
+    Head_dim <= 128 (pairs of tiles, handed out at run time): grouped by the sequence of the
+    unit's first row, counts non-increasing within a sequence; the counter after the order
+    was reset by the pass and drawn past the last unit by the kernel."""
     import ctypes
 
     import flash_attention_forward_attn_gb300 as A
@@ -210,5 +212,12 @@ def test_work_order_is_the_units_sorted_by_kv_tiles(d, packing, causal, window, 
                 for x in range(per)) for u in range(nu)]
     order = ws[:nu].cpu().numpy().tolist()
     assert sorted(order) == list(range(nu))
-    keys = [(-cost[u], u) for u in order]
+    if per == 2:
+        seq = [int(np.searchsorted(cu_q, min(u * per * 128, w.sq - 1), side="right") - 1)
+               for u in range(nu)]
+        keys = [(seq[u], -cost[u], u) for u in order]
+        units = nu * 4  # query-tile pairs x heads
+        assert int(ws[nu].item()) >= units  # every unit was drawn, then one failed draw per CTA
+    else:
+        keys = [(-cost[u], u) for u in order]
     assert keys == sorted(keys)
