@@ -904,65 +904,82 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
     }
 }
 
-// Merge the pieces of one (sequence, head, new token) row by log-sum-exp:
+// Merge the pieces of each (sequence, head, new token) row by log-sum-exp:
 //   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
 //   LSE = (M + log2 L) ln 2   (m_i are in log2 units of the scaled scores);
-// with a sink, the merged row is finished by finish_row (the sink joins M and L).  A row of
-// a sequence whose cache_len is out of range gets O = 0, LSE = -inf and is reported.
+// with a sink, the merged row is finished by finish_row (the sink joins M and L).  One CTA
+// per (sequence, kv head): its group * s_active rows share the piece count, and each thread
+// merges four columns of a row at a time (16-byte loads of the partials).  The rows of a
+// sequence whose cache_len is out of range get O = 0, LSE = -inf and are reported.
+constexpr int kMergeThreads = 256;
+
 template <int D, typename OutT>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const int32_t* __restrict__ cache_len,
-                                                           const float* __restrict__ part_o,
-                                                           const float* __restrict__ part_ml,
-                                                           const int* __restrict__ npieces,
-                                                           const float* __restrict__ sink,
-                                                           OutT* __restrict__ o, float* lse,
-                                                           int hq, int hkv, int s_active,
-                                                           int max_slots, int max_cache_len,
-                                                           int circular) {
-    const size_t rowid = blockIdx.x;
-    const int b = (int)(rowid / ((size_t)hq * s_active));
-    const int h = (int)((rowid / s_active) % hq);
-    const int x = threadIdx.x;
+__global__ void __launch_bounds__(kMergeThreads) decode_combine_kernel(
+    const int32_t* __restrict__ cache_len, const float* __restrict__ part_o,
+    const float* __restrict__ part_ml, const int* __restrict__ npieces,
+    const float* __restrict__ sink, OutT* __restrict__ o, float* lse, int hq, int hkv,
+    int s_active, int max_slots, int max_cache_len, int circular) {
+    const int pair = blockIdx.x;  // b * hkv + g
+    const int b = pair / hkv, g = pair % hkv;
+    const int group = hq / hkv, rows = group * s_active;
     const int len = cache_len[b];  // not written by the split kernel
     griddep_wait();                // the split kernel's partials are complete and visible
-    float out = 0.f, lse_v = -INFINITY;
-    if (len >= s_active && (circular || len <= max_cache_len)) {
-        int ns = npieces[(size_t)b * hkv + h / (hq / hkv)];
+    const bool valid = len >= s_active && (circular || len <= max_cache_len);
+    int ns = 0;
+    if (valid) {
+        ns = npieces[pair];
         if (ns < 1 || ns > max_slots) {  // cannot happen: never read past the slots
-            if (x == 0) atomicOr(&g_decode_error, kDevErrTimeout);
+            if (threadIdx.x == 0) atomicOr(&g_decode_error, kDevErrTimeout);
             ns = 0;
         }
+    } else if (threadIdx.x == 0 && g == 0) {
+        atomicOr(&g_decode_error, kDevErrCacheLen);
+    }
+    constexpr int kQ = D / 4;  // 16-byte column groups of a row
+    for (int c = threadIdx.x; c < rows * kQ; c += kMergeThreads) {
+        const int r = c / kQ, x4 = c % kQ;
+        const int h = g * group + r / s_active, t = r % s_active;
+        const size_t rowid = ((size_t)b * hq + h) * s_active + t;
         const float* ml = part_ml + rowid * max_slots * 2;
         float M = -INFINITY;
         for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
+        float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lse_v = -INFINITY;
         if (M != -INFINITY) {
-            float Lsum = 0.f, acc = 0.f;
-            const float* po = part_o + rowid * max_slots * D + x;
+            float Lsum = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4* po = reinterpret_cast<const float4*>(part_o + rowid * max_slots * D) + x4;
             for (int s = 0; s < ns; ++s) {
                 const float wt = ex2(ml[2 * s] - M);
+                const float4 v = po[(size_t)s * kQ];
                 Lsum += wt * ml[2 * s + 1];
-                acc += wt * po[(size_t)s * D];
+                acc.x += wt * v.x;
+                acc.y += wt * v.y;
+                acc.z += wt * v.z;
+                acc.w += wt * v.w;
             }
             if (sink == nullptr) {
-                out = acc / Lsum;
+                out = make_float4(acc.x / Lsum, acc.y / Lsum, acc.z / Lsum, acc.w / Lsum);
                 lse_v = (M + __log2f(Lsum)) * kLn2;
             } else {
                 float inv;
                 finish_row(true, M, Lsum, sink[h], inv, lse_v);
-                out = acc * inv;
+                out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             }
-        } else if (sink != nullptr) {  // nothing allowed: the sink alone (O = 0, LSE = sink)
+        } else if (valid && sink != nullptr) {  // nothing allowed: the sink alone (O = 0, LSE = sink)
             float inv;
             finish_row(false, 0.f, 0.f, sink[h], inv, lse_v);
         }
-    } else if (x == 0 && h == 0 && rowid % s_active == 0) {
-        atomicOr(&g_decode_error, kDevErrCacheLen);
+        if constexpr (sizeof(OutT) == 2) {
+            uint2 w;
+            w.x = pack_bf16(out.x, out.y);
+            w.y = pack_bf16(out.z, out.w);
+            *reinterpret_cast<uint2*>(o + rowid * D + 4 * x4) = w;
+        } else {
+            *reinterpret_cast<float4*>(o + rowid * D + 4 * x4) = out;
+        }
+        if (lse != nullptr && x4 == 0) lse[rowid] = lse_v;
     }
-    if constexpr (sizeof(OutT) == 2)
-        o[rowid * D + x] = __float2bfloat16_rn(out);
-    else
-        o[rowid * D + x] = out;
-    if (lse != nullptr && x == 0) lse[rowid] = lse_v;
 }
 
 // The new tokens' K and V written into a bf16 cache ("Flash-Attention: Decode (TKG)",
@@ -1121,8 +1138,8 @@ attn_status decode_launch_d(const DecodeArgs& a, cudaStream_t stream) {
     // The merge launches as a programmatic dependent of the split pass, so its launch overlaps
     // the split pass's last CTAs.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((size_t)a.b * a.hq * a.s_active));
-    cfg.blockDim = dim3(D);
+    cfg.gridDim = dim3((unsigned)((size_t)a.b * a.hkv));
+    cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
