@@ -291,7 +291,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[NS], p_full[NS], p_free[NS];
-    __shared__ uint64_t o_done, o_free, mma_drain, stats_full, stats_free;
+    // o_free[h]: the epilogue has read O's columns [h D/2, (h+1) D/2)
+    __shared__ uint64_t o_done, o_free[2], mma_drain, stats_full, stats_free;
     __shared__ uint64_t turn[2];   // S issue turns of the even and odd tiles
     __shared__ float2 stats[kBM];  // per row: the unit's running max and sum, for the epilogue
     __shared__ uint32_t tmem_base_sh;
@@ -331,7 +332,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
             mbar_init(&p_free[i], 1);
         }
         mbar_init(&o_done, 1);
-        mbar_init(&o_free, 128);
+        mbar_init(&o_free[0], 128);
+        mbar_init(&o_free[1], 128);
         mbar_init(&mma_drain, 3);
         mbar_init(&turn[0], 1);
         mbar_init(&turn[1], 1);
@@ -454,7 +456,8 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
         } else if (warp == 3) {
             // ----------------------------------------------------------- PV issuer
             // (warp-collective like the S issuers)
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
+            // P.V in two N = D/2 halves (the same products, column by column)
+            constexpr uint32_t idesc_oh = idesc_bf16_f32(kBM, D / 2, 0, 1);
             const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
             int T = 0;
             int uo = 0;  // units with tiles so far (o_free completes once per such unit)
@@ -465,10 +468,13 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
                 int bh, kvz;
                 const TileRange t = unit_at(w, bh, kvz);
                 if (t.n == 0) continue;
-                // the previous unit's epilogue must have read O before it is overwritten
+                // the previous unit's epilogue must have read each half of O before that
+                // half is overwritten: the first tile's products wait for each half apart
                 bool oko = true;
-                if (uo > 0) oko = wait_or_abort(&o_free, (uo - 1) & 1, &abort_flag);
+                if (uo > 0) oko = wait_or_abort(&o_free[0], (uo - 1) & 1, &abort_flag);
                 if (!__all_sync(0xffffffffu, oko)) break;
+                const uint32_t ofph = (uo - 1) & 1;
+                const bool wait_hi = uo > 0;
                 ++uo;
                 for (int i = 0; i < t.n; ++i, ++T) {
                     const int b = T % NS, slot = T % NV;
@@ -481,7 +487,17 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
                         tc_mma_ts_w(tmem + C::kColO, tmem + b * BN + kk * 8,
-                                    desc_add(vd, kk * 16 * 128), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                                    desc_add(vd, kk * 16 * 128), idesc_oh, (i > 0 || kk > 0) ? 1u : 0u);
+                    if (i == 0 && wait_hi) {
+                        ok = __all_sync(0xffffffffu, wait_or_abort(&o_free[1], ofph, &abort_flag));
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc_mma_ts_w(tmem + C::kColO + D / 2, tmem + b * BN + kk * 8,
+                                    desc_add(vd, (D / 2) / 64 * (BN * 128) + kk * 16 * 128), idesc_oh,
+                                    (i > 0 || kk > 0) ? 1u : 0u);
                     tc_commit_w(&p_free[b]);      // S buffer b may be rewritten; O holds PV(T)
                     tc_commit_w(&v_empty[slot]);  // V(T) consumed
                     if (i == t.n - 1) tc_commit_w(&o_done);
@@ -686,9 +702,9 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
 #pragma unroll
                     for (int e = 0; e < 64; ++e) rr[e] = 0u;
                 }
-                if (c0 + 64 == D && t.n > 0) {
+                if ((c0 + 64 == D / 2 || c0 + 64 == D) && t.n > 0) {
                     tc_fence_before();
-                    mbar_arrive(&o_free);  // O has been read: the next unit may overwrite it
+                    mbar_arrive(&o_free[c0 + 64 == D]);  // this half of O has been read
                 }
                 if (row_valid) {
                     if (p.o_f32) {
