@@ -40,6 +40,14 @@ SMALL = [
     ("paged64_d256", 2, 4, 2, 256, 2, 64, (70, 129), True, 128),
     ("paged_mha_sa16", 1, 2, 2, 128, 16, 32, (50,), True, 32),
     ("paged_len_equals_sa", 2, 4, 1, 128, 4, 32, (4, 33), True, 32),
+    # one long sequence: every CTA of the wave reads a piece of the same pair (79 pieces
+    # per pair against a bound of 80 partial slots)
+    ("one_long_seq_79_pieces", 1, 8, 2, 128, 1, 32, (20000,), True, 0),
+    # short sequences: each CTA's run crosses several pairs, so the two Q slots are reused
+    # and many pieces are shorter than the four consumer warps
+    ("short_seqs_many_pieces_per_cta", 24, 8, 2, 128, 4, 32,
+     (300, 31, 32, 64, 4, 40, 300, 17, 4, 9, 5, 32, 300, 40, 17, 33, 64, 5, 300, 17, 4, 17, 33, 31),
+     True, 256),
 ]
 
 
