@@ -585,27 +585,38 @@ def cpu_packed(pw, q, k, v, threads):
             "sample": f"2 of {pw.hq} heads x {len(rows)} packed rows, each against its sequence"}
 
 
+# Caches up to this size are copied to the host whole and the oracle decodes every
+# sequence; larger ones are sampled (the first DECODE_SAMPLE_SEQS sequences).
+DECODE_FULL_MAX_BYTES = 12 << 30
+
+
 def cpu_decode(w, t, threads, sink=None, e4m3=False, window=0, inv_freq=None):
-    """Oracle decode of the first DECODE_SAMPLE_SEQS sequences (all heads, whole caches,
-    gathered through their own compacted page table)."""
+    """Oracle decode of the whole workload (every sequence and head, the caches copied to the
+    host); for caches above DECODE_FULL_MAX_BYTES, of the first DECODE_SAMPLE_SEQS sequences
+    (all heads, whole caches, gathered through their own compacted page table)."""
     import numpy as np
     import torch
 
     import oracle
     from workloads import configs as C
 
-    n = min(DECODE_SAMPLE_SEQS, w.b)
-    lens = t["lens"][:n]
-    table = t["table"]
-    npg = [-(-int(x) // w.page_size) for x in lens]
-    pages = np.concatenate([table[b, :npg[b]] for b in range(n)]).astype(np.int64)
-    idx = torch.from_numpy(pages).to(t["k_cache"].device)
-    kc, vc = _bits(t["k_cache"][idx]), _bits(t["v_cache"][idx])
-    sub = np.full((n, w.max_pages_per_seq), 0xFFFFFFFF, dtype=np.uint32)
-    off = 0
-    for b in range(n):
-        sub[b, :npg[b]] = np.arange(off, off + npg[b], dtype=np.uint32)
-        off += npg[b]
+    cache_bytes = 2 * t["k_cache"].numel() * t["k_cache"].element_size()
+    if cache_bytes <= DECODE_FULL_MAX_BYTES:
+        n, lens, sub = w.b, t["lens"], t["table"]
+        kc, vc = _bits(t["k_cache"]), _bits(t["v_cache"])
+    else:
+        n = min(DECODE_SAMPLE_SEQS, w.b)
+        lens = t["lens"][:n]
+        table = t["table"]
+        npg = [-(-int(x) // w.page_size) for x in lens]
+        pages = np.concatenate([table[b, :npg[b]] for b in range(n)]).astype(np.int64)
+        idx = torch.from_numpy(pages).to(t["k_cache"].device)
+        kc, vc = _bits(t["k_cache"][idx]), _bits(t["v_cache"][idx])
+        sub = np.full((n, w.max_pages_per_seq), 0xFFFFFFFF, dtype=np.uint32)
+        off = 0
+        for b in range(n):
+            sub[b, :npg[b]] = np.arange(off, off + npg[b], dtype=np.uint32)
+            off += npg[b]
     qb = _bits(t["q"][:n])
     t0 = time.perf_counter()
     if e4m3:
@@ -618,11 +629,17 @@ def cpu_decode(w, t, threads, sink=None, e4m3=False, window=0, inv_freq=None):
     secs = time.perf_counter() - t0
     nbytes = C.decode_io_bytes(w.with_(b=n), lens, kv_bytes=1 if e4m3 else 2, window=window)
     rate = nbytes / secs
-    full = C.decode_io_bytes(w, t["lens"], kv_bytes=1 if e4m3 else 2, window=window)
-    return {"value": rate / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "seconds": secs, "extrapolated_full_s": full / rate,
-            "sample": (f"{n} of {w.b} sequences (cache lens {', '.join(str(int(x)) for x in lens)}),"
-                       f" all {w.hq} heads; rate over their algorithmic bytes")}
+    ent = {"value": rate / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "seconds": secs}
+    if n == w.b:
+        ent["sample"] = f"the whole workload: all {w.b} sequences and {w.hq} heads"
+    else:
+        full = C.decode_io_bytes(w, t["lens"], kv_bytes=1 if e4m3 else 2, window=window)
+        ent["extrapolated_full_s"] = full / rate
+        ent["sample"] = (f"{n} of {w.b} sequences (cache lens "
+                         f"{', '.join(str(int(x)) for x in lens)}), all {w.hq} heads; rate over "
+                         f"their algorithmic bytes")
+    return ent
 
 
 # --------------------------------------------------------------------------- main

@@ -123,8 +123,14 @@ def test_cpu_baselines_run_on_small_host_inputs(monkeypatch):
     inv = bench.rope_inv_freq(wd.d)
     for kw, tt in ((dict(), t), (dict(sink=C.sink_logits(wd.hq)), t), (dict(e4m3=True), te),
                    (dict(window=64, inv_freq=inv), t)):
+        ent = bench.cpu_decode(wd, tt, 2, **kw)  # small caches: the whole workload
+        assert ent["value"] > 0 and ent["unit"] == "GB/s" and "whole workload" in ent["sample"]
+        assert "extrapolated_full_s" not in ent
+    monkeypatch.setattr(bench, "DECODE_FULL_MAX_BYTES", 0)  # as for caches too large to copy
+    for kw, tt in ((dict(), t), (dict(e4m3=True), te), (dict(window=64, inv_freq=inv), t)):
         ent = bench.cpu_decode(wd, tt, 2, **kw)
-        assert ent["value"] > 0 and ent["unit"] == "GB/s" and "2 of 3 sequences" in ent["sample"]
+        assert ent["value"] > 0 and "2 of 3 sequences" in ent["sample"]
+        assert ent["extrapolated_full_s"] > 0
 
 
 def test_final_line_summary_is_compact():
