@@ -750,19 +750,21 @@ __global__ void __launch_bounds__(CfgW<D>::kThreads, 1) prefill_wide_kernel(
 // own producer thread; S_A, S_B, O_A, O_B fill the 512 TMEM columns and P_X is written
 // back into the first BN/2 columns of S_X as packed bf16 pairs.  A bf16 output tile is
 // staged in shared memory and written back with one TMA store per 64 columns.
-template <int D>
+template <int D, bool kQRing = false>
 struct Cfg2Q {
     static constexpr int BN = 128;
     static constexpr int kQBytes = D * kBM * 2;
     static constexpr int kSlotBytes = D * BN * 2;
     static constexpr int kKSlots = (D == 128) ? 2 : 5;
     static constexpr int kVSlots = (D == 128) ? 2 : 3;
-    static constexpr int kQAOff = 0;
-    static constexpr int kQBOff = kQBytes;
-    static constexpr int kKOff = 2 * kQBytes;
+    // Q_A and Q_B; with the Q ring also the next unit's Q_A, in the place of the bf16 O
+    // staging tile (O is then stored from registers)
+    static constexpr int kQSlots = kQRing ? 3 : 2;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQSlots * kQBytes;
     static constexpr int kVOff = kKOff + kKSlots * kSlotBytes;
     static constexpr int kOStOff = kVOff + kVSlots * kSlotBytes;  // bf16 O staging tile
-    static constexpr int kOStBytes = kBM * D * 2;
+    static constexpr int kOStBytes = kQRing ? 0 : kBM * D * 2;
     static constexpr int kSmem = kOStOff + kOStBytes;
     static constexpr int kDynBytes = kSmem + 1024;
     static constexpr int kTmemCols = 512;
@@ -776,7 +778,8 @@ struct Cfg2Q {
 // Warp 0: K producer; warp 2 (also the TMEM owner): Q and V producer (the next unit's
 // Q_A, Q_B once the current unit's last S products are done, and every unit's V tiles);
 // warps 1 / 3: MMA issuers of tile A / B; warps 4-7 / 8-11: softmax of tile A / B
-// (thread = row = TMEM lane), which also run the unit's epilogue.  Per KV tile j the
+// (thread = row = TMEM lane), which also run the unit's epilogue.  Packed sequences take
+// the Q tiles through a three-slot ring instead, loaded by the K producer (below).  Per KV tile j the
 // issuer of tile X runs  O_X += P_X(j-1) V(j-1)  then  S_X = Q_X K(j)^T, so while one
 // softmax warpgroup works on its scores the tensor pipe holds the other tile's products.
 // P_X(j-1) lives in S_X's TMEM columns; the product that reads it is issued before the one
@@ -788,14 +791,16 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
     const PrefillParams p) {
-    using C = Cfg2Q<D>;
+    constexpr bool kRing = kPacked;  // the three-slot Q ring
+    using C = Cfg2Q<D, kRing>;
     constexpr int BN = C::BN;
     constexpr int NK = C::kKSlots;
     constexpr int NV = C::kVSlots;
+    constexpr int NQ = C::kQSlots;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
+    __shared__ uint64_t q_full[NQ], q_empty[NQ], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
     __shared__ uint64_t s_full[2], p_full[2], o_done[2], o_free[2], mma_drain, stage_free;
     __shared__ uint64_t turn[2];  // MMA issue turns of tiles A and B
     __shared__ uint64_t unit_full[4], unit_empty[4];  // the ring of units drawn at run time
@@ -872,9 +877,9 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
     };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&q_full[i], 1);   // Q_A / Q_B landed
-            mbar_init(&q_empty[i], 1);  // tile A's / B's last S of the unit done
+        for (int i = 0; i < NQ; ++i) {
+            mbar_init(&q_full[i], 1);   // the slot's Q tile (Q_A / Q_B without the ring) landed
+            mbar_init(&q_empty[i], 1);  // its tile's last S product of the unit done
         }
         for (int i = 0; i < NK; ++i) {
             mbar_init(&k_full[i], 1);
@@ -918,35 +923,58 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             // K(j) streams through its own ring so it never waits behind a V slot; the V
             // producer also loads each unit's Q tiles once every S of the previous unit is
             // done (V(u0) is needed only after S(u0) and its softmax, so it can wait).
+            // With the Q ring (packed sequences) the K producer loads them, before the
+            // unit's K tiles, in load order Q_A, Q_B of each unit: load n waits only until
+            // load n - 3's tile has had its last S product, so the next unit's Q_A lands
+            // while the current unit still has K tiles to go.  Packed units are short and
+            // many: 972 -> 999 TFLOP/s on 16 sequences (A/B, bit-identical); the 32K causal
+            // prefill lost 1 % with the ring, so the fixed-head kernel keeps two slots.
             const bool is_k = warp == 0;
+            const bool loads_q = kRing ? is_k : !is_k;
             const int ns = is_k ? NK : NV;
             uint64_t* full = is_k ? k_full : v_full;
             uint64_t* empty = is_k ? k_empty : v_empty;
             const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
             uint8_t* ring = sm + (is_k ? C::kKOff : C::kVOff);
             tma_prefetch_desc(tm);
-            if (!is_k) tma_prefetch_desc(&tm_q);
+            if (loads_q) tma_prefetch_desc(&tm_q);
             int L = 0;           // tiles issued so far into this ring
-            int nq[2] = {0, 0};  // Q_A / Q_B loads issued
+            int nq[2] = {0, 0};  // Q_A / Q_B loads issued (two slots)
+            int nql = 0;         // Q tiles issued (the ring)
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int w = is_k ? draw_unit(r, ok) : read_unit(r, true, ok);
                 if (!ok || w >= p.nunits) break;
                 const Unit u = unit_at(w);
-                if (!is_k) {
-                    // Q_X is reloaded as soon as tile X's last S of the previous unit is done
-                    // (tile A's KV range ends a tile before B's, so Q_A comes back first)
-                    for (int x = 0; ok && x < (u.has_b ? 2 : 1); ++x) {
-                        if (nq[x] > 0 && !wait_or_abort(&q_empty[x], (nq[x] - 1) & 1, &abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        ++nq[x];
-                        mbar_arrive_expect_tx(&q_full[x], C::kQBytes);
+                if (loads_q) {
+                    if constexpr (kRing) {
+                        for (int x = 0; x < (u.has_b ? 2 : 1); ++x, ++nql) {
+                            const int qs = nql % NQ;
+                            if (nql >= NQ && !wait_or_abort(&q_empty[qs], ((nql / NQ) - 1) & 1, &abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
 #pragma unroll
-                        for (int dc = 0; dc < D / 64; ++dc)
-                            tma_load_3d(sm + (x ? C::kQBOff : C::kQAOff) + dc * (kBM * 128), &tm_q,
-                                        dc * 64, u.t[x].q0, u.bh, &q_full[x]);
+                            for (int dc = 0; dc < D / 64; ++dc)
+                                tma_load_3d(sm + C::kQOff + qs * C::kQBytes + dc * (kBM * 128), &tm_q,
+                                            dc * 64, u.t[x].q0, u.bh, &q_full[qs]);
+                        }
+                    } else {
+                        // Q_X is reloaded as soon as tile X's last S of the previous unit is
+                        // done (tile A's KV range ends a tile before B's, so Q_A comes back first)
+                        for (int x = 0; ok && x < (u.has_b ? 2 : 1); ++x) {
+                            if (nq[x] > 0 && !wait_or_abort(&q_empty[x], (nq[x] - 1) & 1, &abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            ++nq[x];
+                            mbar_arrive_expect_tx(&q_full[x], C::kQBytes);
+#pragma unroll
+                            for (int dc = 0; dc < D / 64; ++dc)
+                                tma_load_3d(sm + C::kQOff + x * C::kQBytes + dc * (kBM * 128), &tm_q,
+                                            dc * 64, u.t[x].q0, u.bh, &q_full[x]);
+                        }
                     }
                     if (!ok) break;
                 }
@@ -967,6 +995,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 for (int i = max(0, L - ns); i < L; ++i) wait_bounded(&full[i % ns], (i / ns) & 1);
                 for (int x = 0; x < 2; ++x)
                     if (nq[x] > 0) wait_bounded(&q_full[x], (nq[x] - 1) & 1);
+                for (int i = max(0, nql - NQ); i < nql; ++i) wait_bounded(&q_full[i % NQ], (i / NQ) & 1);
             }
         } else if (warp == 1 || warp == 3) {
             // ------------------------------------------------ MMA issuers, one per Q tile
@@ -983,7 +1012,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             const int x = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-            const uint64_t qd = sw128_desc(smem_u32(sm + (x ? C::kQBOff : C::kQAOff)), 16, 1024);
+            const uint64_t qd0 = sw128_desc(smem_u32(sm + C::kQOff), 16, 1024);
             const uint64_t kd0 = sw128_desc(smem_u32(sm + C::kKOff), 16, 1024);
             const uint64_t vd0 = sw128_desc(smem_u32(sm + C::kVOff), BN * 128, 1024);
             const uint32_t tm_sx = tmem + (x ? (uint32_t)BN : 0u);
@@ -993,7 +1022,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             int Lbase = 0;  // ring index (K and V alike) of the unit's first tile
             int cnt = 0;    // S products of this tile issued so far (phase of s/p_full)
             int turns = 0;  // turns taken so far (phase of turn[x])
-            int nq = 0;     // units with a tile X so far (phase of q_full[x])
+            int nq = 0;     // units with a tile X so far (phase of q_full[x], two slots)
+            int nql = 0;    // Q tiles of earlier units (the ring's load order: A, then B)
             int uo = 0;     // units in which tile X had products so far (phase of o_free[x])
             bool ok = true;
             for (int r = 0; ok; ++r) {
@@ -1002,10 +1032,17 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 const Unit u = unit_at(w);
                 const TileRange t = x ? u.t[1] : u.t[0];
                 const bool has_x = x == 0 || u.has_b;  // tile X exists in this unit
+                int qs = x, qpar = nq & 1;              // Q_X's slot and its phase
+                if constexpr (kRing) {
+                    qs = (nql + x) % NQ;
+                    qpar = ((nql + x) / NQ) & 1;
+                    nql += u.has_b ? 2 : 1;
+                }
+                const uint64_t qd = desc_add(qd0, (uint32_t)(qs * C::kQBytes));
                 if (has_x) {
-                    if (!__all_sync(0xffffffffu, wait_or_abort(&q_full[x], nq & 1, &abort_flag))) break;
+                    if (!__all_sync(0xffffffffu, wait_or_abort(&q_full[qs], qpar, &abort_flag))) break;
                     ++nq;
-                    if (t.n == 0) tc_commit_w(&q_empty[x]);  // no product will read Q_X
+                    if (t.n == 0) tc_commit_w(&q_empty[qs]);  // no product will read Q_X
                 }
                 // O_X may be overwritten once the epilogue has read out the previous unit
                 // in which tile X had products (o_free completes once per such unit, so it
@@ -1069,7 +1106,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                         if (in_k) tc_commit_w(&k_empty[ks]);
                         else mbar_arrive_w(&k_empty[ks]);
                     }
-                    if (in_k && j == t.kt0 + t.n - 1) tc_commit_w(&q_empty[x]);  // last S of tile X
+                    if (in_k && j == t.kt0 + t.n - 1) tc_commit_w(&q_empty[qs]);  // last S of tile X
                 }
                 if (t.n > 0) ++uo;
                 Lbase += nu;
@@ -1250,7 +1287,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             if (!p.o_f32) {
                 // bf16: O_X -> registers (then O_X is free), scale, stage in shared memory in
                 // the 128-byte-swizzled box layout, and one thread stores the boxes with TMA
-                // (rows past sq are clipped by the store).
+                // (rows past sq are clipped by the store).  With the Q ring there is no
+                // staging tile: each thread stores its row (rows past sq are not stored).
                 uint32_t ob[D / 2];
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -1268,7 +1306,14 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 }
                 tc_fence_before();
                 if (t.n > 0) mbar_arrive(ofree);  // O_X read out: the next unit may overwrite it
-                if (t.rows > 0) {
+                if constexpr (kRing) {
+                    if (row_valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D);
+#pragma unroll
+                        for (int ch = 0; ch < D / 8; ++ch)
+                            dst[ch] = make_uint4(ob[4 * ch], ob[4 * ch + 1], ob[4 * ch + 2], ob[4 * ch + 3]);
+                    }
+                } else if (t.rows > 0) {
                     if (eidx > 0) ok = wait_or_abort(&stage_free, (eidx - 1) & 1, &abort_flag) && ok;
                     uint8_t* st = sm + C::kOStOff;
 #pragma unroll
@@ -1401,7 +1446,7 @@ attn_status prefill_wide_launch(const PrefillArgs& a, const CUtensorMap& tq, con
 template <int D, bool kPacked>
 attn_status prefill2q_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, const PrefillParams& p, cudaStream_t stream) {
-    using C = Cfg2Q<D>;
+    using C = Cfg2Q<D, kPacked>;
     static std::atomic<unsigned long long> attr_done{0};
     if (needs_setup(attr_done)) {
         if (cudaFuncSetAttribute(prefill2q_kernel<D, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
