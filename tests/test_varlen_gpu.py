@@ -55,6 +55,10 @@ CASES = [
     ("many_prefixed_d128_w", (30, 150, 400), None, 4, 2, 128, True, 100, torch.float32),
     ("many_seqs_d256", (24, 200, 100), None, 4, 2, 256, True, 0, torch.float32),
     ("many_seqs_d64_multi_unit", (60, 300, 64), None, 40, 8, 64, True, 0, torch.bfloat16),
+    # 27 query tiles (the last pair has tile A only) and 560 units, so CTAs run three or four
+    # units each: the packed kernel's three-slot Q ring wraps, and the tile-A-only units
+    # shift its slot order
+    ("d128_ring_wraps_tile_a_only", (50, 128, 60), None, 40, 8, 128, True, 0, torch.bfloat16),
 ]
 
 
