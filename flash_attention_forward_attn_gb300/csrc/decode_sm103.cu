@@ -262,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
     __shared__ PieceInfo info[2];
     __shared__ float m_sh[kConsumers][16], l_sh[kConsumers][16];
     __shared__ float inv_freq[D / 2];  // RoPE inverse frequencies (producer only)
+    // head_dim 256: row r's new token (r mod s_active), which the masked tiles read here
+    // rather than keep in registers; the consumers sit at the 255-register ceiling there, and
+    // this is what keeps them from spilling (8 bytes with the tokens in registers)
+    __shared__ int row_tok[16];
     __shared__ int abort_flag;
 
     // The merge kernel is launched as this grid's programmatic dependent: it may take free
@@ -274,6 +278,8 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
     const bool v0 = r0 < p.rows, v1 = r1 < p.rows;
     const int t0 = r0 % p.s_active, t1 = r1 % p.s_active;
 
+    if constexpr (D > 128)
+        if (threadIdx.x < 16) row_tok[threadIdx.x] = (int)threadIdx.x % p.s_active;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -660,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, DecodeLayout<D, kE4M3>::kMinCtas) de
                             const int r = j0 + nt * 8 + 2 * qd + e;  // slot
                             const int j = p.circular ? circular_pos(r, len, p.max_cache_len) : r;
                             const bool in = r < nslots;
-                            if (!(v0 && in && decode_allowed_w(j, len, p.s_active, t0, p.window))) x0 = -INFINITY;
-                            if (!(v1 && in && decode_allowed_w(j, len, p.s_active, t1, p.window))) x1 = -INFINITY;
+                            const int u0 = D > 128 ? row_tok[r0] : t0, u1 = D > 128 ? row_tok[r1] : t1;
+                            if (!(v0 && in && decode_allowed_w(j, len, p.s_active, u0, p.window))) x0 = -INFINITY;
+                            if (!(v1 && in && decode_allowed_w(j, len, p.s_active, u1, p.window))) x1 = -INFINITY;
                         }
                         sc[nt][e] = x0;
                         sc[nt][2 + e] = x1;
