@@ -929,6 +929,11 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             // while the current unit still has K tiles to go.  Packed units are short and
             // many: 972 -> 999 TFLOP/s on 16 sequences (A/B, bit-identical); the 32K causal
             // prefill lost 1 % with the ring, so the fixed-head kernel keeps two slots.
+            // Only tiles with KV tiles get a Q load.  An issuer waits on a ring slot by
+            // phase parity, which is sound only once the slot's previous load has landed;
+            // when that load was the other tile's, the turns both issuers take in its unit
+            // order this wait after the other issuer's, and a unit takes turns only when
+            // one of its tiles has products.
             const bool is_k = warp == 0;
             const bool loads_q = kRing ? is_k : !is_k;
             const int ns = is_k ? NK : NV;
@@ -948,7 +953,8 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 const Unit u = unit_at(w);
                 if (loads_q) {
                     if constexpr (kRing) {
-                        for (int x = 0; x < (u.has_b ? 2 : 1); ++x, ++nql) {
+                        for (int x = 0; x < (u.has_b ? 2 : 1); ++x) {
+                            if (u.t[x].n == 0) continue;  // no product reads this tile's Q
                             const int qs = nql % NQ;
                             if (nql >= NQ && !wait_or_abort(&q_empty[qs], ((nql / NQ) - 1) & 1, &abort_flag)) {
                                 ok = false;
@@ -959,6 +965,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                             for (int dc = 0; dc < D / 64; ++dc)
                                 tma_load_3d(sm + C::kQOff + qs * C::kQBytes + dc * (kBM * 128), &tm_q,
                                             dc * 64, u.t[x].q0, u.bh, &q_full[qs]);
+                            ++nql;
                         }
                     } else {
                         // Q_X is reloaded as soon as tile X's last S of the previous unit is
@@ -1023,7 +1030,7 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
             int cnt = 0;    // S products of this tile issued so far (phase of s/p_full)
             int turns = 0;  // turns taken so far (phase of turn[x])
             int nq = 0;     // units with a tile X so far (phase of q_full[x], two slots)
-            int nql = 0;    // Q tiles of earlier units (the ring's load order: A, then B)
+            int nql = 0;    // Q loads of earlier units (the ring's load order: A, then B)
             int uo = 0;     // units in which tile X had products so far (phase of o_free[x])
             bool ok = true;
             for (int r = 0; ok; ++r) {
@@ -1033,16 +1040,21 @@ __global__ void __launch_bounds__(384, 1) prefill2q_kernel(
                 const TileRange t = x ? u.t[1] : u.t[0];
                 const bool has_x = x == 0 || u.has_b;  // tile X exists in this unit
                 int qs = x, qpar = nq & 1;              // Q_X's slot and its phase
+                bool wait_q = has_x;                    // Q_X has a load to wait for
                 if constexpr (kRing) {
-                    qs = (nql + x) % NQ;
-                    qpar = ((nql + x) / NQ) & 1;
-                    nql += u.has_b ? 2 : 1;
+                    // the ring loads Q only for tiles with KV tiles
+                    const bool load_a = u.t[0].n > 0, load_b = u.has_b && u.t[1].n > 0;
+                    const int nqx = nql + ((x == 1 && load_a) ? 1 : 0);
+                    qs = nqx % NQ;
+                    qpar = (nqx / NQ) & 1;
+                    wait_q = x ? load_b : load_a;
+                    nql += (load_a ? 1 : 0) + (load_b ? 1 : 0);
                 }
                 const uint64_t qd = desc_add(qd0, (uint32_t)(qs * C::kQBytes));
-                if (has_x) {
+                if (wait_q) {
                     if (!__all_sync(0xffffffffu, wait_or_abort(&q_full[qs], qpar, &abort_flag))) break;
                     ++nq;
-                    if (t.n == 0) tc_commit_w(&q_empty[qs]);  // no product will read Q_X
+                    if (!kRing && t.n == 0) tc_commit_w(&q_empty[qs]);  // no product will read Q_X
                 }
                 // O_X may be overwritten once the epilogue has read out the previous unit
                 // in which tile X had products (o_free completes once per such unit, so it

@@ -59,6 +59,10 @@ CASES = [
     # units each: the packed kernel's three-slot Q ring wraps, and the tile-A-only units
     # shift its slot order
     ("d128_ring_wraps_tile_a_only", (50, 128, 60), None, 40, 8, 128, True, 0, torch.bfloat16),
+    # a sequence of 600 queries and no keys: the first two units of every head have no KV
+    # tile at all (no Q load in the ring, no MMA turns), 128 of them among 256 units, so
+    # CTAs run them back to back before units with work
+    ("d128_keyless_units", [0, 600, 1024], [0, 0, 424], 64, 16, 128, True, 0, torch.bfloat16),
 ]
 
 
