@@ -13,52 +13,13 @@ present or not, tiles with and without KV tiles) and random load, product and is
 for the protocol the kernel uses: a Q load only for tiles that have KV tiles.  It also checks
 that the model finds the race in the earlier protocol, which loaded Q for every tile, so that
 a run of units without KV tiles took no turns to order one issuer's wait after the other's."""
-import heapq
 import random
 
 import pytest
 
+from tests.event_sim import Sim
+
 NQ = 3
-
-
-class Sim:
-    """Actors are generators that yield ("until", predicate) or ("sleep", dt); timed
-    callbacks (a load landing, a product completing) run from the same event queue."""
-
-    def __init__(self, rng):
-        self.rng, self.now, self.seq, self.q = rng, 0.0, 0, []
-        self.blocked = []  # (predicate, actor)
-
-    def at(self, t, fn):
-        self.seq += 1
-        heapq.heappush(self.q, (t, self.seq, fn))
-
-    def start(self, actor):
-        self.at(self.now, lambda: self.step(actor))
-
-    def step(self, actor):
-        try:
-            kind, arg = next(actor)
-        except StopIteration:
-            return
-        if kind == "sleep":
-            self.at(self.now + arg, lambda: self.step(actor))
-        elif arg():
-            self.at(self.now + self.rng.uniform(0.0, 0.05), lambda: self.step(actor))
-        else:
-            self.blocked.append((arg, actor))
-
-    def run(self, limit=500000):
-        for _ in range(limit):
-            if not self.q:
-                return
-            self.now, _, fn = heapq.heappop(self.q)
-            fn()
-            ready = [(p, a) for p, a in self.blocked if p()]
-            self.blocked = [(p, a) for p, a in self.blocked if not p()]
-            for _, a in ready:  # wake-up latency
-                self.at(self.now + self.rng.uniform(0.0, 0.05), lambda a=a: self.step(a))
-        raise AssertionError("the model did not finish")
 
 
 def simulate(units, rng, load_all_tiles):
